@@ -1,0 +1,348 @@
+"""Benchmark of the IQ hot path on B300.
+
+Workload (the pages' encode-speed configuration): one 5632 x 2048 bf16 weight (Student-t nu=4 x
+0.02), importance from 4096 x 2048 bf16 activations with log-normal column scales, seeded synthetic
+codebooks.  One step = the whole hot path over that batch:
+  imatrix accumulation (1024-row chunks) -> importance weights -> for each of the five formats:
+  searched encode with the every-choice error table (anchor fused) + fixed-choice encode (choice 7
+  everywhere) + decode of the searched payload (fp32).
+value = 5 * 5632 * 2048 weight elements / step time (M elem/s; each element goes through the full
+path once per format).  Per-kernel CUDA-event times give per-format encode M elem/s, decode and
+imatrix GB/s and the roofline of the dominant kernel.
+
+--impl reference times the plain C oracle (the CPU definition of the same path) on a bounded row
+sample of the same workload on this host's cores.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "IQ encode M elem/s per format on 5632x2048 (+% FP32 roofline); imatrix/decode GB/s"
+R, C = 5632, 2048
+T_ACT = 4096
+FORMATS = ("IQ2_XXS", "IQ2_XS", "IQ2_S", "IQ1_S", "IQ1_M")
+ENTRIES = {"IQ2_XXS": 256, "IQ2_XS": 512, "IQ2_S": 1024, "IQ1_S": 2048, "IQ1_M": 2048}
+BPW = {"IQ2_XXS": 2.0625, "IQ2_XS": 2.3125, "IQ2_S": 2.5625, "IQ1_S": 1.5625, "IQ1_M": 1.75}
+CONFIG = {"workload": "encode 5632x2048 bf16 weight in IQ2_XXS/IQ2_XS/IQ2_S/IQ1_S/IQ1_M (searched + every-choice "
+                      "table, fixed choice 7, decode) with importance from a 4096x2048 bf16 imatrix pass",
+          "rows": R, "cols": C, "activation_rows": T_ACT, "rows_per_chunk": 1024,
+          "l2": "flushed before every timed step (512 MiB write); inputs 23 MiB + 16 MiB < L2"}
+
+
+def flops_per_element(fmt):
+    """Algorithmic FP32 work of the searched encode per weight element: per codebook entry and
+    8-value vector, IQ2 16 FMA for (A, B) + 16 choices x (FMA + min) = 80 flops; IQ1 24 FMA +
+    4 shifted-form FMA + 16 x (FMA + min) = 104 flops (FMA = 2, min = 1)."""
+    return (10 if fmt.startswith("IQ2") else 13) * ENTRIES[fmt]
+
+
+def fp32_peak_tflops(sms, mhz):
+    return sms * 128 * 2 * mhz * 1e6 / 1e12
+
+
+def inputs():
+    from ggml_iq_codebook_accumulate_b300 import synth
+    Wst, Wv = synth.as_dtype(synth.weight_t4(R, C, seed=1), "bf16")
+    Xst, Xv = synth.as_dtype(synth.activations(T_ACT, C, seed=1), "bf16")
+    grids = {f: synth.grid(f) for f in FORMATS}
+    return Wst, Wv, Xst, Xv, grids
+
+
+# ----------------------------------------------------------------------------------------------
+def run_reference(args):
+    """The oracle (plain C, fp64 direct-form search, OpenMP over blocks) on a bounded row sample."""
+    import oracle
+    oracle.build()
+    Wst, Wv, Xst, Xv, grids = inputs()
+    rows = int(os.environ.get("IQ_REF_ROWS", "16"))
+    ids = np.zeros((T_ACT, 1), np.int32)
+
+    def step():
+        s2, cn, _ = oracle.imatrix_accumulate(Xv, ids, 1)
+        w = oracle.imatrix_weights(s2, cn)[0]
+        for f in FORMATS:
+            p, _ = oracle.encode(f, Wv[:rows], grids[f], importance=w)
+            ch = np.full((rows * C // 256, oracle.format_info(f)["groups"]), 7, np.uint8)
+            oracle.encode(f, Wv[:rows], grids[f], importance=w, choices=ch)
+            oracle.decode(f, p, rows, C, grids[f])
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 5 * rows * C / dt / 1e6
+    cores = os.cpu_count()
+    sample = (f"{rows} of {R} rows per format (searched + fixed-choice encode, decode) plus the full "
+              f"{T_ACT}x{C} imatrix pass, per step")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "M elem/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": CONFIG,
+            "cpu_baseline": {"value": round(value, 4), "unit": "M elem/s", "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "M elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def cpu_baseline_sample(Wv, Xv, grids, budget_rows=16):
+    import oracle
+    oracle.build()
+    ids = np.zeros((T_ACT, 1), np.int32)
+    t0 = time.perf_counter()
+    s2, cn, _ = oracle.imatrix_accumulate(Xv, ids, 1)
+    w = oracle.imatrix_weights(s2, cn)[0]
+    for f in FORMATS:
+        p, _ = oracle.encode(f, Wv[:budget_rows], grids[f], importance=w)
+        ch = np.full((budget_rows * C // 256, oracle.format_info(f)["groups"]), 7, np.uint8)
+        oracle.encode(f, Wv[:budget_rows], grids[f], importance=w, choices=ch)
+        oracle.decode(f, p, budget_rows, C, grids[f])
+    dt = time.perf_counter() - t0
+    return {"value": round(5 * budget_rows * C / dt / 1e6, 4), "unit": "M elem/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": f"one step on {budget_rows} of {R} rows per format (searched + fixed encode, decode) plus the "
+                      f"full {T_ACT}x{C} imatrix pass; {dt:.1f} s"}
+
+
+# ----------------------------------------------------------------------------------------------
+class Clocks:
+    def __init__(self):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+        dev = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0] or "0"
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", dev, f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                       "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.p:
+            self.p.terminate()
+            self.p.wait()
+
+    def summary(self):
+        self.f.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1])); mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_ours(args):
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    api.lib()
+    Wst, Wv, Xst, Xv, grids = inputs()
+
+    def to_dev(store):
+        return torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    W = to_dev(Wst)
+    X = to_dev(Xst)
+    G = {f: torch.from_numpy(grids[f]).to(dev) for f in FORMATS}
+    ids = torch.zeros(T_ACT, 1, dtype=torch.int32, device=dev)
+    s2 = torch.zeros(1, C, dtype=torch.float32, device=dev)
+    cn = torch.zeros(1, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    B = R * C // 256
+    info = {f: api.format_info(f) for f in FORMATS}
+    pay = {f: torch.empty(B, info[f]["block_bytes"], dtype=torch.uint8, device=dev) for f in FORMATS}
+    pay7 = {f: torch.empty_like(pay[f]) for f in FORMATS}
+    tbl = {f: torch.empty(B, info[f]["choice_groups"], info[f]["num_choices"], dtype=torch.float32, device=dev)
+           for f in FORMATS}
+    ch7 = {f: torch.full((B, info[f]["choice_groups"]), 7, dtype=torch.uint8, device=dev) for f in FORMATS}
+    dec = torch.empty(R, C, dtype=torch.float32, device=dev)
+    ws = {f: api.encode_workspace(f, R, C, dev) for f in FORMATS}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    names = ["imatrix", "weights"] + [f"{k}:{f}" for f in FORMATS for k in ("encode", "fixed", "decode")]
+
+    def step(evs=None):
+        def mark(i):
+            if evs is not None:
+                evs[i].record(stream)
+        mark(0)
+        s2.zero_(); cn.zero_()
+        api.imatrix_accumulate(X, ids, 1, 1024, s2, cn, status=st)
+        mark(1)
+        w = api.imatrix_weights(s2, cn)
+        mark(2)
+        i = 2
+        for f in FORMATS:
+            api.encode(f, W, G[f], importance=w[0], status=st, payload=pay[f], table=tbl[f], every_choice=True,
+                       workspace=ws[f])
+            mark(i + 1)
+            api.encode(f, W, G[f], importance=w[0], choices=ch7[f], status=st, payload=pay7[f], workspace=ws[f])
+            mark(i + 2)
+            api.decode(f, pay[f], R, C, G[f], out=dec)
+            mark(i + 3)
+            i += 3
+
+    nev = 2 + 3 * len(FORMATS) + 1
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    per = {n: [] for n in names}
+    totals = []
+    with Clocks() as clk:
+        torch.cuda.synchronize()
+        for _ in range(args.steps):
+            flush.fill_(1)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
+            step(evs)
+            torch.cuda.synchronize()
+            for k, n in enumerate(names):
+                per[n].append(evs[k].elapsed_time(evs[k + 1]))
+            totals.append(evs[0].elapsed_time(evs[-1]))
+        torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = float(np.mean(totals))
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    if rank != 0:
+        return
+    clocks = clk.summary()
+    value = world * 5 * R * C / (ms * 1e-3) / 1e6
+    # per-kernel figures
+    pf = {}
+    for f in FORMATS:
+        e_ms = float(np.mean(per[f"encode:{f}"]))
+        x_ms = float(np.mean(per[f"fixed:{f}"]))
+        d_ms = float(np.mean(per[f"decode:{f}"]))
+        dec_bytes = R * C * (BPW[f] / 8 + 4) + ENTRIES[f] * 32
+        pf[f] = {"encode_searched_Melem_s": round(R * C / (e_ms * 1e-3) / 1e6, 1),
+                 "encode_fixed_Melem_s": round(R * C / (x_ms * 1e-3) / 1e6, 1),
+                 "decode_GB_s": round(dec_bytes / (d_ms * 1e-3) / 1e9, 1),
+                 "encode_ms": round(e_ms, 4), "fixed_ms": round(x_ms, 4), "decode_ms": round(d_ms, 4)}
+    im_ms = float(np.mean(per["imatrix"]))
+    im_bytes = T_ACT * C * 2 + T_ACT * 4 + 2 * C * 4
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    dom = max(FORMATS, key=lambda f: pf[f]["encode_ms"])
+    dom_ms = pf[dom]["encode_ms"]
+    achieved = R * C * flops_per_element(dom) / (dom_ms * 1e-3) / 1e12
+    peak = fp32_peak_tflops(sms, 2032.0)
+    prof_traffic = None
+    roofline = {"kernel": f"encode (searched + every-choice table) {dom}", "bound": "alu",
+                "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
+                "frac": round(achieved / peak, 4), "traffic": prof_traffic,
+                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flops x 2032 MHz (max SM clock)"}
+    if clocks.get("sm_mhz"):
+        roofline["frac_at_observed_clock"] = round(achieved / fp32_peak_tflops(sms, clocks["sm_mhz"]), 4)
+    # end to end through the public API with host buffers
+    e2e = measure_e2e(args, dev, Wst, Xst, grids, G, ids, info)
+    launches = args.steps * (3 + 5 * (3 + 3 + 1))
+    cpu = cpu_baseline_sample(Wv, Xv, grids) if world == 1 or rank == 0 else None
+    line = {"metric": METRIC, "value": round(value, 2), "unit": "M elem/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": CONFIG,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
+            "per_format": pf,
+            "imatrix": {"ms": round(im_ms, 4), "GB_s": round(im_bytes / (im_ms * 1e-3) / 1e9, 1)}}
+    print(json.dumps(line))
+
+
+def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
+    """The same step through the public API with host inputs: pinned host -> device copies of the
+    weight and activations, and device -> host copies of the five searched payloads, timed."""
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api
+    Wh = torch.from_numpy(np.ascontiguousarray(Wst).view(np.int16)).view(torch.bfloat16).pin_memory()
+    Xh = torch.from_numpy(np.ascontiguousarray(Xst).view(np.int16)).view(torch.bfloat16).pin_memory()
+    B = R * C // 256
+    outs = {f: torch.empty(B, info[f]["block_bytes"], dtype=torch.uint8).pin_memory() for f in FORMATS}
+    W = torch.empty(R, C, dtype=torch.bfloat16, device=dev)
+    X = torch.empty(T_ACT, C, dtype=torch.bfloat16, device=dev)
+    ch7 = {f: torch.full((B, info[f]["choice_groups"]), 7, dtype=torch.uint8, device=dev) for f in FORMATS}
+
+    def step():
+        W.copy_(Wh, non_blocking=True)
+        X.copy_(Xh, non_blocking=True)
+        s2, cn = api.imatrix_accumulate(X, ids, 1, 1024)
+        w = api.imatrix_weights(s2, cn)
+        for f in FORMATS:
+            p, t = api.encode(f, W, G[f], importance=w[0], every_choice=True)
+            api.encode(f, W, G[f], importance=w[0], choices=ch7[f])
+            api.decode(f, p, R, C, G[f])
+            outs[f].copy_(p, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(2):
+        step()
+    t0 = time.perf_counter()
+    n = max(1, args.steps)
+    for _ in range(n):
+        step()
+    dt = (time.perf_counter() - t0) / n
+    h2d = Wh.numel() * 2 + Xh.numel() * 2
+    d2h = sum(o.numel() for o in outs.values())
+    return {"value": round(5 * R * C / dt / 1e6, 2), "unit": "M elem/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    args = ap.parse_args()
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        run_reference(args)
+        return
+    run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

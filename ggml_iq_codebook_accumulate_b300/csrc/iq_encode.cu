@@ -1,0 +1,818 @@
+// Importance-weighted codebook encoder for the GGML IQ formats, its every-choice error table and
+// the super-block anchor.
+//
+// Sources: PR #2513 (IQ2_XXS / IQ2_S / IQ1_M commit texts: single-pass grid search at a fixed
+// anchored super-block scale, even-parity sign rule, full sign mask for IQ2_S, +-1/8 shift for IQ1,
+// tie order (lower shift, then lower entry), anchors); PR #3157 "[1/5] Let the GGML IQ encoders take
+// fixed per-group choices" (one choice per group by least weighted squared error, fixed choices keep
+// the entry search, choices in [0, num_choices), zero blocks); PR #3159 (every choice from one
+// sweep).
+//
+// Work layout: one warp per 256-value block, lane g = vector g (8 values).  The codebook, prepared
+// as [entry][g(8) | g^2 or |g| (8)] fp32, is copied once per CTA into dynamic shared memory with a
+// bulk async copy (TMA engine, mbarrier completion) and read as warp-wide broadcasts.
+//
+// For vector v with weights w, targets t (signed magnitudes for IQ2, x for IQ1) and a candidate
+// (entry e [, shift delta]) under local scale alpha, the error is
+//     E = sum w (t - alpha u)^2 = Cs + alpha * s,   s = alpha * B - 2 A,
+// with u = g (IQ2) or g + delta (IQ1), A = sum w t u, B = sum w u^2, Cs = sum w t^2.  The sweep
+// computes A and B once per entry (FMA chains) and s for every choice (one FMA + one min each), so
+// per (vector, choice) it keeps min_e s.  The group's choice minimises alpha * sum_v min s; the
+// vector's candidate under that choice is found by a second sweep at one alpha.
+//
+// Exactness: every decision the fp32 sweep makes with a gap larger than its rounding bound
+// (kMargin, see iq_common.cuh) equals the exact decision.  Smaller gaps are flagged per block; a
+// second kernel rescores the flagged groups: it screens candidates in fp32 and evaluates every
+// candidate the bound cannot exclude with the direct fp64 form sum_i w_i (x_i - q_i)^2 of the
+// decoded values q, then takes the exact minimum with the lowest (choice) / (delta bit, entry) on
+// equal error.
+#include "iq_common.cuh"
+
+namespace iqk {
+
+enum { MODE_SEARCH = 0, MODE_FIXED = 1, MODE_TABLE = 2 };
+
+__host__ __device__ inline size_t al256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+struct EncWs {
+  int32_t *hdr;  // [0] codebook invalid, [1] number of flagged blocks
+  float4 *tab;   // [N][4] prepared codebook
+  uint2 *fb;     // [B] flagged blocks: (block index, vector mask)
+};
+__host__ __device__ inline EncWs enc_ws(void *ws, int N) {
+  uint8_t *p = (uint8_t *)ws;
+  EncWs r;
+  r.hdr = (int32_t *)p; p += 256;
+  r.tab = (float4 *)p; p += al256((size_t)N * 64);
+  r.fb = (uint2 *)p;
+  return r;
+}
+static size_t enc_ws_bytes(int N, int64_t nblocks) { return 256 + al256((size_t)N * 64) + al256((size_t)nblocks * 8); }
+
+struct EncArgs {
+  const void *W;
+  int64_t rows, cols, nblocks;
+  const float *imp;
+  int64_t rows_per_expert;
+  const float *grid;
+  const uint16_t *d16;
+  const uint8_t *choices;
+  uint8_t *payload;
+  float *table;
+  int32_t *status;
+};
+
+// ---------------------------------------------------------------------------------------------
+template <int F>
+__global__ void prep_codebook(const float *__restrict__ grid, EncWs ws) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= Fmt<F>::N) return;
+  float g[8];
+  load8(grid + 8 * e, g);
+  bool ok = true;
+  float h[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    if (Fmt<F>::IQ1) {
+      ok &= (g[i] == -1.0f || g[i] == 0.0f || g[i] == 1.0f);
+      h[i] = fabsf(g[i]);
+    } else {
+      ok &= (g[i] >= 1.0f && g[i] <= 127.0f && g[i] == floorf(g[i]));
+      h[i] = g[i] * g[i];
+    }
+  }
+  if (!ok) atomicOr(&ws.hdr[0], 1);
+  ws.tab[4 * e + 0] = make_float4(g[0], g[1], g[2], g[3]);
+  ws.tab[4 * e + 1] = make_float4(g[4], g[5], g[6], g[7]);
+  ws.tab[4 * e + 2] = make_float4(h[0], h[1], h[2], h[3]);
+  ws.tab[4 * e + 3] = make_float4(h[4], h[5], h[6], h[7]);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Per-vector state.
+struct Vec {
+  float x[8], w[8];
+  float nw2[8];  // -2 * w * t (exact scaling of the rounded product w*t)
+  float Cs;      // sum w t^2 (fp32, only for the rounding bound)
+  float nT2;     // sum of nw2 (IQ1)
+  float Ws;      // sum of w (IQ1)
+  int sgn;       // IQ2 sign mask
+};
+
+template <int F>
+__device__ __forceinline__ void vec_setup(Vec &v) {
+  float t[8];
+  if (!Fmt<F>::IQ1) {
+    v.sgn = sign_rule<F>(v.x, v.w, t);
+  } else {
+    v.sgn = 0;
+#pragma unroll
+    for (int i = 0; i < 8; i++) t[i] = v.x[i];
+  }
+  float cs = 0.0f, nt = 0.0f, ws = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    const float wt = __fmul_rn(v.w[i], t[i]);
+    v.nw2[i] = -2.0f * wt;
+    cs = __fmaf_rn(wt, t[i], cs);
+    nt = __fadd_rn(nt, v.nw2[i]);
+    ws = __fadd_rn(ws, v.w[i]);
+  }
+  v.Cs = cs; v.nT2 = nt; v.Ws = ws;
+}
+
+// A and B of one codebook entry (IQ2): An = -2 A, B = sum w g^2.
+__device__ __forceinline__ void ab2(const float *nw2, const float *w, const float4 *te, float &An, float &B) {
+  const float4 g0 = te[0], g1 = te[1], q0 = te[2], q1 = te[3];
+  An = __fmul_rn(nw2[0], g0.x);
+  An = __fmaf_rn(nw2[1], g0.y, An); An = __fmaf_rn(nw2[2], g0.z, An); An = __fmaf_rn(nw2[3], g0.w, An);
+  An = __fmaf_rn(nw2[4], g1.x, An); An = __fmaf_rn(nw2[5], g1.y, An); An = __fmaf_rn(nw2[6], g1.z, An);
+  An = __fmaf_rn(nw2[7], g1.w, An);
+  B = __fmul_rn(w[0], q0.x);
+  B = __fmaf_rn(w[1], q0.y, B); B = __fmaf_rn(w[2], q0.z, B); B = __fmaf_rn(w[3], q0.w, B);
+  B = __fmaf_rn(w[4], q1.x, B); B = __fmaf_rn(w[5], q1.y, B); B = __fmaf_rn(w[6], q1.z, B);
+  B = __fmaf_rn(w[7], q1.w, B);
+}
+// IQ1: shifted sums for delta = +1/8 (p) and -1/8 (m).
+__device__ __forceinline__ void ab1(const Vec &v, const float4 *te, float &Anp, float &Bp, float &Anm, float &Bm) {
+  const float4 g0 = te[0], g1 = te[1], a0 = te[2], a1 = te[3];
+  float An = __fmul_rn(v.nw2[0], g0.x);
+  An = __fmaf_rn(v.nw2[1], g0.y, An); An = __fmaf_rn(v.nw2[2], g0.z, An); An = __fmaf_rn(v.nw2[3], g0.w, An);
+  An = __fmaf_rn(v.nw2[4], g1.x, An); An = __fmaf_rn(v.nw2[5], g1.y, An); An = __fmaf_rn(v.nw2[6], g1.z, An);
+  An = __fmaf_rn(v.nw2[7], g1.w, An);
+  float Cg = __fmul_rn(v.w[0], g0.x);
+  Cg = __fmaf_rn(v.w[1], g0.y, Cg); Cg = __fmaf_rn(v.w[2], g0.z, Cg); Cg = __fmaf_rn(v.w[3], g0.w, Cg);
+  Cg = __fmaf_rn(v.w[4], g1.x, Cg); Cg = __fmaf_rn(v.w[5], g1.y, Cg); Cg = __fmaf_rn(v.w[6], g1.z, Cg);
+  Cg = __fmaf_rn(v.w[7], g1.w, Cg);
+  float B = __fmul_rn(v.w[0], a0.x);
+  B = __fmaf_rn(v.w[1], a0.y, B); B = __fmaf_rn(v.w[2], a0.z, B); B = __fmaf_rn(v.w[3], a0.w, B);
+  B = __fmaf_rn(v.w[4], a1.x, B); B = __fmaf_rn(v.w[5], a1.y, B); B = __fmaf_rn(v.w[6], a1.z, B);
+  B = __fmaf_rn(v.w[7], a1.w, B);
+  Anp = __fmaf_rn(0.125f, v.nT2, An);
+  Anm = __fmaf_rn(-0.125f, v.nT2, An);
+  const float Bw = __fmaf_rn(0.015625f, v.Ws, B);
+  Bp = __fmaf_rn(0.25f, Cg, Bw);
+  Bm = __fmaf_rn(-0.25f, Cg, Bw);
+}
+
+// local scale multipliers: IQ2 alpha_s = d * (2s+1) / 8, IQ1 alpha_s = d * (2s+1) (both exact)
+template <int F> __device__ __forceinline__ float alpha_of(float d, int s) {
+  return Fmt<F>::IQ1 ? __fmul_rn(d, (float)(2 * s + 1)) : __fmul_rn(__fmul_rn(d, (float)(2 * s + 1)), 0.125f);
+}
+// alpha of choice c (IQ1_S: scale = c & 7)
+template <int F> __device__ __forceinline__ float alpha_choice(float d, int c) {
+  return alpha_of<F>(d, F == IQ1_S ? (c & 7) : c);
+}
+
+// Sweep 1: per choice, the minimum over the vector's candidates of the scaled score s.
+template <int F>
+__device__ __forceinline__ void sweep_minima(const Vec &v, const float4 *tab, const float *al, float *m) {
+  constexpr int C = Fmt<F>::C, N = Fmt<F>::N;
+#pragma unroll
+  for (int c = 0; c < C; c++) m[c] = INFINITY;
+#pragma unroll 2
+  for (int e = 0; e < N; e++) {
+    const float4 *te = tab + 4 * e;
+    if (!Fmt<F>::IQ1) {
+      float An, B;
+      ab2(v.nw2, v.w, te, An, B);
+#pragma unroll
+      for (int c = 0; c < C; c++) m[c] = fminf(m[c], __fmaf_rn(al[c], B, An));
+    } else {
+      float Anp, Bp, Anm, Bm;
+      ab1(v, te, Anp, Bp, Anm, Bm);
+      if (F == IQ1_S) {
+#pragma unroll
+        for (int s = 0; s < 8; s++) {
+          m[s] = fminf(m[s], __fmaf_rn(al[s], Bp, Anp));
+          m[8 + s] = fminf(m[8 + s], __fmaf_rn(al[s], Bm, Anm));
+        }
+      } else {
+#pragma unroll
+        for (int s = 0; s < 8; s++) m[s] = fminf(m[s], fminf(__fmaf_rn(al[s], Bp, Anp), __fmaf_rn(al[s], Bm, Anm)));
+      }
+    }
+  }
+}
+
+// Sweep 2: under one choice, the best candidate key and the best and runner-up scores.
+// key = entry (IQ2, IQ1_S) or delta_bit * N + entry (IQ1_M).
+template <int F>
+__device__ __forceinline__ void sweep_pick(const Vec &v, const float4 *tab, float alpha, int dbit_fixed, float &best,
+                                           float &second, int &key) {
+  constexpr int N = Fmt<F>::N;
+  best = INFINITY; second = INFINITY; key = 0;
+#pragma unroll 2
+  for (int e = 0; e < N; e++) {
+    const float4 *te = tab + 4 * e;
+    if (!Fmt<F>::IQ1) {
+      float An, B;
+      ab2(v.nw2, v.w, te, An, B);
+      const float s = __fmaf_rn(alpha, B, An);
+      second = fminf(second, fmaxf(best, s));
+      if (s < best) { best = s; key = e; }
+    } else {
+      float Anp, Bp, Anm, Bm;
+      ab1(v, te, Anp, Bp, Anm, Bm);
+      if (F == IQ1_S) {
+        const float s = dbit_fixed ? __fmaf_rn(alpha, Bm, Anm) : __fmaf_rn(alpha, Bp, Anp);
+        second = fminf(second, fmaxf(best, s));
+        if (s < best) { best = s; key = e; }
+      } else {
+        const float s0 = __fmaf_rn(alpha, Bp, Anp), s1 = __fmaf_rn(alpha, Bm, Anm);
+        second = fminf(second, fmaxf(best, s0));
+        if (s0 < best) { best = s0; key = e; }
+        second = fminf(second, fmaxf(best, s1));
+        if (s1 < best) { best = s1; key = N + e; }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Copy the prepared codebook (bytes, multiple of 16) into shared memory with bulk async copies;
+// every thread waits on the mbarrier for at most ~2 s.  Returns false on timeout.
+__device__ bool load_codebook(float4 *dst, const float4 *src, uint32_t bytes, uint64_t *mbar) {
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_u32(mbar)));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(mbar)), "r"(bytes)
+                 : "memory");
+    constexpr uint32_t CH = 32768;
+    for (uint32_t off = 0; off < bytes; off += CH) {
+      const uint32_t n = bytes - off < CH ? bytes - off : CH;
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_u32(reinterpret_cast<uint8_t *>(dst) + off)),
+          "l"(reinterpret_cast<const uint8_t *>(src) + off), "r"(n), "r"(smem_u32(mbar))
+          : "memory");
+    }
+  }
+  const uint64_t t0 = global_timer_ns();
+  bool done = false;
+  while (!done) {
+    done = mbar_try_wait(mbar, 0);
+    if (!done && global_timer_ns() - t0 > 2000000000ull) break;
+  }
+  return done;
+}
+
+template <typename TIn>
+__device__ __forceinline__ void load_block_vec(const EncArgs &a, int64_t b, int lane, Vec &v) {
+  const int64_t bpr = a.cols / 256;
+  const int64_t row = b / bpr, kb = b % bpr;
+  const TIn *W = reinterpret_cast<const TIn *>(a.W);
+  load8(W + row * a.cols + kb * 256 + lane * 8, v.x);
+  if (a.imp) {
+    const int64_t er = a.rows_per_expert > 0 ? row / a.rows_per_expert : 0;
+    load8(a.imp + er * a.cols + kb * 256 + lane * 8, v.w);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; i++) v.w[i] = 1.0f;
+  }
+}
+
+// Validates the block and returns its scale bits; 0 means "write an all-zero payload".
+template <int F, int MODE>
+__device__ __forceinline__ uint32_t block_scale(const EncArgs &a, int64_t b, int lane, const Vec &v, int &bad_bits) {
+  constexpr int G = Fmt<F>::G, C = Fmt<F>::C;
+  bad_bits = 0;
+  bool fin = finite8(v.x);
+  bool wok = true;
+#pragma unroll
+  for (int i = 0; i < 8; i++) wok &= (v.w[i] >= 0.0f) && isfinite(v.w[i]);
+  if (!__all_sync(0xffffffffu, fin)) bad_bits |= IQ_STATUS_BAD_INPUT;
+  else if (!__all_sync(0xffffffffu, wok)) bad_bits |= IQ_STATUS_BAD_IMPORTANCE;
+  if (bad_bits) return 0;
+  uint32_t d16 = a.d16 ? (uint32_t)a.d16[b] : (uint32_t)half_bits_rn(anchor_scale<F>(v.x));
+  if ((d16 & 0x7c00u) == 0x7c00u || ((d16 & 0x8000u) && (d16 & 0x7fffu))) { bad_bits |= IQ_STATUS_BAD_SCALE; return 0; }
+  d16 &= 0x7fffu;
+  if (MODE == MODE_FIXED) {
+    const int c = lane < G ? (int)a.choices[b * G + lane] : 0;
+    if (__any_sync(0xffffffffu, c >= C)) { bad_bits |= IQ_STATUS_BAD_CHOICE; return 0; }
+  }
+  return d16;
+}
+
+// Group reduction over the VPG lanes of each choice group, in vector order.
+template <int VPG>
+__device__ __forceinline__ float group_sum(float val, int g0) {
+  float s = __shfl_sync(0xffffffffu, val, g0);
+#pragma unroll
+  for (int k = 1; k < VPG; k++) s = __fadd_rn(s, __shfl_sync(0xffffffffu, val, g0 + k));
+  return s;
+}
+
+template <int F, int MODE, typename TIn, int THREADS>
+__global__ void __launch_bounds__(THREADS, 1) encode_kernel(EncArgs a, EncWs ws) {
+  constexpr int C = Fmt<F>::C, N = Fmt<F>::N, VPG = Fmt<F>::VPG, BB = Fmt<F>::BB;
+  constexpr int NW = THREADS / 32;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float4 *tab = reinterpret_cast<float4 *>(smem);
+  uint32_t *packbuf = reinterpret_cast<uint32_t *>(smem + N * 64);  // [NW][24]
+  __shared__ uint64_t mbar;
+
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const bool grid_bad = ws.hdr[0] != 0;
+  bool ok = true;
+  if (!grid_bad) ok = load_codebook(tab, ws.tab, N * 64, &mbar);
+  if (!ok) {
+    if (lane == 0 && a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+    // give an unfinished copy one more bounded wait before the CTA exits
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(&mbar, 0) && global_timer_ns() - t0 < 2000000000ull) {}
+    return;
+  }
+  if (grid_bad && blockIdx.x == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, IQ_STATUS_BAD_GRID);
+  uint32_t *pb = packbuf + wid * 24;
+  const int g0 = lane & ~(VPG - 1);
+  const int cg = lane / VPG;
+  int st_acc = 0;
+
+  for (int64_t b = (int64_t)blockIdx.x * NW + wid; b < a.nblocks; b += (int64_t)gridDim.x * NW) {
+    Vec v;
+    load_block_vec<TIn>(a, b, lane, v);
+    int bad = 0;
+    const uint32_t d16 = grid_bad ? 0u : block_scale<F, MODE>(a, b, lane, v, bad);
+    st_acc |= bad;
+    if (d16 == 0) {
+      if (MODE != MODE_TABLE)
+        for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = 0;
+      if (a.table && MODE != MODE_FIXED) {
+        // every choice decodes to zeros: the error is sum w x^2 (NaN for a rejected block)
+        float cs = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; i++) cs = __fmaf_rn(__fmul_rn(v.w[i], v.x[i]), v.x[i], cs);
+        const float e0 = group_sum<VPG>(cs, g0);
+        const float val = (bad || grid_bad) ? __int_as_float(0x7fc00000) : e0;
+        if (lane == g0)
+          for (int c = 0; c < C; c++) a.table[(b * Fmt<F>::G + cg) * C + c] = val;
+      }
+      continue;
+    }
+    const float d = half_bits_to_float((uint16_t)d16);
+    vec_setup<F>(v);
+    const float Cg = group_sum<VPG>(v.Cs, g0);
+
+    int c1;
+    bool gflag = false;
+    if (MODE != MODE_FIXED) {
+      float al[Fmt<F>::IQ1 ? 8 : 16];
+#pragma unroll
+      for (int s = 0; s < (Fmt<F>::IQ1 ? 8 : 16); s++) al[s] = alpha_of<F>(d, s);
+      float m[C];
+      sweep_minima<F>(v, tab, al, m);
+      float D1 = INFINITY, D2 = INFINITY;
+      c1 = 0;
+#pragma unroll
+      for (int c = 0; c < C; c++) {
+        const float S = group_sum<VPG>(m[c], g0);
+        const float D = __fmul_rn(al[F == IQ1_S ? (c & 7) : c], S);
+        if (a.table && lane == g0) a.table[(b * Fmt<F>::G + cg) * C + c] = __fadd_rn(Cg, D);
+        D2 = fminf(D2, fmaxf(D1, D));
+        if (D < D1) { D1 = D; c1 = c; }
+      }
+      gflag = __fsub_rn(D2, D1) <= kMargin * (4.0f * Cg + D1 + D2);
+      if (MODE == MODE_TABLE) continue;
+    } else {
+      c1 = a.choices[b * Fmt<F>::G + cg];
+    }
+    // entry pick under c1
+    const float alpha = alpha_choice<F>(d, c1);
+    float s1, s2;
+    int key;
+    sweep_pick<F>(v, tab, alpha, F == IQ1_S ? (c1 >> 3) : 0, s1, s2, key);
+    const float e1 = __fmul_rn(alpha, s1), e2 = __fmul_rn(alpha, s2);
+    const bool vflag = __fsub_rn(e2, e1) <= kMargin * (4.0f * v.Cs + e1 + e2);
+    // pack
+    if (lane < 24) pb[lane] = 0u;
+    __syncwarp();
+    const int idx = F == IQ1_M ? (key % N) : key;
+    const Bits lo = f_idx_lo<F>(lane);
+    put_bits(pb, lo, (uint32_t)idx);
+    if (F == IQ2_S || Fmt<F>::IQ1) put_bits(pb, f_idx_hi<F>(lane), (uint32_t)idx >> lo.width);
+    if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)v.sgn);
+    if (F == IQ1_M) {
+      put_bits(pb, f_dbit_vec<F>(lane), (uint32_t)(key / N));
+      if (lane < 4) put_bits(pb, f_d16_nib<F>(lane), (d16 >> (4 * lane)) & 15u);
+    } else if (lane == 0) {
+      put_bits(pb, f_d16<F>(), d16);
+    }
+    if (lane == g0) {
+      put_bits(pb, f_scale<F>(cg), (uint32_t)(F == IQ1_S ? (c1 & 7) : c1));
+      if (F == IQ1_S) put_bits(pb, f_dbit_grp<F>(cg), (uint32_t)(c1 >> 3));
+    }
+    __syncwarp();
+    const uint8_t *pbytes = reinterpret_cast<const uint8_t *>(pb);
+    for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = pbytes[i];
+    __syncwarp();
+    const uint32_t flags = __ballot_sync(0xffffffffu, gflag || vflag);
+    if (flags && lane == 0) {
+      const int slot = atomicAdd(&ws.hdr[1], 1);
+      ws.fb[slot] = make_uint2((uint32_t)b, flags);
+    }
+  }
+  if (st_acc && a.status) atomicOr(a.status, st_acc);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Exact rescoring of flagged groups.
+template <int F>
+__device__ __forceinline__ double exact_err(const float *x, const float *w, const float4 *te, float d, int s, int sgn,
+                                            int dbit) {
+  const float4 g0 = __ldg(te), g1 = __ldg(te + 1);
+  const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  double acc = 0.0;
+  if (!Fmt<F>::IQ1) {
+    const float dl = __fmul_rn(__fmul_rn(d, (float)(2 * s + 1)), 0.125f);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      float q = __fmul_rn(dl, g[i]);
+      q = ((sgn >> i) & 1) ? -q : q;
+      const double df = __dsub_rn((double)x[i], (double)q);
+      acc = __dadd_rn(acc, __dmul_rn((double)w[i], __dmul_rn(df, df)));
+    }
+  } else {
+    const float dl = __fmul_rn(d, (float)(2 * s + 1));
+    const float delta = dbit ? -0.125f : 0.125f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const float q = __fmul_rn(dl, __fadd_rn(g[i], delta));
+      const double df = __dsub_rn((double)x[i], (double)q);
+      acc = __dadd_rn(acc, __dmul_rn((double)w[i], __dmul_rn(df, df)));
+    }
+  }
+  return acc;
+}
+
+__device__ __forceinline__ Vec shfl_vec(const Vec &v, int src) {
+  Vec r;
+#pragma unroll
+  for (int i = 0; i < 8; i++) {
+    r.x[i] = __shfl_sync(0xffffffffu, v.x[i], src);
+    r.w[i] = __shfl_sync(0xffffffffu, v.w[i], src);
+    r.nw2[i] = __shfl_sync(0xffffffffu, v.nw2[i], src);
+  }
+  r.Cs = __shfl_sync(0xffffffffu, v.Cs, src);
+  r.nT2 = __shfl_sync(0xffffffffu, v.nT2, src);
+  r.Ws = __shfl_sync(0xffffffffu, v.Ws, src);
+  r.sgn = __shfl_sync(0xffffffffu, v.sgn, src);
+  return r;
+}
+
+// the fp32 score of candidate (entry e, delta bit db) under alpha, computed exactly as the sweep does
+template <int F>
+__device__ __forceinline__ float cand_score(const Vec &v, const float4 *te, float alpha, int db) {
+  if (!Fmt<F>::IQ1) {
+    float An, B;
+    ab2(v.nw2, v.w, te, An, B);
+    return __fmaf_rn(alpha, B, An);
+  } else {
+    float Anp, Bp, Anm, Bm;
+    ab1(v, te, Anp, Bp, Anm, Bm);
+    return db ? __fmaf_rn(alpha, Bm, Anm) : __fmaf_rn(alpha, Bp, Anp);
+  }
+}
+
+template <int F>
+__device__ __forceinline__ void cand_of_choice(int c, int &s, int &db0, int &db1) {
+  if (F == IQ1_S) { s = c & 7; db0 = db1 = c >> 3; }
+  else if (F == IQ1_M) { s = c; db0 = 0; db1 = 1; }
+  else { s = c; db0 = db1 = 0; }
+}
+
+struct RescoreSmem {
+  float mh[4][16];
+  double ex[4][16];
+  int exkey[4][16];
+  uint32_t pay[24];
+};
+
+template <int F, int MODE, typename TIn>
+__global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
+  constexpr int C = Fmt<F>::C, N = Fmt<F>::N, VPG = Fmt<F>::VPG, BB = Fmt<F>::BB, G = Fmt<F>::G;
+  __shared__ RescoreSmem sm_all[8];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  RescoreSmem &sm = sm_all[wid];
+  const int nflag = ws.hdr[1];
+  const float4 *tab = ws.tab;
+  for (int it = blockIdx.x * 8 + wid; it < nflag; it += gridDim.x * 8) {
+    const uint2 item = ws.fb[it];
+    const int64_t b = item.x;
+    const uint32_t mask = item.y;
+    Vec v;
+    load_block_vec<TIn>(a, b, lane, v);
+    uint8_t *pbytes = reinterpret_cast<uint8_t *>(sm.pay);
+    for (int i = lane; i < BB; i += 32) pbytes[i] = a.payload[b * BB + i];
+    uint32_t d16;
+    if (F == IQ1_M) {
+      d16 = 0;
+      for (int k = 0; k < 4; k++) d16 |= get_bits(pbytes, f_d16_nib<F>(k)) << (4 * k);
+    } else {
+      d16 = get_bits(pbytes, f_d16<F>());
+    }
+    __syncwarp();
+    const float d = half_bits_to_float((uint16_t)d16);
+    vec_setup<F>(v);
+    for (int g = 0; g < G; g++) {
+      const uint32_t gm = ((1u << VPG) - 1u) << (g * VPG);
+      if (!(mask & gm)) continue;
+      float Cg = 0.0f;
+      // (a) fp32 per-vector minima for every choice (or the fixed one), as the sweep computes them
+      int cfix = MODE == MODE_FIXED ? (int)a.choices[b * G + g] : -1;
+      for (int k = 0; k < VPG; k++) {
+        const Vec u = shfl_vec(v, g * VPG + k);
+        Cg = k == 0 ? u.Cs : __fadd_rn(Cg, u.Cs);
+        float lm[C];
+#pragma unroll
+        for (int c = 0; c < C; c++) lm[c] = INFINITY;
+        for (int e = lane; e < N; e += 32) {
+#pragma unroll
+          for (int c = 0; c < C; c++) {
+            if (MODE == MODE_FIXED && c != cfix) continue;
+            int s, db0, db1;
+            cand_of_choice<F>(c, s, db0, db1);
+            const float al = alpha_of<F>(d, s);
+            lm[c] = fminf(lm[c], cand_score<F>(u, tab + 4 * e, al, db0));
+            if (db1 != db0) lm[c] = fminf(lm[c], cand_score<F>(u, tab + 4 * e, al, db1));
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+          float x = lm[c];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, off));
+          lm[c] = x;
+        }
+        if (lane == 0)
+          for (int c = 0; c < C; c++) sm.mh[k][c] = lm[c];
+      }
+      __syncwarp();
+      // (b) near set of choices
+      float D[C];
+      float D1 = INFINITY;
+      for (int c = 0; c < C; c++) {
+        if (MODE == MODE_FIXED && c != cfix) { D[c] = INFINITY; continue; }
+        float S = sm.mh[0][c];
+        for (int k = 1; k < VPG; k++) S = __fadd_rn(S, sm.mh[k][c]);
+        D[c] = __fmul_rn(alpha_choice<F>(d, c), S);
+        D1 = fminf(D1, D[c]);
+      }
+      uint32_t near = 0;
+      for (int c = 0; c < C; c++)
+        if (D[c] != INFINITY && __fsub_rn(D[c], D1) <= kMargin * (4.0f * Cg + D1 + D[c])) near |= 1u << c;
+      // (c) exact minimum per (vector, near choice) over the candidates the bound cannot exclude
+      for (int c = 0; c < C; c++) {
+        if (!((near >> c) & 1)) continue;
+        int s, db0, db1;
+        cand_of_choice<F>(c, s, db0, db1);
+        const float al = alpha_of<F>(d, s);
+        for (int k = 0; k < VPG; k++) {
+          const Vec u = shfl_vec(v, g * VPG + k);
+          const float mh = sm.mh[k][c];
+          const float emin = __fmul_rn(al, mh);
+          double bestE = INFINITY;
+          int bestK = 0x7fffffff;
+          for (int e = lane; e < N; e += 32) {
+            for (int db = db0; db <= db1; db++) {
+              const float sc = cand_score<F>(u, tab + 4 * e, al, db);
+              const float ec = __fmul_rn(al, sc);
+              if (__fsub_rn(ec, emin) <= kMargin * (4.0f * u.Cs + emin + ec)) {
+                const double E = exact_err<F>(u.x, u.w, tab + 4 * e, d, s, u.sgn, db);
+                const int kk = (F == IQ1_M ? db * N : 0) + e;
+                if (E < bestE || (E == bestE && kk < bestK)) { bestE = E; bestK = kk; }
+              }
+            }
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            const double oE = __shfl_xor_sync(0xffffffffu, bestE, off);
+            const int oK = __shfl_xor_sync(0xffffffffu, bestK, off);
+            if (oE < bestE || (oE == bestE && oK < bestK)) { bestE = oE; bestK = oK; }
+          }
+          if (lane == 0) { sm.ex[k][c] = bestE; sm.exkey[k][c] = bestK; }
+        }
+      }
+      __syncwarp();
+      // (d) exact choice: least sum over the vectors, lowest choice on equal error
+      int cstar = -1;
+      double bestG = INFINITY;
+      for (int c = 0; c < C; c++) {
+        if (!((near >> c) & 1)) continue;
+        double Eg = sm.ex[0][c];
+        for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, sm.ex[k][c]);
+        if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
+      }
+      // (e) rewrite the group's fields (keep the sweep's decision if nothing was comparable)
+      if (lane == 0 && cstar >= 0) {
+        set_bits_bytes(pbytes, f_scale<F>(g), (uint32_t)(F == IQ1_S ? (cstar & 7) : cstar));
+        if (F == IQ1_S) set_bits_bytes(pbytes, f_dbit_grp<F>(g), (uint32_t)(cstar >> 3));
+        for (int k = 0; k < VPG; k++) {
+          const int vv = g * VPG + k;
+          const int key = sm.exkey[k][cstar];
+          const int idx = F == IQ1_M ? key % N : key;
+          const Bits lo = f_idx_lo<F>(vv);
+          set_bits_bytes(pbytes, lo, (uint32_t)idx);
+          if (F == IQ2_S || Fmt<F>::IQ1) set_bits_bytes(pbytes, f_idx_hi<F>(vv), (uint32_t)idx >> lo.width);
+          if (F == IQ1_M) set_bits_bytes(pbytes, f_dbit_vec<F>(vv), (uint32_t)(key / N));
+        }
+      }
+      __syncwarp();
+    }
+    for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = pbytes[i];
+    __syncwarp();
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+template <int F, typename TIn>
+__global__ void __launch_bounds__(256) anchor_kernel(const TIn *__restrict__ W, int64_t cols, int64_t nblocks,
+                                                     uint16_t *__restrict__ d16, int32_t *__restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  const int64_t bpr = cols / 256;
+  int st = 0;
+  for (int64_t b = warp; b < nblocks; b += nw) {
+    float x[8];
+    load8(W + (b / bpr) * cols + (b % bpr) * 256 + lane * 8, x);
+    const bool fin = __all_sync(0xffffffffu, finite8(x));
+    uint16_t h = 0;
+    if (fin) h = half_bits_rn(anchor_scale<F>(x));
+    else st |= IQ_STATUS_BAD_INPUT;
+    if (lane == 0) d16[b] = h;
+  }
+  if (st && lane == 0 && status) atomicOr(status, st);
+}
+
+static int num_sms() {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  return sms;
+}
+
+template <int F, typename TIn>
+static int run_anchor(const void *W, int64_t cols, int64_t nb, uint16_t *d16, int32_t *status, cudaStream_t st) {
+  if (nb == 0) return IQ_OK;
+  const int64_t want = (nb + 7) / 8;
+  const int grid = (int)(want < (int64_t)num_sms() * 8 ? want : (int64_t)num_sms() * 8);
+  anchor_kernel<F, TIn><<<grid, 256, 0, st>>>((const TIn *)W, cols, nb, d16, status);
+  return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+}
+
+template <int F, int MODE, typename TIn>
+static int run_encode(const EncArgs &a, void *workspace, size_t ws_bytes, cudaStream_t st) {
+  constexpr int N = Fmt<F>::N;
+  constexpr int THREADS = Fmt<F>::IQ1 ? 512 : 256;
+  if (a.nblocks == 0) return IQ_OK;
+  EncWs ws = enc_ws(workspace, N);
+  if (cudaMemsetAsync(ws.hdr, 0, 256, st) != cudaSuccess) return IQ_ERR_CUDA;
+  prep_codebook<F><<<(N + 255) / 256, 256, 0, st>>>(a.grid, ws);
+  const size_t smem = (size_t)N * 64 + (THREADS / 32) * 24 * 4;
+  auto kern = encode_kernel<F, MODE, TIn, THREADS>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return IQ_ERR_CUDA;
+  int per_sm = 1;
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem);
+  if (per_sm < 1) per_sm = 1;
+  const int64_t want = (a.nblocks + THREADS / 32 - 1) / (THREADS / 32);
+  const int64_t cap = (int64_t)num_sms() * per_sm;
+  const int grid = (int)(want < cap ? want : cap);
+  kern<<<grid, THREADS, smem, st>>>(a, ws);
+  if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
+  if (MODE != MODE_TABLE) {
+    rescore_kernel<F, MODE, TIn><<<num_sms() * 2, 256, 0, st>>>(a, ws);
+    if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
+  }
+  return IQ_OK;
+}
+
+template <int MODE, typename TIn>
+static int dispatch_encode(iq_format f, const EncArgs &a, void *ws, size_t wsb, cudaStream_t st) {
+  switch (f) {
+    case IQ2_XXS: return run_encode<IQ2_XXS, MODE, TIn>(a, ws, wsb, st);
+    case IQ2_XS: return run_encode<IQ2_XS, MODE, TIn>(a, ws, wsb, st);
+    case IQ2_S: return run_encode<IQ2_S, MODE, TIn>(a, ws, wsb, st);
+    case IQ1_S: return run_encode<IQ1_S, MODE, TIn>(a, ws, wsb, st);
+    default: return run_encode<IQ1_M, MODE, TIn>(a, ws, wsb, st);
+  }
+}
+
+static int grid_entries(iq_format f) {
+  return f == IQ2_XXS ? 256 : f == IQ2_XS ? 512 : f == IQ2_S ? 1024 : 2048;
+}
+
+static int check_common(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols, const float *imp,
+                        int64_t rpe, const float *grid) {
+  if ((unsigned)f > IQ1_M || (dt != IQ_F32 && dt != IQ_BF16)) return IQ_ERR_ARG;
+  if (rows < 0 || cols <= 0 || cols % 256) return IQ_ERR_ARG;
+  if (rows * (cols / 256) >= (int64_t)1 << 32) return IQ_ERR_ARG;
+  if (rpe < 0 || (rpe > 0 && rows % rpe)) return IQ_ERR_ARG;
+  if (rows > 0 && (!W || !grid)) return IQ_ERR_ARG;
+  if (((uintptr_t)W & 15) || ((uintptr_t)grid & 15) || ((uintptr_t)imp & 15)) return IQ_ERR_ARG;
+  return IQ_OK;
+}
+
+}  // namespace iqk
+
+using namespace iqk;
+
+extern "C" int iq_anchor_scales(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols, uint16_t *d16,
+                                int32_t *status, void *stream) {
+  if ((unsigned)f > IQ1_M || (dt != IQ_F32 && dt != IQ_BF16) || rows < 0 || cols <= 0 || cols % 256) return IQ_ERR_ARG;
+  const int64_t nb = rows * (cols / 256);
+  if (nb > 0 && (!W || !d16)) return IQ_ERR_ARG;
+  if ((uintptr_t)W & 15) return IQ_ERR_ARG;
+  cudaStream_t st = (cudaStream_t)stream;
+#define IQ_ANCHOR_CASE(FF)                                                                  \
+  case FF:                                                                                  \
+    return dt == IQ_BF16 ? run_anchor<FF, __nv_bfloat16>(W, cols, nb, d16, status, st)      \
+                         : run_anchor<FF, float>(W, cols, nb, d16, status, st);
+  switch (f) {
+    IQ_ANCHOR_CASE(IQ2_XXS)
+    IQ_ANCHOR_CASE(IQ2_XS)
+    IQ_ANCHOR_CASE(IQ2_S)
+    IQ_ANCHOR_CASE(IQ1_S)
+    IQ_ANCHOR_CASE(IQ1_M)
+  }
+#undef IQ_ANCHOR_CASE
+  return IQ_ERR_ARG;
+}
+
+extern "C" int iq_encode_workspace_size(iq_format f, int64_t rows, int64_t cols, size_t *bytes) {
+  if ((unsigned)f > IQ1_M || rows < 0 || cols <= 0 || cols % 256 || !bytes) return IQ_ERR_ARG;
+  *bytes = enc_ws_bytes(grid_entries(f), rows * (cols / 256));
+  return IQ_OK;
+}
+
+extern "C" int iq_encode(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols, const float *importance,
+                         int64_t rows_per_expert, const float *grid, const uint16_t *d16, const uint8_t *choices,
+                         uint8_t *payload, float *group_errors, int32_t *status, void *workspace,
+                         size_t workspace_bytes, void *stream) {
+  int rc = check_common(f, W, dt, rows, cols, importance, rows_per_expert, grid);
+  if (rc) return rc;
+  const int64_t nb = rows * (cols / 256);
+  if (nb > 0 && !payload) return IQ_ERR_ARG;
+  if (choices && group_errors) return IQ_ERR_ARG;  // the table is a product of the search
+  if ((uintptr_t)group_errors & 15) return IQ_ERR_ARG;
+  size_t need = 0;
+  iq_encode_workspace_size(f, rows, cols, &need);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, choices, payload, group_errors, status};
+  cudaStream_t st = (cudaStream_t)stream;
+  if (choices)
+    return dt == IQ_BF16 ? dispatch_encode<MODE_FIXED, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
+                         : dispatch_encode<MODE_FIXED, float>(f, a, workspace, workspace_bytes, st);
+  return dt == IQ_BF16 ? dispatch_encode<MODE_SEARCH, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
+                       : dispatch_encode<MODE_SEARCH, float>(f, a, workspace, workspace_bytes, st);
+}
+
+extern "C" int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                               const float *importance, int64_t rows_per_expert, const float *grid, const uint16_t *d16,
+                               float *group_errors, int32_t *status, void *workspace, size_t workspace_bytes,
+                               void *stream) {
+  int rc = check_common(f, W, dt, rows, cols, importance, rows_per_expert, grid);
+  if (rc) return rc;
+  const int64_t nb = rows * (cols / 256);
+  if (nb > 0 && !group_errors) return IQ_ERR_ARG;
+  if ((uintptr_t)group_errors & 15) return IQ_ERR_ARG;
+  size_t need = 0;
+  iq_encode_workspace_size(f, rows, cols, &need);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, nullptr, group_errors, status};
+  cudaStream_t st = (cudaStream_t)stream;
+  return dt == IQ_BF16 ? dispatch_encode<MODE_TABLE, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
+                       : dispatch_encode<MODE_TABLE, float>(f, a, workspace, workspace_bytes, st);
+}
+
+extern "C" int iq_format_info(iq_format f, iq_format_info_t *out) {
+  if ((unsigned)f > IQ1_M || !out) return IQ_ERR_ARG;
+  const int bits[5] = {8, 9, 10, 11, 11};
+  const int G[5] = {8, 16, 16, 8, 16}, C[5] = {16, 16, 16, 16, 8}, V[5] = {4, 2, 2, 4, 2};
+  out->block_bytes = fmt_block_bytes(f);
+  out->choice_groups = G[f];
+  out->num_choices = C[f];
+  out->grid_entries = grid_entries(f);
+  out->vectors_per_group = V[f];
+  out->index_bits = bits[f];
+  return IQ_OK;
+}

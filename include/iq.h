@@ -1,0 +1,178 @@
+/*
+ * iq.h — C ABI of the B300 (sm_103a) IQ codebook library: the importance-weighted encoder for the
+ * GGML IQ formats (IQ2_XXS, IQ2_XS, IQ2_S, IQ1_S, IQ1_M), its decoder, and the per-expert imatrix
+ * statistic that supplies the encoder's importance weights.
+ *
+ * Conventions for every call
+ *  - Pointers named as device pointers are CUDA global-memory addresses on the current device;
+ *    the caller allocates and owns every buffer.  The library keeps no state and allocates nothing;
+ *    calls that need scratch take a caller-provided `workspace` of at least the size reported by
+ *    the matching *_workspace_size call (device memory, 256-byte aligned, contents ignored).
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy default stream).
+ *  - Return value: IQ_OK (0) or a negative IQ_ERR_* code.  Argument checks run on the host before
+ *    anything is launched or written (a refused call changes no buffer).
+ *  - Data-dependent problems are never trapped and never synchronise the host: the kernels OR an
+ *    IQ_STATUS_* bit into `*status` (a device int32, may be NULL) and skip the offending unit.
+ *  - Matrices are row-major and contiguous.  A weight [rows, cols] has cols % 256 == 0 and is cut
+ *    into B = rows * cols / 256 blocks of 256 consecutive values of a row; block b covers row
+ *    b / (cols/256), columns 256 * (b % (cols/256)) ...; a block has 32 vectors of 8 values.
+ *
+ * Sources (web pages, cited by title and section):
+ *  [imatrix]  "Add imatrix calibration for the GGML formats and use it for fused MoE experts"
+ *             (PR #2735), "What imatrix does" and its unit-test list.
+ *  [coverage] "MoE expert coverage in imatrix calibration", Facts.
+ *  [formats]  PR #2513: the IQ2_XXS, IQ2_S and IQ1_M commit texts and the IQ1_M description.
+ *  [choices]  PR #3157 "[1/5] Let the GGML IQ encoders take fixed per-group choices", and PR #3159
+ *             "one-pass every-choice encode" (same page).
+ *  [iq1m-cuda] the IQ1_M CUDA-encoder commit message on the recipes-folder page.
+ */
+#ifndef IQ_B300_IQ_H
+#define IQ_B300_IQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define IQ_API __attribute__((visibility("default")))
+#else
+#define IQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { IQ2_XXS = 0, IQ2_XS = 1, IQ2_S = 2, IQ1_S = 3, IQ1_M = 4 } iq_format;
+typedef enum { IQ_F32 = 0, IQ_BF16 = 1 } iq_dtype;
+
+enum {
+  IQ_OK = 0,
+  IQ_ERR_ARG = -1,       /* null / misaligned pointer, bad size or enum, cols % 256 != 0, ... */
+  IQ_ERR_CUDA = -2,      /* a CUDA call or launch failed */
+  IQ_ERR_WORKSPACE = -3  /* workspace missing or smaller than the reported size */
+};
+
+/* Bits OR-ed into *status by the kernels. */
+#define IQ_STATUS_BAD_CHOICE 1        /* a fixed choice >= num_choices: that block is all zero */
+#define IQ_STATUS_BAD_EXPERT_ID 2     /* an expert id outside [0, num_experts): that slot ignored */
+#define IQ_STATUS_NONFINITE_SUM2 4    /* a non-finite in_sum2 value of an expert this call touched */
+#define IQ_STATUS_DUP_EXPERT_ID 8     /* an id repeated within one token's top-k: counted once */
+#define IQ_STATUS_BAD_INPUT 16        /* a non-finite weight value: that block is all zero */
+#define IQ_STATUS_BAD_IMPORTANCE 32   /* a negative or non-finite importance: that block is all zero */
+#define IQ_STATUS_BAD_SCALE 64        /* a negative / inf / nan fp16 scale: that block is all zero */
+#define IQ_STATUS_BAD_GRID 128        /* codebook values outside the format's set: all blocks zero */
+#define IQ_STATUS_TIMEOUT 256         /* an internal bounded wait gave up: results unspecified */
+
+typedef struct {
+  int block_bytes;        /* payload bytes per 256-value block */
+  int choice_groups;      /* groups per block that each store one choice */
+  int num_choices;        /* choices per group: valid choice values are [0, num_choices) */
+  int grid_entries;       /* codebook rows (each 8 fp32 values) */
+  int vectors_per_group;  /* 8-value vectors per choice group */
+  int index_bits;         /* bits of a stored codebook index */
+} iq_format_info_t;
+
+/* Per-format constants [formats]: bits per weight 2.0625 / 2.3125 / 2.5625 / 1.5625 / 1.75 give
+ * 66 / 74 / 82 / 50 / 56 bytes per block.  Returns IQ_ERR_ARG for an unknown format. */
+IQ_API int iq_format_info(iq_format f, iq_format_info_t *out);
+
+/*
+ * Block layouts (bit p of a block is bit p % 8 of byte p / 8; multi-byte fields little-endian).
+ * g = vector (8 values) 0..31, s = sub-block of 32 values 0..7, cg = choice group.
+ *  IQ2_XXS (66 B): d fp16 @0; per s: 4 index bytes @2+8s (vectors 4s..4s+3), then a u32 @6+8s with
+ *           four 7-bit sign indices (bits 7k..7k+6, vector 4s+k) and the 4-bit scale (bits 28..31).
+ *           cg = s (32 values, 8 per block).
+ *  IQ2_XS  (74 B): d @0; per g a u16 @2+2g = 9-bit index | 7-bit sign index << 9; byte 66+s holds
+ *           the scales of cg 2s (low nibble) and 2s+1 (high).  cg = g/2 (16 values, 16 per block).
+ *  IQ2_S   (82 B): d @0; index low bytes @2+g; 8-bit sign masks @34+g; byte 66+s holds the index
+ *           high 2 bits of vector 4s+k at bits 2k; byte 74+s the scales of cg 2s, 2s+1.  cg = g/2.
+ *  IQ1_S   (50 B): d @0; index low bytes @2+g; per s a u16 @34+2s: index high 3 bits of vector
+ *           4s+k at bits 3k, scale at bits 12..14, delta bit at 15.  cg = s; choice = scale + 8*delta.
+ *  IQ1_M   (56 B): index low bytes @g; byte 32+g/2, nibble g%2: index high 3 bits | delta bit << 3;
+ *           u16 @48+2k: scales of cg 4k..4k+3 at bits 3j, and d's fp16 bits 4k..4k+3 at 12..15.
+ *           cg = g/2; choice = scale (the delta is per vector, free in the entry search).
+ * Values: IQ2 q = d * (2s+1)/8 * g[i], negated where sign bit i is set; IQ2_XXS/XS store bits 0..6
+ * and bit 7 is the parity of bits 0..6 (even parity).  IQ1 q = d * (2s+1) * (g[i] + delta), delta
+ * = +1/8 for delta bit 0 and -1/8 for 1.  Codebooks: IQ2 values must be integers in [1, 127], IQ1
+ * values in {-1, 0, 1}; every decoded value is then exact in fp32.
+ */
+
+/* ---- imatrix ([imatrix] "What imatrix does", Bounded memory; [coverage] Facts) ----------------
+ * For each chunk of `rows_per_chunk` consecutive tokens (1,024 on the pages) and each expert e the
+ * chunk routes tokens to: partial[e][j] = fp32 sum, in ascending token order, of x[t][j]*x[t][j]
+ * (one rounded multiply, one rounded add) over the chunk's tokens whose top-k ids contain e; then
+ * in_sum2[e][j] += partial[e][j] (chunk order) and counts[e] += tokens routed to e.  A token's ids
+ * are a set (a repeated id counts once and sets IQ_STATUS_DUP_EXPERT_ID).  After the call, a
+ * non-finite in_sum2 row of an expert this call touched sets IQ_STATUS_NONFINITE_SUM2.
+ *   x            device, [tokens, cols] of dtype dt (IQ_F32 or IQ_BF16), 16-byte aligned
+ *   expert_ids   device, [tokens, top_k] int32
+ *   in_sum2      device, [num_experts, cols] fp32, accumulated in place (16-byte aligned)
+ *   counts       device, [num_experts] int64, accumulated in place
+ *   requires cols % 64 == 0, 1 <= top_k <= num_experts <= 1024, 1 <= rows_per_chunk <= 4096.
+ * Results are bit-identical to the sequential definition above. */
+IQ_API int iq_imatrix_workspace_size(int64_t tokens, int num_experts, int64_t rows_per_chunk, size_t *bytes);
+IQ_API int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens, int64_t cols,
+                          const int32_t *expert_ids, int top_k, int num_experts, int64_t rows_per_chunk,
+                          float *in_sum2, int64_t *counts, int32_t *status, void *workspace,
+                          size_t workspace_bytes, void *stream);
+
+/* Importance weights ([imatrix] "Why the square root"; [coverage] Facts: count 0 -> weight 1):
+ * w[e][j] = sqrt(m) with m = in_sum2[e][j] / (float)counts[e] (IEEE fp32 division and square root),
+ * m raised to `floor` first when floor > 0 and m < floor; w = 1 for every channel of an expert
+ * with counts[e] == 0.  All pointers device; w may not alias in_sum2. */
+IQ_API int iq_imatrix_weights(const float *in_sum2, const int64_t *counts, int num_experts, int64_t cols,
+                       float floor, float *w, void *stream);
+
+/* ---- super-block scale anchor ([formats]: "single-pass grid search at a fixed anchored
+ * super-block scale"; IQ1_S flat 0.61; IQ1_M clamp(0.58 + 0.035 * peak_to_rms, 0.65, 0.95)) -----
+ * d16[b] = fp16 (round to nearest even, saturated at 65504) of (ratio * amax) / K, amax = max |x|
+ * over the block, K = 166.625 (IQ2: 43 * 31/8) or 15 (IQ1), ratio = 1 for IQ2, 0.61 for IQ1_S and
+ * the clamp above for IQ1_M with rms = sqrt(s/256), s = sum of x^2 summed as 32 sequential partial
+ * sums of 8 consecutive squares, then pairwise (l, l+16), (l, l+8), (l, l+4), (l, l+2), (l, l+1).
+ * Blocks with a non-finite value get d16 = 0 and IQ_STATUS_BAD_INPUT.  W device [rows, cols]. */
+IQ_API int iq_anchor_scales(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols, uint16_t *d16,
+                     int32_t *status, void *stream);
+
+/* ---- encoder ([formats]; [choices]; [iq1m-cuda]) --------------------------------------------
+ * For every choice group: for every allowed choice c, each vector takes the candidate (entry, plus
+ * the delta for IQ1_M) with the least weighted squared error sum_i w_i (x_i - q_i)^2; the group
+ * takes the choice with the least sum over its vectors (lowest c on equal error), and each vector
+ * its best candidate under it (lowest (delta bit, entry) on equal error).  IQ2_XXS/XS first flip
+ * the sign of argmin_i w_i x_i^2 when an odd number of x_i are negative (even parity); IQ2_S keeps
+ * the input signs.  Decisions equal those of an exact evaluation: candidates the fp32 sweep cannot
+ * separate from the best within its proven rounding bound are rescored in fp64.
+ *   W            device [rows, cols], dtype dt; 16-byte aligned
+ *   importance   device fp32, NULL (w = 1), [cols] (rows_per_expert == 0) or [E, cols] with row r
+ *                using expert r / rows_per_expert ([coverage]: global row / rows per expert)
+ *   grid         device fp32 [grid_entries, 8] codebook
+ *   d16          device fp16 bits [B], or NULL to compute the anchor above inside the call
+ *   choices      device uint8 [B, choice_groups] fixed choices, or NULL to search; a value >=
+ *                num_choices sets IQ_STATUS_BAD_CHOICE and zeroes that block
+ *   payload      device uint8 [B, block_bytes] output
+ *   group_errors device fp32 [B, choice_groups, num_choices] or NULL: with choices == NULL, the
+ *                weighted squared error of every (group, choice) pair from the same sweep (the
+ *                every-choice mode); each value is within 2^-17 * (4 * sum_g w x^2 + 2 * E) of exact
+ *   workspace    device scratch of iq_encode_workspace_size bytes
+ * A block whose scale is 0 encodes to all-zero bytes ([choices] review: zero blocks). */
+IQ_API int iq_encode_workspace_size(iq_format f, int64_t rows, int64_t cols, size_t *bytes);
+IQ_API int iq_encode(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols, const float *importance,
+              int64_t rows_per_expert, const float *grid, const uint16_t *d16, const uint8_t *choices,
+              uint8_t *payload, float *group_errors, int32_t *status, void *workspace,
+              size_t workspace_bytes, void *stream);
+
+/* Every-choice error table only (same sweep, no payload): group_errors as in iq_encode. */
+IQ_API int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                    const float *importance, int64_t rows_per_expert, const float *grid, const uint16_t *d16,
+                    float *group_errors, int32_t *status, void *workspace, size_t workspace_bytes,
+                    void *stream);
+
+/* ---- decoder ([formats]: the value rule above) ------------------------------------------------
+ * out[rows, cols] (device; IQ_F32, or IQ_BF16 rounded to nearest even) from payload [B,
+ * block_bytes].  fp32 output is exact.  out must be 16-byte aligned. */
+IQ_API int iq_decode(iq_format f, const uint8_t *payload, int64_t rows, int64_t cols, const float *grid, void *out,
+              iq_dtype out_dtype, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* IQ_B300_IQ_H */

@@ -562,7 +562,25 @@ int or_encode(int f, const float *W, int64_t rows, int64_t cols, const float *im
     }
     if (!bad && choices)
       for (int g = 0; g < o.groups; g++) if (choices[b * o.groups + g] >= o.num_choices) { st |= OR_ST_BAD_CHOICE; bad = 1; }
-    if (bad || d16 == 0) { memset(p, 0, (size_t)o.block_bytes); continue; }
+    if (bad || d16 == 0) {
+      memset(p, 0, (size_t)o.block_bytes);
+      if (!bad) {
+        /* a zero scale decodes every choice to zeros: report that payload's error */
+        float zq[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int g = 0; g < o.groups; g++) {
+          double Eg = 0.0;
+          for (int k = 0; k < o.vpg; k++) {
+            int v = g * o.vpg + k;
+            double e = vec_err(x + 8 * v, w + 8 * v, zq);
+            if (vbest) vbest[b * 32 + v] = e;
+            Eg = Eg + e;
+          }
+          if (table) for (int c = 0; c < o.num_choices; c++) table[(b * o.groups + g) * o.num_choices + c] = Eg;
+          if (gbest) gbest[b * o.groups + g] = Eg;
+        }
+      }
+      continue;
+    }
     const float d = or_float_from_half(d16);
     blockfields bf; memset(&bf, 0, sizeof bf);
     bf.d16 = d16;
