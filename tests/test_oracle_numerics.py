@@ -3,6 +3,8 @@
 Each test ties the oracle to something other than itself: numpy's IEEE conversions and float32
 arithmetic (a library routine), exact histograms, closed forms, or a higher-precision sum.
 """
+from fractions import Fraction
+
 import numpy as np
 import pytest
 
@@ -64,22 +66,75 @@ def test_imatrix_all_ones_gives_counts(orc):
     assert np.array_equal(s2, np.repeat(counts.astype(np.float32)[:, None], 256, axis=1))
 
 
+def f32_nearest(q: Fraction) -> np.float32:
+    """The float32 nearest to the rational q, ties to even, found by exact comparison of the
+    neighbours of a first guess (float() of a Fraction is correctly rounded to fp64; the fp64 ->
+    fp32 step can be off by one ulp, which the neighbour check corrects)."""
+    c = np.float32(float(q))
+    cands = [np.nextafter(c, np.float32(-np.inf)), c, np.nextafter(c, np.float32(np.inf))]
+    return min(cands, key=lambda v: (abs(Fraction(float(v)) - q), int(np.float32(v).view(np.uint32)) & 1))
+
+
+def fused_running_sum_exact(col):
+    """partial = fl(partial + x*x) for each x in order, with exact rational arithmetic and one
+    correct rounding per step: the definition of the single-rounding running sum."""
+    acc = np.float32(0.0)
+    for x in col:
+        acc = f32_nearest(Fraction(float(acc)) + Fraction(float(x)) ** 2)
+    return acc
+
+
+def bounded_bf16_acts(tokens, cols, seed):
+    """bf16-valued activations with 2^-4 <= |x| < 2^4.  A square then has at most 16 significant
+    bits and lies in [2^-8, 2^8); a running sum of up to 1,024 of them stays below 2^18 with its
+    lowest bit at or above 2^-31, so every step partial + x*x is exact in fp64 (at most 50
+    significant bits) and one fp64 -> fp32 rounding is the single correct rounding."""
+    x = synth.activations(tokens, cols, seed=seed)
+    mag = np.clip(np.abs(x), 2.0 ** -4, 2.0 ** 4 * (1 - 2.0 ** -9))
+    x = np.where(x < 0, -mag, mag).astype(np.float32)
+    return synth.as_dtype(x, "bf16")[1]
+
+
+def fused_running_sum_f64(rows):
+    """Vectorised running sum over axis 0, one fp32 rounding per step from an exact fp64 step
+    (valid for the bounded inputs above)."""
+    acc = np.zeros(rows.shape[1], np.float32)
+    for r in rows:
+        acc = (acc.astype(np.float64) + r.astype(np.float64) ** 2).astype(np.float32)
+    return acc
+
+
+def test_imatrix_single_rounding_exact_small(orc):
+    """Values spanning 1e-22 .. 1e4, fp32-valued, some squares subnormal: each step of the running
+    sum is the exact square added and rounded once (exact rational reference)."""
+    rng = np.random.default_rng(19)
+    x = (rng.standard_normal((48, 40)) * 10.0 ** rng.integers(-22, 4, (48, 40))).astype(np.float32)
+    x[5, 0] = np.float32(3e-20)            # square 9e-40: subnormal in fp32
+    x[:3, 4] = np.float32(1e-23)           # squares far below the fp32 range, then larger terms
+    s2, counts, _ = orc.imatrix_accumulate(x, np.zeros((48, 1), np.int32), 1, rows_per_chunk=1024)
+    assert counts[0] == 48
+    ref = np.array([fused_running_sum_exact(x[:, j]) for j in range(40)], np.float32)
+    assert np.array_equal(s2[0].view(np.uint32), ref.view(np.uint32))
+    # the two-rounding form (fp32 multiply, then fp32 add) differs in some columns, so this pin
+    # tells the two readings apart
+    assert not np.array_equal(s2[0], np.cumsum(x * x, axis=0, dtype=np.float32)[-1])
+
+
 def test_imatrix_single_expert_is_sequential_column_sum(orc):
-    """One expert, top-1, one chunk: the sum is the fp32 running sum of x*x down each column,
-    which numpy's cumsum computes sequentially in float32."""
-    x = synth.activations(700, 512, seed=8)
+    """One expert, top-1, one chunk: the sum is the running single-rounding sum of x*x down each
+    column (exact fp64 steps on bounded bf16 inputs)."""
+    x = bounded_bf16_acts(700, 512, seed=8)
     ids = np.zeros((700, 1), np.int32)
     s2, counts, _ = orc.imatrix_accumulate(x, ids, 1, rows_per_chunk=1024)
-    ref = np.cumsum(x * x, axis=0, dtype=np.float32)[-1]
     assert counts[0] == 700
-    assert np.array_equal(s2[0], ref)
+    assert np.array_equal(s2[0], fused_running_sum_f64(x))
 
 
 def test_imatrix_chunks_add_partial_sums(orc):
-    """Chunked: each chunk's per-expert partial (sequential over its routed tokens) is added to the
-    running total in chunk order; checked against numpy cumsums of the routed rows."""
+    """Chunked: each chunk's per-expert partial (running single-rounding sum over its routed tokens)
+    is added to the running total (one fp32 add) in chunk order."""
     T, C, E, K, R = 530, 256, 6, 2, 128
-    x = synth.activations(T, C, seed=9)
+    x = bounded_bf16_acts(T, C, seed=9)
     ids = synth.router(T, E, K, idle=1, seed=10)
     s2, _, _ = orc.imatrix_accumulate(x, ids, E, rows_per_chunk=R)
     ref = np.zeros((E, C), np.float32)
@@ -88,7 +143,7 @@ def test_imatrix_chunks_add_partial_sums(orc):
         for e in range(E):
             rows = [t for t in range(sl.start, sl.stop) if e in ids[t]]
             if rows:
-                ref[e] = ref[e] + np.cumsum(x[rows] * x[rows], axis=0, dtype=np.float32)[-1]
+                ref[e] = ref[e] + fused_running_sum_f64(x[rows])
     assert np.array_equal(s2, ref)
 
 
