@@ -41,6 +41,19 @@ CONFIG = {"workload": "encode 5632x2048 bf16 weight in IQ2_XXS/IQ2_XS/IQ2_S/IQ1_
           "l2": "flushed before every timed step (512 MiB write); inputs 23 MiB + 16 MiB < L2"}
 
 
+MOE_T, MOE_C, MOE_E, MOE_K = 4096, 17408, 128, 8
+
+
+def measured_peaks():
+    """HBM copy bandwidth (GB/s) measured on this GPU pool, else the fallback figure."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6400.0, "fallback"
+
+
 def flops_per_element(fmt):
     """Algorithmic FP32 work of the searched encode per weight element: per codebook entry and
     8-value vector, IQ2 16 FMA for (A, B) + 16 choices x (FMA + min) = 80 flops; IQ1 24 FMA +
@@ -197,6 +210,7 @@ def run_ours(args):
     ch7 = {f: torch.full((B, info[f]["choice_groups"]), 7, dtype=torch.uint8, device=dev) for f in FORMATS}
     dec = torch.empty(R, C, dtype=torch.float32, device=dev)
     ws = {f: api.encode_workspace(f, R, C, dev) for f in FORMATS}
+    ws_im = api.imatrix_workspace(T_ACT, C, torch.bfloat16, 1, 1, 1024, dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     names = ["imatrix", "weights"] + [f"{k}:{f}" for f in FORMATS for k in ("encode", "fixed", "decode")]
@@ -207,7 +221,7 @@ def run_ours(args):
                 evs[i].record(stream)
         mark(0)
         s2.zero_(); cn.zero_()
-        api.imatrix_accumulate(X, ids, 1, 1024, s2, cn, status=st)
+        api.imatrix_accumulate(X, ids, 1, 1024, s2, cn, status=st, workspace=ws_im)
         mark(1)
         w = api.imatrix_weights(s2, cn)
         mark(2)
@@ -265,6 +279,10 @@ def run_ours(args):
                  "encode_ms": round(e_ms, 4), "fixed_ms": round(x_ms, 4), "decode_ms": round(d_ms, 4)}
     im_ms = float(np.mean(per["imatrix"]))
     im_bytes = T_ACT * C * 2 + T_ACT * 4 + 2 * C * 4
+    hbm, hbm_src = measured_peaks()
+    moe = measure_imatrix_moe(args, dev, flush, hbm)
+    for f in FORMATS:
+        pf[f]["decode_frac_hbm"] = round(pf[f]["decode_GB_s"] / hbm, 4)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     dom = max(FORMATS, key=lambda f: pf[f]["encode_ms"])
     dom_ms = pf[dom]["encode_ms"]
@@ -279,15 +297,59 @@ def run_ours(args):
         roofline["frac_at_observed_clock"] = round(achieved / fp32_peak_tflops(sms, clocks["sm_mhz"]), 4)
     # end to end through the public API with host buffers
     e2e = measure_e2e(args, dev, Wst, Xst, grids, G, ids, info)
-    launches = args.steps * (3 + 5 * (3 + 3 + 1))
+    # this library's kernels per step: imatrix route + csr + accumulate (+ combine when chunks run
+    # in parallel), weights, and per format: codebook prep + encode + rescore (searched and fixed)
+    # and decode
+    im_kernels = 4 if T_ACT > 1024 and (C + 127) // 128 < 112 else 3
+    launches = args.steps * (im_kernels + 1 + len(FORMATS) * (3 + 3 + 1))
     cpu = cpu_baseline_sample(Wv, Xv, grids) if world == 1 or rank == 0 else None
     line = {"metric": METRIC, "value": round(value, 2), "unit": "M elem/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": CONFIG,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches, "clocks": clocks,
             "per_format": pf,
-            "imatrix": {"ms": round(im_ms, 4), "GB_s": round(im_bytes / (im_ms * 1e-3) / 1e9, 1)}}
+            "imatrix": {"ms": round(im_ms, 4), "GB_s": round(im_bytes / (im_ms * 1e-3) / 1e9, 1),
+                        "frac_hbm": round(im_bytes / (im_ms * 1e-3) / 1e9 / hbm, 4)},
+            "imatrix_moe": moe, "hbm_peak_GB_s": hbm, "hbm_peak_source": hbm_src}
     print(json.dumps(line))
+
+
+def measure_imatrix_moe(args, dev, flush, hbm):
+    """The routed-MoE imatrix workload: 4096 tokens x 17408-wide bf16 activations (log-normal
+    column scales), 128 experts, top-8 from a Zipf(1.2) router with 8 idle experts, 1,024-row
+    chunks.  Algorithmic bytes: x and the ids read once, in_sum2 of the touched experts read and
+    written once."""
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api, synth
+    xs, _ = synth.as_dtype(synth.activations(MOE_T, MOE_C, seed=2), "bf16")
+    ids_np = synth.router(MOE_T, MOE_E, MOE_K, seed=2)
+    X = torch.from_numpy(np.ascontiguousarray(xs).view(np.int16)).view(torch.bfloat16).to(dev)
+    ids = torch.from_numpy(ids_np).to(dev)
+    s2 = torch.zeros(MOE_E, MOE_C, dtype=torch.float32, device=dev)
+    cn = torch.zeros(MOE_E, dtype=torch.int64, device=dev)
+    ws = api.imatrix_workspace(MOE_T, MOE_C, torch.bfloat16, MOE_E, MOE_K, 1024, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        api.imatrix_accumulate(X, ids, MOE_E, 1024, s2, cn, workspace=ws)
+    times = []
+    for _ in range(max(5, args.steps)):
+        flush.fill_(2)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        api.imatrix_accumulate(X, ids, MOE_E, 1024, s2, cn, workspace=ws)
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.median(times))
+    counts = np.bincount(ids_np.ravel(), minlength=MOE_E)
+    touched = int((counts > 0).sum())
+    nbytes = MOE_T * MOE_C * 2 + ids_np.nbytes + 2 * touched * MOE_C * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"{MOE_T}x{MOE_C} bf16, {MOE_E} experts, top-{MOE_K} Zipf(1.2), 1024-row chunks",
+            "ms": round(ms, 4), "GB_s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+            "algorithmic_bytes": nbytes, "idle_experts": int((counts == 0).sum()),
+            "tokens_per_expert_min_median_max": [int(counts.min()), int(np.median(counts)), int(counts.max())]}
 
 
 def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):

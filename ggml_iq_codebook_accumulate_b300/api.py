@@ -47,7 +47,7 @@ def lib():
         L = ctypes.CDLL(LIB_PATH)
         i64, i32, p, sz = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_size_t
         L.iq_format_info.argtypes = [i32, ctypes.POINTER(_Info)]
-        L.iq_imatrix_workspace_size.argtypes = [i64, i32, i64, ctypes.POINTER(sz)]
+        L.iq_imatrix_workspace_size.argtypes = [i64, i64, i32, i32, i32, i64, ctypes.POINTER(sz)]
         L.iq_imatrix_accumulate.argtypes = [p, i32, i64, i64, p, i32, i32, i64, p, p, p, p, sz, p]
         L.iq_imatrix_weights.argtypes = [p, p, i32, i64, ctypes.c_float, p, p]
         L.iq_anchor_scales.argtypes = [i32, p, i32, i64, i64, p, p, p]
@@ -99,7 +99,16 @@ def _workspace(nbytes, device):
     return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
 
 
-def imatrix_accumulate(x, expert_ids, num_experts, rows_per_chunk=1024, in_sum2=None, counts=None, status=None):
+def imatrix_workspace(tokens, cols, dtype, num_experts, top_k, rows_per_chunk, device):
+    nb = ctypes.c_size_t()
+    dt = IQ_BF16 if dtype == torch.bfloat16 else IQ_F32
+    _check(lib().iq_imatrix_workspace_size(tokens, cols, dt, num_experts, top_k, rows_per_chunk, ctypes.byref(nb)),
+           "workspace size")
+    return _workspace(nb.value, device)
+
+
+def imatrix_accumulate(x, expert_ids, num_experts, rows_per_chunk=1024, in_sum2=None, counts=None, status=None,
+                       workspace=None):
     """Accumulates the routed sum of squares into ``in_sum2`` [E, cols] fp32 and token counts into
     ``counts`` [E] int64 (both created as zeros when None).  Returns (in_sum2, counts)."""
     _cuda(x, "x"); _cuda(expert_ids, "expert_ids")
@@ -109,9 +118,8 @@ def imatrix_accumulate(x, expert_ids, num_experts, rows_per_chunk=1024, in_sum2=
         in_sum2 = torch.zeros(num_experts, C, dtype=torch.float32, device=dev)
     if counts is None:
         counts = torch.zeros(num_experts, dtype=torch.int64, device=dev)
-    nb = ctypes.c_size_t()
-    _check(lib().iq_imatrix_workspace_size(T, num_experts, rows_per_chunk, ctypes.byref(nb)), "workspace size")
-    ws = _workspace(nb.value, dev)
+    ws = workspace if workspace is not None else imatrix_workspace(T, C, x.dtype, num_experts, expert_ids.shape[1],
+                                                                    rows_per_chunk, dev)
     _check(lib().iq_imatrix_accumulate(_p(x), _dt(x), T, C, _p(expert_ids.to(torch.int32)), expert_ids.shape[1],
                                        num_experts, rows_per_chunk, _p(in_sum2), _p(counts), _p(status), _p(ws),
                                        ws.numel(), _stream(dev)), "iq_imatrix_accumulate")

@@ -230,21 +230,6 @@ __device__ __forceinline__ void sweep_pick(const Vec &v, const float4 *tab, floa
 }
 
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint64_t global_timer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *m, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(m)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
 // Copy the prepared codebook (bytes, multiple of 16) into shared memory with bulk async copies;
 // every thread waits on the mbarrier for at most ~2 s.  Returns false on timeout.
 __device__ bool load_codebook(float4 *dst, const float4 *src, uint32_t bytes, uint64_t *mbar) {

@@ -1,54 +1,105 @@
 // imatrix statistic: routed per-expert sums of squared activations and token counts
-// ("Add imatrix calibration for the GGML formats ...", What imatrix does: one statistic per
-// routed expert over the tokens routed to it, rows squared 1,024 at a time; "MoE expert coverage
-// in imatrix calibration", Facts: x^2 added only to the token's top-k experts, a per-expert token
-// count, non-finite sums checked only for touched experts, count 0 -> weight 1).
+// ("Add imatrix calibration for the GGML formats and use it for fused MoE experts", What imatrix
+// does: one statistic per routed expert over the tokens routed to it, rows squared 1,024 at a
+// time; "MoE expert coverage in imatrix calibration", Facts: x^2 added only to the token's top-k
+// experts, a per-expert token count, non-finite sums checked only for touched experts, count 0
+// -> weight 1).
 //
-// Two kernels per call:
-//  route       one CTA per chunk: a bitmap [E][rows/32] of which chunk rows each expert receives
-//              (a token's ids are a set), per-chunk counts, and an expert order by descending count;
-//  accumulate  one CTA per 64-column tile walks the chunks in order.  Each chunk is streamed through
-//              shared memory in sub-tiles (cp.async, double buffered); warp w owns a fixed set of
-//              experts (dealt from the count order so heavy and light experts mix) and, for each,
-//              walks the set bits of its bitmap in ascending row order adding x*x to a register
-//              accumulator per column (one rounded multiply and one rounded add).  After the chunk
-//              the partial sums are added to in_sum2 once, in chunk order.  This is exactly the
-//              sequential definition, so sums are bit-identical to it; no atomics touch in_sum2.
+// Definition computed (bit for bit): for each chunk of rows_per_chunk tokens and each expert e the
+// chunk routes tokens to, partial[e][j] starts at +0 and, over those tokens in ascending order,
+// becomes fl(partial + x*x) -- the exact square added with one rounding; then in_sum2[e][j] =
+// fl(in_sum2[e][j] + partial[e][j]), chunk by chunk.
+//
+// Kernels per call:
+//  route       one CTA per chunk: a bitmap [E][rows/32] of the chunk rows each expert receives
+//              (a token's ids are a set), per-chunk counts, list offsets (an exclusive scan over
+//              experts) and an expert order by descending count;
+//  csr         one warp per (chunk, expert): expands the bitmap into the ascending list of the
+//              expert's chunk-local rows;
+//  accumulate  one CTA per column tile (128 bf16 / 64 fp32 columns, 256 bytes of a row) and,
+//              when there are too few tiles to fill the GPU, per chunk as well.  A producer warp
+//              streams the tile's rows through a 3-stage shared-memory ring with 2-D TMA tensor
+//              copies (mbarrier completion, bounded waits); each consumer warp owns up to 8
+//              experts (dealt from the count order so heavy and light experts mix), walks their
+//              row lists and keeps one register accumulator per (expert, column of its lane);
+//  combine     (per-chunk mode only) adds the chunk partials to in_sum2 in chunk order.
+// No atomics touch in_sum2, so the sums are the sequential definition above.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "iq_common.cuh"
 
 namespace iqk {
 
-constexpr int kAccWarps = 8;          // warps per accumulate CTA
-constexpr int kExpPerWarp = 16;       // experts a warp holds accumulators for (per expert batch)
-constexpr int kExpBatch = kAccWarps * kExpPerWarp;  // 128 experts per pass over x
-constexpr int kTileCols = 64;         // columns per accumulate CTA (2 per lane)
+constexpr int kSub = 128;           // rows per stage
+constexpr int kStages = 3;          // shared-memory ring depth
+constexpr int kRowBytes = 256;      // bytes of one row of a column tile
+constexpr int kSlots = 8;           // experts per consumer warp
+constexpr int kMaxConsumers = 16;   // consumer warps per CTA
+constexpr int kBatch = kSlots * kMaxConsumers;  // experts per pass over x
+constexpr int kMinSeqCtas = 112;    // below this many (tile, batch) CTAs, chunks also run in parallel
 
-struct RouteWs {
-  uint32_t *bits;      // [nchunks][E][W]
-  int32_t *ccount;     // [nchunks][E]
-  int32_t *order;      // [nchunks][E]
-  int32_t *touched;    // [E]
-};
+template <typename T> struct Col;
+template <> struct Col<__nv_bfloat16> { static constexpr int CPL = 4, TILE = 128; };
+template <> struct Col<float> { static constexpr int CPL = 2, TILE = 64; };
 
 __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
-__host__ __device__ inline RouteWs route_ws(void *ws, int64_t nchunks, int E, int W) {
-  uint8_t *p = (uint8_t *)ws;
-  RouteWs r;
-  r.bits = (uint32_t *)p; p += align256((size_t)nchunks * E * W * 4);
-  r.ccount = (int32_t *)p; p += align256((size_t)nchunks * E * 4);
-  r.order = (int32_t *)p; p += align256((size_t)nchunks * E * 4);
-  r.touched = (int32_t *)p;
-  return r;
-}
-static size_t route_ws_bytes(int64_t nchunks, int E, int W) {
-  return align256((size_t)nchunks * E * W * 4) + 2 * align256((size_t)nchunks * E * 4) + align256((size_t)E * 4);
+struct RouteWs {
+  int32_t *touched;    // [E]   experts this call routed at least one token to
+  uint32_t *bits;      // [nchunks][E][W]
+  int32_t *ccount;     // [nchunks][E] tokens per (chunk, expert)
+  int32_t *order;      // [nchunks][E] experts by descending chunk count (ties: lower id)
+  int32_t *loff;       // [nchunks][E] start of the expert's list within the chunk's list
+  uint16_t *list;      // [nchunks][lcap] chunk-local rows, ascending per expert
+  float *partial;      // [nchunks][E][cols] (per-chunk mode only)
+  size_t zero_bytes;   // bytes from the start to clear before the call (touched + bits)
+};
+
+struct Plan {
+  int64_t nchunks, lcap, ntiles, nbatch;
+  int W;
+  bool split;
+};
+
+static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_k, int64_t rpc) {
+  Plan p;
+  p.nchunks = (tokens + rpc - 1) / rpc;
+  p.W = (int)((rpc + 31) / 32);
+  p.lcap = rpc * (int64_t)(top_k < E ? top_k : E);
+  const int tile = dt == IQ_BF16 ? Col<__nv_bfloat16>::TILE : Col<float>::TILE;
+  p.ntiles = (cols + tile - 1) / tile;
+  p.nbatch = (E + kBatch - 1) / kBatch;
+  p.split = p.nchunks > 1 && p.ntiles * p.nbatch < kMinSeqCtas;
+  return p;
 }
 
-__global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__ ids, int64_t tokens, int top_k,
-                                                     int E, int64_t rpc, int W, RouteWs ws,
-                                                     unsigned long long *__restrict__ counts,
-                                                     int32_t *__restrict__ status) {
+static RouteWs route_ws(void *ws, const Plan &p, int E, int64_t cols) {
+  uint8_t *q = (uint8_t *)ws;
+  RouteWs r;
+  r.touched = (int32_t *)q; q += align256((size_t)E * 4);
+  r.bits = (uint32_t *)q; q += align256((size_t)p.nchunks * E * p.W * 4);
+  r.zero_bytes = (size_t)(q - (uint8_t *)ws);
+  r.ccount = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
+  r.order = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
+  r.loff = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
+  r.list = (uint16_t *)q; q += align256((size_t)p.nchunks * p.lcap * 2);
+  r.partial = p.split ? (float *)q : nullptr;
+  return r;
+}
+static size_t route_ws_bytes(const Plan &p, int E, int64_t cols) {
+  size_t n = align256((size_t)E * 4) + align256((size_t)p.nchunks * E * p.W * 4) +
+             3 * align256((size_t)p.nchunks * E * 4) + align256((size_t)p.nchunks * p.lcap * 2);
+  if (p.split) n += align256((size_t)p.nchunks * E * cols * 4);
+  return n;
+}
+
+// ---------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) imatrix_route(const int32_t *__restrict__ ids, int64_t tokens, int top_k,
+                                                      int E, int64_t rpc, int W, RouteWs ws,
+                                                      unsigned long long *__restrict__ counts,
+                                                      int32_t *__restrict__ status) {
   __shared__ int cnt[1024];
   const int64_t k = blockIdx.x;
   const int64_t t0 = k * rpc, t1 = min(tokens, t0 + rpc);
@@ -70,7 +121,6 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
     }
   }
   __syncthreads();
-  // order experts by descending chunk count (ties: lower id first) with a rank count
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int c = cnt[e];
     int rank = 0;
@@ -82,167 +132,289 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
     ws.ccount[(size_t)k * E + e] = c;
     if (c) {
       atomicAdd(&counts[e], (unsigned long long)c);
-      atomicOr(&ws.touched[e], 1);
+      ws.touched[e] = 1;
+    }
+  }
+  // exclusive scan of the chunk counts over expert ids -> list offsets (warp 0)
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int run = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int v = base + lane < E ? cnt[base + lane] : 0;
+      int incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      if (base + lane < E) ws.loff[(size_t)k * E + base + lane] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
   }
   if (st && status) atomicOr(status, st);
 }
 
-template <typename T> struct AccIn;
-template <> struct AccIn<__nv_bfloat16> { static constexpr int SUB = 256; using Pair = uint32_t; };
-template <> struct AccIn<float> { static constexpr int SUB = 128; using Pair = uint64_t; };
-
-// acc (a packed pair of fp32 partial sums) += (x0*x0, x1*x1): one rounded multiply and one rounded
-// add per value (never fused), two values per instruction with the packed f32x2 forms.
-__device__ __forceinline__ void sq_add(uint64_t &acc, uint64_t v) {
-  uint64_t sq;
-  asm("mul.rn.f32x2 %0, %1, %1;" : "=l"(sq) : "l"(v));
-  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(sq));
-}
-__device__ __forceinline__ void sq_add(uint64_t &acc, uint32_t pr) {  // bf16 pair, widened exactly
-  uint64_t v;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(v) : "r"(pr << 16), "r"(pr & 0xffff0000u));
-  sq_add(acc, v);
-}
-__device__ __forceinline__ float2 unpack2(uint64_t v) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
-  return r;
-}
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-  const uint32_t s = (uint32_t)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N> __device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
-
-template <typename T>
-__global__ void __launch_bounds__(kAccWarps * 32) imatrix_accumulate_kernel(
-    const T *__restrict__ x, int64_t tokens, int64_t cols, int E, int64_t rpc, int W, RouteWs ws,
-    float *__restrict__ in_sum2, int32_t *__restrict__ status) {
-  constexpr int SUB = AccIn<T>::SUB;                 // rows per sub-tile
-  constexpr int ROWB = kTileCols * (int)sizeof(T);   // bytes per sub-tile row
-  constexpr int TILEB = SUB * ROWB;                  // bytes per sub-tile buffer
-  using Pair = typename AccIn<T>::Pair;
-  extern __shared__ __align__(128) uint8_t smem[];
-  uint8_t *buf[2] = {smem, smem + TILEB};
-  uint32_t *sbits = reinterpret_cast<uint32_t *>(smem + 2 * TILEB);  // [kExpBatch][SUB/32]
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int64_t col0 = (int64_t)blockIdx.x * kTileCols;
-  const int64_t nchunks = (tokens + rpc - 1) / rpc;
-  const int subs_per_chunk = (int)((rpc + SUB - 1) / SUB);
-  const int64_t nsteps = nchunks * subs_per_chunk;
-
-  for (int eb = 0; eb < E; eb += kExpBatch) {
-    const int ne = min(kExpBatch, E - eb);
-    uint64_t acc[kExpPerWarp];  // packed (column 2*lane, column 2*lane+1) partial sums, +0.0f each
+__global__ void __launch_bounds__(256) imatrix_csr(int E, int W, int64_t lcap, RouteWs ws) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t k = blockIdx.y;
+  if (e >= E) return;
+  const uint32_t *bits = ws.bits + ((size_t)k * E + e) * W;
+  uint16_t *list = ws.list + (size_t)k * lcap + ws.loff[(size_t)k * E + e];
+  int pos = 0;
+  for (int w0 = 0; w0 < W; w0 += 32) {
+    uint32_t word = w0 + lane < W ? bits[w0 + lane] : 0u;
+    const int n = __popc(word);
+    int incl = n;
 #pragma unroll
-    for (int j = 0; j < kExpPerWarp; j++) acc[j] = 0ull;
-
-    // issue the cp.async copies of sub-tile `step` into buffer step & 1
-    auto issue = [&](int64_t step) {
-      const int64_t k = step / subs_per_chunk;
-      const int sidx = (int)(step % subs_per_chunk);
-      const int64_t r0 = k * rpc + (int64_t)sidx * SUB;
-      const int64_t r1 = min(min(tokens, (k + 1) * rpc), r0 + SUB);
-      const int nrows = (int)(r1 - r0);
-      uint8_t *dst = buf[step & 1];
-      constexpr int PIECES = ROWB / 16;
-      for (int i = threadIdx.x; i < nrows * PIECES; i += blockDim.x) {
-        const int r = i / PIECES, c16 = i % PIECES;
-        const uint8_t *src = reinterpret_cast<const uint8_t *>(x + (r0 + r) * cols + col0) + c16 * 16;
-        cp_async16(dst + r * ROWB + c16 * 16, src);
-      }
-      cp_async_commit();
-    };
-
-    issue(0);
-    for (int64_t step = 0; step < nsteps; step++) {
-      const int64_t k = step / subs_per_chunk;
-      const int sidx = (int)(step % subs_per_chunk);
-      // stage this sub-tile's bitmap rows for the batch's experts
-      const int wps = SUB / 32;
-      for (int i = threadIdx.x; i < kExpBatch * wps; i += blockDim.x) {
-        const int je = i / wps, wi = i % wps;
-        const int gw = sidx * wps + wi;
-        uint32_t v = 0;
-        if (je < ne && gw < W) {
-          const int e = ws.order[(size_t)k * E + eb + je];
-          v = ws.bits[((size_t)k * E + e) * W + gw];
-        }
-        sbits[je * wps + wi] = v;
-      }
-      if (step + 1 < nsteps) { issue(step + 1); cp_async_wait<1>(); } else { cp_async_wait<0>(); }
-      __syncthreads();
-      const uint8_t *tile = buf[step & 1];
-#pragma unroll
-      for (int j = 0; j < kExpPerWarp; j++) {
-        // snake deal over the count order: warp w takes positions w, 2*8-1-w, 16+w, ...
-        const int je = j * kAccWarps + ((j & 1) ? (kAccWarps - 1 - warp) : warp);
-        if (je >= ne) continue;
-        for (int wi = 0; wi < wps; wi++) {
-          uint32_t word = sbits[je * wps + wi];
-          while (word) {
-            const int r = wi * 32 + (__ffs(word) - 1);
-            word &= word - 1;
-            const Pair pr = reinterpret_cast<const Pair *>(tile + r * ROWB)[lane];
-            sq_add(acc[j], pr);
-          }
-        }
-      }
-      __syncthreads();  // buffer step&1 is refilled two steps later; sbits is rewritten next step
-      if (sidx == subs_per_chunk - 1) {
-#pragma unroll
-        for (int j = 0; j < kExpPerWarp; j++) {
-          const int je = j * kAccWarps + ((j & 1) ? (kAccWarps - 1 - warp) : warp);
-          if (je >= ne) continue;
-          const int e = ws.order[(size_t)k * E + eb + je];
-          if (ws.ccount[(size_t)k * E + e] == 0) continue;
-          float2 *dst = reinterpret_cast<float2 *>(in_sum2 + (int64_t)e * cols + col0) + lane;
-          float2 v = *dst;
-          const float2 a = unpack2(acc[j]);
-          v.x = __fadd_rn(v.x, a.x);
-          v.y = __fadd_rn(v.y, a.y);
-          *dst = v;
-          acc[j] = 0ull;
-        }
-      }
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
     }
-    // non-finite check of every expert this call touched (its rows of this column tile)
-    if (status) {
-      int bad = 0;
-      for (int je = warp; je < ne; je += kAccWarps) {
-        const int e = eb + je;
-        if (!ws.touched[e]) continue;
-        const float2 v = reinterpret_cast<const float2 *>(in_sum2 + (int64_t)e * cols + col0)[lane];
-        bad |= !(isfinite(v.x) && isfinite(v.y));
-      }
-      if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(status, IQ_STATUS_NONFINITE_SUM2);
+    int p = pos + incl - n;
+    while (word) {
+      const int b = __ffs(word) - 1;
+      word &= word - 1;
+      list[p++] = (uint16_t)((w0 + lane) * 32 + b);
     }
-    __syncthreads();
+    pos += __shfl_sync(0xffffffffu, incl, 31);
   }
 }
 
+// ---------------------------------------------------------------------------------------------
+struct AccArgs {
+  int64_t tokens, cols, rpc, nchunks, lcap;
+  int E, nconsumers;
+  RouteWs ws;
+  float *in_sum2;
+  int32_t *status;
+};
+
+// acc[0..CPL) += x^2 for the CPL values of this lane at `p` (shared memory), one rounding each.
+__device__ __forceinline__ void sq_acc(float *acc, const uint8_t *p, __nv_bfloat16) {
+  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %4;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n"
+      " mov.b32 {l, h}, %5;\n fma.rn.f32.bf16 %2, l, l, %2;\n fma.rn.f32.bf16 %3, h, h, %3;\n}\n"
+      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
+      : "r"(u.x), "r"(u.y));
+}
+__device__ __forceinline__ void sq_acc(float *acc, const uint8_t *p, float) {
+  const float2 v = *reinterpret_cast<const float2 *>(p);
+  acc[0] = __fmaf_rn(v.x, v.x, acc[0]);
+  acc[1] = __fmaf_rn(v.y, v.y, acc[1]);
+}
+
 template <typename T>
-static size_t acc_smem_bytes() {
-  return 2 * (size_t)AccIn<T>::SUB * kTileCols * sizeof(T) + (size_t)kExpBatch * (AccIn<T>::SUB / 32) * 4;
+__global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_kernel(
+    const __grid_constant__ CUtensorMap tmap, AccArgs a) {
+  constexpr int CPL = Col<T>::CPL, TILE = Col<T>::TILE;
+  constexpr uint32_t kStageBytes = kSub * kRowBytes;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  // stage buffers start on a 128-byte boundary (one spare 128 bytes is allocated for this)
+  uint8_t *smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
+  __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ int abort_flag;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int NW = a.nconsumers;
+  const int64_t col0 = (int64_t)blockIdx.x * TILE;
+  const int eb = blockIdx.z * kBatch;
+  const int ne = min(kBatch, a.E - eb);
+  const bool split = a.ws.partial != nullptr;
+  const int64_t kbeg = split ? blockIdx.y : 0, kend = split ? blockIdx.y + 1 : a.nchunks;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; s++) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], NW); }
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == NW) {
+    // ---- producer: lane 0 issues the tile's row stages in consumption order --------------
+    if (lane == 0) {
+      int64_t q = 0;
+      bool ok = true;
+      for (int64_t k = kbeg; k < kend && ok; k++) {
+        const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
+        const int nsub = (int)((rows + kSub - 1) / kSub);
+        for (int sub = 0; sub < nsub && ok; sub++, q++) {
+          const int st = (int)(q % kStages);
+          if (q >= kStages) ok = mbar_wait_bounded(&empty_bar[st], (uint32_t)((q / kStages - 1) & 1));
+          if (!ok || *(volatile int *)&abort_flag) { ok = false; break; }
+          mbar_expect_tx(&full_bar[st], kStageBytes);
+          tma_load_2d(smem + (size_t)st * kStageBytes, &tmap, (int)col0, (int)(k * a.rpc + (int64_t)sub * kSub),
+                      &full_bar[st]);
+        }
+      }
+      if (!ok) {
+        atomicExch(&abort_flag, 1);
+        if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+      }
+      // every issued copy must land before the CTA's shared memory is released
+      for (int64_t u = q - kStages < 0 ? 0 : q - kStages; u < q; u++)
+        mbar_wait_bounded(&full_bar[u % kStages], (uint32_t)((u / kStages) & 1));
+    }
+  } else if (warp < NW) {
+    // ---- consumers ----------------------------------------------------------------------------
+    const int64_t mycol = col0 + lane * CPL;
+    const bool col_ok = mycol < a.cols;
+    int64_t q = 0;
+    bool ok = true;
+    for (int64_t k = kbeg; k < kend && ok; k++) {
+      const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
+      const int nsub = (int)((rows + kSub - 1) / kSub);
+      int e_[kSlots], cnt_[kSlots], lb_[kSlots], cur_[kSlots];
+      float acc[kSlots][CPL];
+#pragma unroll
+      for (int s = 0; s < kSlots; s++) {
+        const int je = s * NW + ((s & 1) ? NW - 1 - warp : warp);
+        e_[s] = je < ne ? a.ws.order[(size_t)k * a.E + eb + je] : -1;
+        cnt_[s] = e_[s] >= 0 ? a.ws.ccount[(size_t)k * a.E + e_[s]] : 0;
+        lb_[s] = e_[s] >= 0 ? a.ws.loff[(size_t)k * a.E + e_[s]] : 0;
+        cur_[s] = 0;
+#pragma unroll
+        for (int c = 0; c < CPL; c++) acc[s][c] = 0.0f;
+      }
+      const uint16_t *list = a.ws.list + (size_t)k * a.lcap;
+      for (int sub = 0; sub < nsub; sub++, q++) {
+        const int st = (int)(q % kStages);
+        if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((q / kStages) & 1)) || *(volatile int *)&abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint8_t *tile = smem + (size_t)st * kStageBytes + lane * (CPL * sizeof(T));
+        const int rlo = sub * kSub, rhi = rlo + kSub;
+#pragma unroll
+        for (int s = 0; s < kSlots; s++) {
+          while (cur_[s] < cnt_[s]) {
+            const int i = cur_[s] + lane;
+            const int r = i < cnt_[s] ? (int)list[lb_[s] + i] : 0x7fffffff;
+            const int n = __popc(__ballot_sync(0xffffffffu, r < rhi));
+            const int rl = r - rlo;
+            int j = 0;
+#pragma unroll 1
+            for (; j + 4 <= n; j += 4) {
+              const int r0 = __shfl_sync(0xffffffffu, rl, j), r1 = __shfl_sync(0xffffffffu, rl, j + 1);
+              const int r2 = __shfl_sync(0xffffffffu, rl, j + 2), r3 = __shfl_sync(0xffffffffu, rl, j + 3);
+              sq_acc(acc[s], tile + r0 * kRowBytes, T());
+              sq_acc(acc[s], tile + r1 * kRowBytes, T());
+              sq_acc(acc[s], tile + r2 * kRowBytes, T());
+              sq_acc(acc[s], tile + r3 * kRowBytes, T());
+            }
+            for (; j < n; j++) sq_acc(acc[s], tile + __shfl_sync(0xffffffffu, rl, j) * kRowBytes, T());
+            cur_[s] += n;
+            if (n < 32) break;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
+      }
+      if (!ok) break;
+      // chunk done: add the partials to in_sum2 (or store them for the ordered combine)
+#pragma unroll
+      for (int s = 0; s < kSlots; s++) {
+        if (cnt_[s] == 0 || !col_ok) continue;
+        if (split) {
+          float *dst = a.ws.partial + ((size_t)k * a.E + e_[s]) * a.cols + mycol;
+#pragma unroll
+          for (int c = 0; c < CPL; c++) dst[c] = acc[s][c];
+        } else {
+          float *dst = a.in_sum2 + (size_t)e_[s] * a.cols + mycol;
+#pragma unroll
+          for (int c = 0; c < CPL; c++) dst[c] = __fadd_rn(dst[c], acc[s][c]);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      atomicExch(&abort_flag, 1);
+      if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+    }
+  }
+  __syncthreads();
+  // non-finite check of the touched experts' final sums in this tile (sequential mode; the
+  // combine kernel checks in per-chunk mode)
+  if (!split && a.status && warp < NW) {
+    const int64_t mycol = col0 + lane * CPL;
+    int bad = 0;
+    for (int je = warp; je < ne; je += NW) {
+      const int e = eb + je;
+      if (!a.ws.touched[e] || mycol >= a.cols) continue;
+      const float *v = a.in_sum2 + (size_t)e * a.cols + mycol;
+#pragma unroll
+      for (int c = 0; c < CPL; c++) bad |= !isfinite(v[c]);
+    }
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, IQ_STATUS_NONFINITE_SUM2);
+  }
+}
+
+// per-chunk mode: in_sum2 += partial[k] for k = 0, 1, ... (experts the chunk routed tokens to)
+__global__ void __launch_bounds__(256) imatrix_combine(int64_t cols, int E, int64_t nchunks, RouteWs ws,
+                                                       float *__restrict__ in_sum2, int32_t *__restrict__ status) {
+  const int64_t n = (int64_t)E * cols;
+  int bad = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / cols);
+    if (!ws.touched[e]) continue;
+    float v = in_sum2[i];
+    for (int64_t k = 0; k < nchunks; k++)
+      if (ws.ccount[(size_t)k * E + e]) v = __fadd_rn(v, ws.partial[(size_t)k * E * cols + i]);
+    in_sum2[i] = v;
+    bad |= !isfinite(v);
+  }
+  if (status && __any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, IQ_STATUS_NONFINITE_SUM2);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host: 2-D tensor map of x ([tokens, cols], row-major) with a box of 256 bytes x kSub rows.
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+  });
+  return fn;
+}
+
+static bool make_tmap(CUtensorMap *m, const void *x, iq_dtype dt, int64_t tokens, int64_t cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const int esz = dt == IQ_BF16 ? 2 : 4;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)tokens};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esz), (cuuint32_t)kSub};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt == IQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T>
+static int launch_accumulate(const CUtensorMap &tm, const AccArgs &a, const Plan &p, cudaStream_t st) {
+  const size_t smem = (size_t)kStages * kSub * kRowBytes + 128;
+  auto kern = imatrix_accumulate_kernel<T>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return IQ_ERR_CUDA;
+  dim3 grid((unsigned)p.ntiles, p.split ? (unsigned)p.nchunks : 1u, (unsigned)p.nbatch);
+  kern<<<grid, 32 * (a.nconsumers + 1), smem, st>>>(tm, a);
+  return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
 }
 
 }  // namespace iqk
 
 using namespace iqk;
 
-extern "C" int iq_imatrix_workspace_size(int64_t tokens, int num_experts, int64_t rows_per_chunk, size_t *bytes) {
-  if (!bytes || tokens < 0 || num_experts <= 0 || num_experts > 1024 || rows_per_chunk <= 0 ||
-      rows_per_chunk > 4096)
+extern "C" int iq_imatrix_workspace_size(int64_t tokens, int64_t cols, iq_dtype dt, int num_experts, int top_k,
+                                         int64_t rows_per_chunk, size_t *bytes) {
+  if (!bytes || tokens < 0 || cols <= 0 || (dt != IQ_F32 && dt != IQ_BF16) || num_experts <= 0 ||
+      num_experts > 1024 || top_k < 1 || rows_per_chunk <= 0 || rows_per_chunk > 4096)
     return IQ_ERR_ARG;
-  const int64_t nchunks = (tokens + rows_per_chunk - 1) / rows_per_chunk;
-  const int W = (int)((rows_per_chunk + 31) / 32);
-  *bytes = route_ws_bytes(nchunks, num_experts, W);
+  const Plan p = make_plan(tokens, cols, dt, num_experts, top_k, rows_per_chunk);
+  *bytes = route_ws_bytes(p, num_experts, cols);
   return IQ_OK;
 }
 
@@ -251,37 +423,45 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
                                      float *in_sum2, int64_t *counts, int32_t *status, void *workspace,
                                      size_t workspace_bytes, void *stream) {
   if (dt != IQ_F32 && dt != IQ_BF16) return IQ_ERR_ARG;
-  if (tokens < 0 || cols <= 0 || cols % kTileCols || top_k < 1 || num_experts < top_k || num_experts > 1024 ||
-      rows_per_chunk < 1 || rows_per_chunk > 4096)
+  if (tokens < 0 || tokens > INT32_MAX || cols <= 0 || cols % 64 || top_k < 1 || num_experts < top_k ||
+      num_experts > 1024 || rows_per_chunk < 1 || rows_per_chunk > 4096 ||
+      (tokens + rows_per_chunk - 1) / rows_per_chunk > 65535)
     return IQ_ERR_ARG;
   if (!in_sum2 || !counts || (tokens > 0 && (!x || !expert_ids))) return IQ_ERR_ARG;
   if (((uintptr_t)x & 15) || ((uintptr_t)in_sum2 & 15) || ((uintptr_t)counts & 7) || ((uintptr_t)expert_ids & 3))
     return IQ_ERR_ARG;
   size_t need = 0;
-  iq_imatrix_workspace_size(tokens, num_experts, rows_per_chunk, &need);
+  iq_imatrix_workspace_size(tokens, cols, dt, num_experts, top_k, rows_per_chunk, &need);
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
   if (tokens == 0) return IQ_OK;
+  const Plan p = make_plan(tokens, cols, dt, num_experts, top_k, rows_per_chunk);
+  CUtensorMap tm;
+  if (!make_tmap(&tm, x, dt, tokens, cols)) return IQ_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
-  const int64_t nchunks = (tokens + rows_per_chunk - 1) / rows_per_chunk;
-  const int W = (int)((rows_per_chunk + 31) / 32);
-  RouteWs ws = route_ws(workspace, nchunks, num_experts, W);
-  if (cudaMemsetAsync(workspace, 0, need, st) != cudaSuccess) return IQ_ERR_CUDA;
-  imatrix_route<<<(unsigned)nchunks, 256, 0, st>>>(expert_ids, tokens, top_k, num_experts, rows_per_chunk, W, ws,
-                                                   (unsigned long long *)counts, status);
+  RouteWs ws = route_ws(workspace, p, num_experts, cols);
+  if (cudaMemsetAsync(workspace, 0, ws.zero_bytes, st) != cudaSuccess) return IQ_ERR_CUDA;
+  imatrix_route<<<(unsigned)p.nchunks, 1024, 0, st>>>(expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.W,
+                                                     ws, (unsigned long long *)counts, status);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
-  const unsigned grid = (unsigned)(cols / kTileCols);
-  if (dt == IQ_BF16) {
-    const size_t sm = acc_smem_bytes<__nv_bfloat16>();
-    cudaFuncSetAttribute(imatrix_accumulate_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    imatrix_accumulate_kernel<__nv_bfloat16><<<grid, kAccWarps * 32, sm, st>>>(
-        (const __nv_bfloat16 *)x, tokens, cols, num_experts, rows_per_chunk, W, ws, in_sum2, status);
-  } else {
-    const size_t sm = acc_smem_bytes<float>();
-    cudaFuncSetAttribute(imatrix_accumulate_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-    imatrix_accumulate_kernel<float><<<grid, kAccWarps * 32, sm, st>>>(
-        (const float *)x, tokens, cols, num_experts, rows_per_chunk, W, ws, in_sum2, status);
+  imatrix_csr<<<dim3((unsigned)((num_experts + 7) / 8), (unsigned)p.nchunks), 256, 0, st>>>(num_experts, p.W, p.lcap,
+                                                                                           ws);
+  if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
+  AccArgs a;
+  a.tokens = tokens; a.cols = cols; a.rpc = rows_per_chunk; a.nchunks = p.nchunks; a.lcap = p.lcap;
+  a.E = num_experts;
+  const int ne = num_experts < kBatch ? num_experts : kBatch;
+  a.nconsumers = (ne + kSlots - 1) / kSlots;
+  a.ws = ws; a.in_sum2 = in_sum2; a.status = status;
+  const int rc = dt == IQ_BF16 ? launch_accumulate<__nv_bfloat16>(tm, a, p, st) : launch_accumulate<float>(tm, a, p, st);
+  if (rc != IQ_OK) return rc;
+  if (p.split) {
+    const int64_t n = (int64_t)num_experts * cols;
+    const int64_t blocks = (n + 255) / 256;
+    imatrix_combine<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(cols, num_experts, p.nchunks, ws,
+                                                                              in_sum2, status);
+    if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   }
-  return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+  return IQ_OK;
 }
 
 // ---------------------------------------------------------------------------------------------

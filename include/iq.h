@@ -99,18 +99,23 @@ IQ_API int iq_format_info(iq_format f, iq_format_info_t *out);
 
 /* ---- imatrix ([imatrix] "What imatrix does", Bounded memory; [coverage] Facts) ----------------
  * For each chunk of `rows_per_chunk` consecutive tokens (1,024 on the pages) and each expert e the
- * chunk routes tokens to: partial[e][j] = fp32 sum, in ascending token order, of x[t][j]*x[t][j]
- * (one rounded multiply, one rounded add) over the chunk's tokens whose top-k ids contain e; then
- * in_sum2[e][j] += partial[e][j] (chunk order) and counts[e] += tokens routed to e.  A token's ids
- * are a set (a repeated id counts once and sets IQ_STATUS_DUP_EXPERT_ID).  After the call, a
- * non-finite in_sum2 row of an expert this call touched sets IQ_STATUS_NONFINITE_SUM2.
+ * chunk routes tokens to: partial[e][j] starts at +0 and, over the chunk's tokens whose top-k ids
+ * contain e in ascending token order, becomes fl(partial + x[t][j]*x[t][j]) -- the exact square
+ * added with ONE rounding (a fused multiply-add); then in_sum2[e][j] = fl(in_sum2[e][j] +
+ * partial[e][j]) (chunk order) and counts[e] += tokens routed to e.  A token's ids are a set (a
+ * repeated id counts once and sets IQ_STATUS_DUP_EXPERT_ID; an id outside [0, num_experts) is
+ * skipped and sets IQ_STATUS_BAD_EXPERT_ID).  After the call, a non-finite in_sum2 value of an
+ * expert this call touched sets IQ_STATUS_NONFINITE_SUM2.
  *   x            device, [tokens, cols] of dtype dt (IQ_F32 or IQ_BF16), 16-byte aligned
  *   expert_ids   device, [tokens, top_k] int32
  *   in_sum2      device, [num_experts, cols] fp32, accumulated in place (16-byte aligned)
  *   counts       device, [num_experts] int64, accumulated in place
- *   requires cols % 64 == 0, 1 <= top_k <= num_experts <= 1024, 1 <= rows_per_chunk <= 4096.
- * Results are bit-identical to the sequential definition above. */
-IQ_API int iq_imatrix_workspace_size(int64_t tokens, int num_experts, int64_t rows_per_chunk, size_t *bytes);
+ *   workspace    device scratch of iq_imatrix_workspace_size bytes (256-byte aligned)
+ *   requires cols % 64 == 0, 1 <= top_k <= num_experts <= 1024, 1 <= rows_per_chunk <= 4096,
+ *   tokens < 2^31 and at most 65535 chunks.
+ * Results are bit-identical to the sequential definition above, whatever the launch layout. */
+IQ_API int iq_imatrix_workspace_size(int64_t tokens, int64_t cols, iq_dtype dt, int num_experts, int top_k,
+                              int64_t rows_per_chunk, size_t *bytes);
 IQ_API int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens, int64_t cols,
                           const int32_t *expert_ids, int top_k, int num_experts, int64_t rows_per_chunk,
                           float *in_sum2, int64_t *counts, int32_t *status, void *workspace,
