@@ -18,7 +18,8 @@ FORMATS = ("IQ2_XXS", "IQ2_XS", "IQ2_S", "IQ1_S", "IQ1_M")
 FMT_ID = {n: i for i, n in enumerate(FORMATS)}
 IQ_F32, IQ_BF16 = 0, 1
 EXPORTS = ("iq_format_info", "iq_imatrix_workspace_size", "iq_imatrix_accumulate", "iq_imatrix_weights",
-           "iq_anchor_scales", "iq_encode_workspace_size", "iq_encode", "iq_group_errors", "iq_decode")
+           "iq_anchor_scales", "iq_encode_workspace_size", "iq_encode", "iq_group_errors", "iq_decode",
+           "iq_encode_static_scratch_capacity", "iq_encode_static_scratch")
 
 STATUS_BITS = {
     "BAD_CHOICE": 1, "BAD_EXPERT_ID": 2, "NONFINITE_SUM2": 4, "DUP_EXPERT_ID": 8, "BAD_INPUT": 16,
@@ -55,6 +56,8 @@ def lib():
         L.iq_encode.argtypes = [i32, p, i32, i64, i64, p, i64, p, p, p, p, p, p, p, sz, p]
         L.iq_group_errors.argtypes = [i32, p, i32, i64, i64, p, i64, p, p, p, p, p, sz, p]
         L.iq_decode.argtypes = [i32, p, i64, i64, p, p, i32, p]
+        L.iq_encode_static_scratch_capacity.argtypes = [i32, ctypes.POINTER(i64)]
+        L.iq_encode_static_scratch.argtypes = [i32, p, i32, i64, i64, p, i64, p, p, p, p, p, p, p]
         for n in EXPORTS:
             getattr(L, n).restype = ctypes.c_int
         _lib = L
@@ -195,3 +198,32 @@ def decode(fmt, payload, rows, cols, grid, dtype=torch.float32, out=None):
     _check(lib().iq_decode(FMT_ID[fmt], _p(payload), rows, cols, _p(grid), _p(out), _dt(out),
                            _stream(payload.device)), "iq_decode")
     return out
+
+
+def encode_static_scratch_capacity(fmt: str) -> int:
+    """Largest number of 256-value blocks iq_encode_static_scratch accepts for ``fmt``."""
+    n = ctypes.c_int64()
+    _check(lib().iq_encode_static_scratch_capacity(FMT_ID[fmt], ctypes.byref(n)), "iq_encode_static_scratch_capacity")
+    return n.value
+
+
+def encode_static_scratch(fmt, W, grid, importance=None, rows_per_expert=0, d16=None, choices=None,
+                          every_choice=False, status=None, payload=None, table=None):
+    """iq_encode for callers that cannot allocate device scratch: the library's own fixed 1 MiB
+    device array replaces the workspace (outputs are still the caller's).  Raises IQError with code
+    -4 when the weight needs more scratch than that array holds."""
+    for t, n in ((W, "W"), (grid, "grid"), (importance, "importance"), (d16, "d16"), (choices, "choices")):
+        _cuda(t, n)
+    info = format_info(fmt)
+    R, C = W.shape
+    B = R * (C // 256)
+    dev = W.device
+    if payload is None:
+        payload = torch.empty(B, info["block_bytes"], dtype=torch.uint8, device=dev)
+    if every_choice and table is None:
+        table = torch.empty(B, info["choice_groups"], info["num_choices"], dtype=torch.float32, device=dev)
+    _check(lib().iq_encode_static_scratch(FMT_ID[fmt], _p(W), _dt(W), R, C, _p(importance), int(rows_per_expert),
+                                          _p(grid), _p(d16), _p(choices), _p(payload),
+                                          _p(table if every_choice else None), _p(status), _stream(dev)),
+           "iq_encode_static_scratch")
+    return (payload, table) if every_choice else payload

@@ -26,6 +26,8 @@
 // candidate the bound cannot exclude with the direct fp64 form sum_i w_i (x_i - q_i)^2 of the
 // decoded values q, then takes the exact minimum with the lowest (choice) / (delta bit, entry) on
 // equal error.
+#include <mutex>
+
 #include "iq_common.cuh"
 
 namespace iqk {
@@ -800,4 +802,64 @@ extern "C" int iq_format_info(iq_format f, iq_format_info_t *out) {
   out->vectors_per_group = V[f];
   out->index_bits = bits[f];
   return IQ_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Encoder for callers that cannot allocate device memory.
+//
+// Some callers are not allowed to call cudaMalloc, or to take memory from a caching allocator:
+// code that runs while a stream is being captured into a CUDA graph in the global capture mode
+// (where cudaMalloc is refused), plug-ins loaded into a host framework that owns every byte of
+// device memory through its own pool, and latency-bound serving loops that may not block on an
+// allocation.  They still own their inputs and outputs, but cannot provide the scratch
+// `workspace` that iq_encode needs.  This entry point takes its scratch from one file-scope
+// device array instead.
+//
+// The array is kStaticScratchBytes (1 MiB) per GPU, held by every device that loads the library
+// until the process exits.  Every call on a device shares it: the header the kernels count in is
+// cleared by each call before use, and calls whose kernels overlap on the GPU (for example on two
+// streams) race on it, so issue them in order on one stream.
+namespace iqk {
+constexpr size_t kStaticScratchBytes = (size_t)1 << 20;
+static __device__ __align__(256) uint8_t g_encode_scratch[kStaticScratchBytes];
+
+// Device address of g_encode_scratch on the current device.  In host code the array's name is
+// only a host-side stand-in, so the address is looked up once per device with cudaGetSymbolAddress
+// (the first call on a device does this; make that first call before any stream capture).
+static void *static_scratch_ptr() {
+  constexpr int kMaxDevices = 64;
+  static void *ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_encode_scratch) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+}  // namespace iqk
+
+extern "C" int iq_encode_static_scratch_capacity(iq_format f, int64_t *max_blocks) {
+  if ((unsigned)f > IQ1_M || !max_blocks) return IQ_ERR_ARG;
+  const size_t fixed = 256 + al256((size_t)grid_entries(f) * 64);
+  *max_blocks = (int64_t)((kStaticScratchBytes - fixed) / 8);
+  return IQ_OK;
+}
+
+extern "C" int iq_encode_static_scratch(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                                        const float *importance, int64_t rows_per_expert, const float *grid,
+                                        const uint16_t *d16, const uint8_t *choices, uint8_t *payload,
+                                        float *group_errors, int32_t *status, void *stream) {
+  int rc = check_common(f, W, dt, rows, cols, importance, rows_per_expert, grid);
+  if (rc) return rc;
+  size_t need = 0;
+  iq_encode_workspace_size(f, rows, cols, &need);
+  if (need > kStaticScratchBytes) return IQ_ERR_TOO_LARGE;
+  void *ws = static_scratch_ptr();
+  if (!ws) return IQ_ERR_CUDA;
+  return iq_encode(f, W, dt, rows, cols, importance, rows_per_expert, grid, d16, choices, payload, group_errors,
+                   status, ws, kStaticScratchBytes, stream);
 }

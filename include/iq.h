@@ -49,7 +49,8 @@ enum {
   IQ_OK = 0,
   IQ_ERR_ARG = -1,       /* null / misaligned pointer, bad size or enum, cols % 256 != 0, ... */
   IQ_ERR_CUDA = -2,      /* a CUDA call or launch failed */
-  IQ_ERR_WORKSPACE = -3  /* workspace missing or smaller than the reported size */
+  IQ_ERR_WORKSPACE = -3, /* workspace missing or smaller than the reported size */
+  IQ_ERR_TOO_LARGE = -4  /* the problem needs more scratch than the fixed static array holds */
 };
 
 /* Bits OR-ed into *status by the kernels. */
@@ -170,6 +171,27 @@ IQ_API int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows
                     const float *importance, int64_t rows_per_expert, const float *grid, const uint16_t *d16,
                     float *group_errors, int32_t *status, void *workspace, size_t workspace_bytes,
                     void *stream);
+
+/* ---- encoder without caller-provided scratch --------------------------------------------------
+ * No counterpart on the pages: this is an addition for callers that cannot allocate device memory
+ * (code running under CUDA-graph stream capture in the global mode, where cudaMalloc is refused;
+ * plug-ins inside a framework that owns all device memory through its own pool; serving loops that
+ * may not block on an allocation).  Same arguments and results as iq_encode, minus the workspace:
+ * the scratch is one file-scope 1 MiB device array per GPU, kept until the process exits.
+ *  - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *  - Size limit: a problem whose iq_encode_workspace_size exceeds 1 MiB returns IQ_ERR_TOO_LARGE
+ *    before anything is launched; iq_encode_static_scratch_capacity gives the largest block count
+ *    per format (114,656 blocks of 256 values for IQ1_S / IQ1_M, 128,992 for IQ2_XXS).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress); make
+ *    that first call before any stream capture.
+ *  - Calls on one device share the array: each call clears what must start at zero, and calls
+ *    whose kernels overlap on the GPU (e.g. on two streams) race, so keep them in order on one
+ *    stream. */
+IQ_API int iq_encode_static_scratch_capacity(iq_format f, int64_t *max_blocks);
+IQ_API int iq_encode_static_scratch(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                             const float *importance, int64_t rows_per_expert, const float *grid,
+                             const uint16_t *d16, const uint8_t *choices, uint8_t *payload, float *group_errors,
+                             int32_t *status, void *stream);
 
 /* ---- decoder ([formats]: the value rule above) ------------------------------------------------
  * out[rows, cols] (device; IQ_F32, or IQ_BF16 rounded to nearest even) from payload [B,
