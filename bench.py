@@ -38,7 +38,8 @@ BPW = {"IQ2_XXS": 2.0625, "IQ2_XS": 2.3125, "IQ2_S": 2.5625, "IQ1_S": 1.5625, "I
 CONFIG = {"workload": "encode 5632x2048 bf16 weight in IQ2_XXS/IQ2_XS/IQ2_S/IQ1_S/IQ1_M (searched + every-choice "
                       "table, fixed choice 7, decode) with importance from a 4096x2048 bf16 imatrix pass",
           "rows": R, "cols": C, "activation_rows": T_ACT, "rows_per_chunk": 1024,
-          "l2": "flushed before every timed step (512 MiB write); inputs 23 MiB + 16 MiB < L2"}
+          "l2": "flushed before every timed step (512 MiB write); inputs 23 MiB + 16 MiB < L2",
+          "timing": "one CUDA graph of the whole step per timed step, CUDA events on the launching stream"}
 
 
 MOE_T, MOE_C, MOE_E, MOE_K = 4096, 17408, 128, 8
@@ -213,50 +214,76 @@ def run_ours(args):
     ws_im = api.imatrix_workspace(T_ACT, C, torch.bfloat16, 1, 1, 1024, dev)
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    names = ["imatrix", "weights"] + [f"{k}:{f}" for f in FORMATS for k in ("encode", "fixed", "decode")]
+    wbuf = {}
 
-    def step(evs=None):
-        def mark(i):
-            if evs is not None:
-                evs[i].record(stream)
-        mark(0)
+    def c_imatrix():
         s2.zero_(); cn.zero_()
         api.imatrix_accumulate(X, ids, 1, 1024, s2, cn, status=st, workspace=ws_im)
-        mark(1)
-        w = api.imatrix_weights(s2, cn)
-        mark(2)
-        i = 2
-        for f in FORMATS:
-            api.encode(f, W, G[f], importance=w[0], status=st, payload=pay[f], table=tbl[f], every_choice=True,
-                       workspace=ws[f])
-            mark(i + 1)
-            api.encode(f, W, G[f], importance=w[0], choices=ch7[f], status=st, payload=pay7[f], workspace=ws[f])
-            mark(i + 2)
-            api.decode(f, pay[f], R, C, G[f], out=dec)
-            mark(i + 3)
-            i += 3
 
-    nev = 2 + 3 * len(FORMATS) + 1
-    for _ in range(args.warmup):
+    def c_weights():
+        wbuf["w"] = api.imatrix_weights(s2, cn)
+
+    def c_encode(f):
+        api.encode(f, W, G[f], importance=wbuf["w"][0], status=st, payload=pay[f], table=tbl[f], every_choice=True,
+                   workspace=ws[f])
+
+    def c_fixed(f):
+        api.encode(f, W, G[f], importance=wbuf["w"][0], choices=ch7[f], status=st, payload=pay7[f], workspace=ws[f])
+
+    def c_decode(f):
+        api.decode(f, pay[f], R, C, G[f], out=dec)
+
+    parts = [("imatrix", c_imatrix), ("weights", c_weights)]
+    for f in FORMATS:
+        parts += [(f"encode:{f}", lambda f=f: c_encode(f)), (f"fixed:{f}", lambda f=f: c_fixed(f)),
+                  (f"decode:{f}", lambda f=f: c_decode(f))]
+
+    def step():
+        for _, fn in parts:
+            fn()
+
+    for _ in range(args.warmup):                       # eager warm-up (loads modules, sets attributes)
         step()
+    torch.cuda.synchronize()
+    # The step and each of its calls are captured as CUDA graphs: a replay runs exactly the
+    # library's kernels of the step with no host launch gaps.
+    g_step = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step):
+        step()
+    g_part = {}
+    for name, fn in parts:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        g_part[name] = g
+    for _ in range(2):
+        g_step.replay()
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    per = {n: [] for n in names}
+
+    def timed(g):
+        flush.fill_(1)                                 # L2 flushed before every timed replay
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        return a, b
+
     totals = []
     with Clocks() as clk:
         torch.cuda.synchronize()
-        for _ in range(args.steps):
-            flush.fill_(1)
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(nev)]
-            step(evs)
-            torch.cuda.synchronize()
-            for k, n in enumerate(names):
-                per[n].append(evs[k].elapsed_time(evs[k + 1]))
-            totals.append(evs[0].elapsed_time(evs[-1]))
+        evs = [timed(g_step) for _ in range(args.steps)]
         torch.cuda.synchronize()
+        totals = [a.elapsed_time(b) for a, b in evs]
     if dist:
         dist.barrier()
+    per = {n: [] for n, _ in parts}
+    for _ in range(max(3, args.steps)):
+        evs = {n: timed(g_part[n]) for n, _ in parts}
+        torch.cuda.synchronize()
+        for n, (a, b) in evs.items():
+            per[n].append(a.elapsed_time(b))
     ms = float(np.mean(totals))
     if dist:
         t = torch.tensor([ms], device=dev)
@@ -332,12 +359,16 @@ def measure_imatrix_moe(args, dev, flush, hbm):
     stream = torch.cuda.current_stream(dev)
     for _ in range(3):
         api.imatrix_accumulate(X, ids, MOE_E, 1024, s2, cn, workspace=ws)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        api.imatrix_accumulate(X, ids, MOE_E, 1024, s2, cn, workspace=ws)
     times = []
     for _ in range(max(5, args.steps)):
         flush.fill_(2)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        api.imatrix_accumulate(X, ids, MOE_E, 1024, s2, cn, workspace=ws)
+        g.replay()
         b.record(stream)
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))

@@ -65,6 +65,12 @@ struct EncArgs {
 };
 
 // ---------------------------------------------------------------------------------------------
+// Prepared codebook, pair-interleaved: entries 2p and 2p+1 occupy 128 bytes as sixteen packed
+// pairs, (g_2p[i], g_2p+1[i]) for i = 0..7, then (h_2p[i], h_2p+1[i]) with h = g^2 (IQ2) or |g|
+// (IQ1).  One fma.rn.f32x2 then advances the dot products of two entries at once.
+__host__ __device__ __forceinline__ int tab_g(int e, int i) { return (e >> 1) * 32 + 2 * i + (e & 1); }
+__host__ __device__ __forceinline__ int tab_h(int e, int i) { return (e >> 1) * 32 + 16 + 2 * i + (e & 1); }
+
 template <int F>
 __global__ void prep_codebook(const float *__restrict__ grid, EncWs ws) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
@@ -72,22 +78,51 @@ __global__ void prep_codebook(const float *__restrict__ grid, EncWs ws) {
   float g[8];
   load8(grid + 8 * e, g);
   bool ok = true;
-  float h[8];
+  float *tf = reinterpret_cast<float *>(ws.tab);
 #pragma unroll
   for (int i = 0; i < 8; i++) {
+    float h;
     if (Fmt<F>::IQ1) {
       ok &= (g[i] == -1.0f || g[i] == 0.0f || g[i] == 1.0f);
-      h[i] = fabsf(g[i]);
+      h = fabsf(g[i]);
     } else {
       ok &= (g[i] >= 1.0f && g[i] <= 127.0f && g[i] == floorf(g[i]));
-      h[i] = g[i] * g[i];
+      h = g[i] * g[i];  // exact: at most 14 bits
     }
+    tf[tab_g(e, i)] = g[i];
+    tf[tab_h(e, i)] = h;
   }
   if (!ok) atomicOr(&ws.hdr[0], 1);
-  ws.tab[4 * e + 0] = make_float4(g[0], g[1], g[2], g[3]);
-  ws.tab[4 * e + 1] = make_float4(g[4], g[5], g[6], g[7]);
-  ws.tab[4 * e + 2] = make_float4(h[0], h[1], h[2], h[3]);
-  ws.tab[4 * e + 3] = make_float4(h[4], h[5], h[6], h[7]);
+}
+
+struct Entry { float g[8], h[8]; };
+__device__ __forceinline__ void load_entry(const float4 *tab, int e, Entry &en) {
+  const float *tf = reinterpret_cast<const float *>(tab);
+#pragma unroll
+  for (int i = 0; i < 8; i++) { en.g[i] = tf[tab_g(e, i)]; en.h[i] = tf[tab_h(e, i)]; }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Packed f32x2 arithmetic (two IEEE fp32 operations per instruction, each rounded on its own).
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 up2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ float min3f(float a, float b, float c) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -123,38 +158,89 @@ __device__ __forceinline__ void vec_setup(Vec &v) {
   v.Cs = cs; v.nT2 = nt; v.Ws = ws;
 }
 
-// A and B of one codebook entry (IQ2): An = -2 A, B = sum w g^2.
-__device__ __forceinline__ void ab2(const float *nw2, const float *w, const float4 *te, float &An, float &B) {
-  const float4 g0 = te[0], g1 = te[1], q0 = te[2], q1 = te[3];
-  An = __fmul_rn(nw2[0], g0.x);
-  An = __fmaf_rn(nw2[1], g0.y, An); An = __fmaf_rn(nw2[2], g0.z, An); An = __fmaf_rn(nw2[3], g0.w, An);
-  An = __fmaf_rn(nw2[4], g1.x, An); An = __fmaf_rn(nw2[5], g1.y, An); An = __fmaf_rn(nw2[6], g1.z, An);
-  An = __fmaf_rn(nw2[7], g1.w, An);
-  B = __fmul_rn(w[0], q0.x);
-  B = __fmaf_rn(w[1], q0.y, B); B = __fmaf_rn(w[2], q0.z, B); B = __fmaf_rn(w[3], q0.w, B);
-  B = __fmaf_rn(w[4], q1.x, B); B = __fmaf_rn(w[5], q1.y, B); B = __fmaf_rn(w[6], q1.z, B);
-  B = __fmaf_rn(w[7], q1.w, B);
+// The per-entry sums, scalar (rescoring) and packed over an entry pair (sweeps).  Both evaluate
+// the same rounded operations in the same order, so their fp32 values agree bit for bit:
+//   An = -2 sum w t g   (first product rounded, then a chain of FMAs over i = 1..7)
+//   B  = sum w h        (IQ2: h = g^2, IQ1: h = |g| = g^2)
+//   Cg = sum w g        (IQ1)
+// and for IQ1 the sums of the shifted values g + delta, delta = +-1/8:
+//   Anp/Anm = An +- nT2/8,   Bp/Bm = (B + Ws/64) +- Cg/4.
+__device__ __forceinline__ void ab2(const float *nw2, const float *w, const Entry &en, float &An, float &B) {
+  An = __fmul_rn(nw2[0], en.g[0]);
+  B = __fmul_rn(w[0], en.h[0]);
+#pragma unroll
+  for (int i = 1; i < 8; i++) { An = __fmaf_rn(nw2[i], en.g[i], An); B = __fmaf_rn(w[i], en.h[i], B); }
 }
-// IQ1: shifted sums for delta = +1/8 (p) and -1/8 (m).
-__device__ __forceinline__ void ab1(const Vec &v, const float4 *te, float &Anp, float &Bp, float &Anm, float &Bm) {
-  const float4 g0 = te[0], g1 = te[1], a0 = te[2], a1 = te[3];
-  float An = __fmul_rn(v.nw2[0], g0.x);
-  An = __fmaf_rn(v.nw2[1], g0.y, An); An = __fmaf_rn(v.nw2[2], g0.z, An); An = __fmaf_rn(v.nw2[3], g0.w, An);
-  An = __fmaf_rn(v.nw2[4], g1.x, An); An = __fmaf_rn(v.nw2[5], g1.y, An); An = __fmaf_rn(v.nw2[6], g1.z, An);
-  An = __fmaf_rn(v.nw2[7], g1.w, An);
-  float Cg = __fmul_rn(v.w[0], g0.x);
-  Cg = __fmaf_rn(v.w[1], g0.y, Cg); Cg = __fmaf_rn(v.w[2], g0.z, Cg); Cg = __fmaf_rn(v.w[3], g0.w, Cg);
-  Cg = __fmaf_rn(v.w[4], g1.x, Cg); Cg = __fmaf_rn(v.w[5], g1.y, Cg); Cg = __fmaf_rn(v.w[6], g1.z, Cg);
-  Cg = __fmaf_rn(v.w[7], g1.w, Cg);
-  float B = __fmul_rn(v.w[0], a0.x);
-  B = __fmaf_rn(v.w[1], a0.y, B); B = __fmaf_rn(v.w[2], a0.z, B); B = __fmaf_rn(v.w[3], a0.w, B);
-  B = __fmaf_rn(v.w[4], a1.x, B); B = __fmaf_rn(v.w[5], a1.y, B); B = __fmaf_rn(v.w[6], a1.z, B);
-  B = __fmaf_rn(v.w[7], a1.w, B);
+__device__ __forceinline__ void ab1(const Vec &v, const Entry &en, float &Anp, float &Bp, float &Anm, float &Bm) {
+  float An = __fmul_rn(v.nw2[0], en.g[0]), Cg = __fmul_rn(v.w[0], en.g[0]), B = __fmul_rn(v.w[0], en.h[0]);
+#pragma unroll
+  for (int i = 1; i < 8; i++) {
+    An = __fmaf_rn(v.nw2[i], en.g[i], An);
+    Cg = __fmaf_rn(v.w[i], en.g[i], Cg);
+    B = __fmaf_rn(v.w[i], en.h[i], B);
+  }
   Anp = __fmaf_rn(0.125f, v.nT2, An);
   Anm = __fmaf_rn(-0.125f, v.nT2, An);
   const float Bw = __fmaf_rn(0.015625f, v.Ws, B);
   Bp = __fmaf_rn(0.25f, Cg, Bw);
   Bm = __fmaf_rn(-0.25f, Cg, Bw);
+}
+
+// Packed per-vector operands of the sweeps: every scalar duplicated into both halves of a pair.
+struct VecP {
+  uint64_t nw2[8], w[8];
+  uint64_t nT2, Ws;
+};
+__device__ __forceinline__ VecP vec_pack(const Vec &v) {
+  VecP p;
+#pragma unroll
+  for (int i = 0; i < 8; i++) { p.nw2[i] = pk2(v.nw2[i], v.nw2[i]); p.w[i] = pk2(v.w[i], v.w[i]); }
+  p.nT2 = pk2(v.nT2, v.nT2);
+  p.Ws = pk2(v.Ws, v.Ws);
+  return p;
+}
+
+// Sums of an entry pair from its 128 bytes of the shared-memory table.
+__device__ __forceinline__ void ab2_pair(const VecP &vp, const uint64_t *T, uint64_t &An, uint64_t &B) {
+  const ulonglong2 *Q = reinterpret_cast<const ulonglong2 *>(T);
+  const ulonglong2 g01 = Q[0], g23 = Q[1], g45 = Q[2], g67 = Q[3];
+  const ulonglong2 h01 = Q[4], h23 = Q[5], h45 = Q[6], h67 = Q[7];
+  const uint64_t zero = 0ull;
+  An = ffma2(vp.nw2[0], g01.x, zero);
+  B = ffma2(vp.w[0], h01.x, zero);
+  An = ffma2(vp.nw2[1], g01.y, An); B = ffma2(vp.w[1], h01.y, B);
+  An = ffma2(vp.nw2[2], g23.x, An); B = ffma2(vp.w[2], h23.x, B);
+  An = ffma2(vp.nw2[3], g23.y, An); B = ffma2(vp.w[3], h23.y, B);
+  An = ffma2(vp.nw2[4], g45.x, An); B = ffma2(vp.w[4], h45.x, B);
+  An = ffma2(vp.nw2[5], g45.y, An); B = ffma2(vp.w[5], h45.y, B);
+  An = ffma2(vp.nw2[6], g67.x, An); B = ffma2(vp.w[6], h67.x, B);
+  An = ffma2(vp.nw2[7], g67.y, An); B = ffma2(vp.w[7], h67.y, B);
+}
+struct IQ1Const { uint64_t p125, m125, p025, m025, w64; };
+__device__ __forceinline__ IQ1Const iq1_consts() {
+  return {pk2(0.125f, 0.125f), pk2(-0.125f, -0.125f), pk2(0.25f, 0.25f), pk2(-0.25f, -0.25f),
+          pk2(0.015625f, 0.015625f)};
+}
+// IQ1: the An and B sums of the two shifts (An +- nT2/8, B + Ws/64 +- Cg/4) for an entry pair.
+__device__ __forceinline__ void ab1_pair(const VecP &vp, const IQ1Const &k, const uint64_t *T, uint64_t &Anp,
+                                         uint64_t &Bp, uint64_t &Anm, uint64_t &Bm) {
+  const ulonglong2 *Q = reinterpret_cast<const ulonglong2 *>(T);
+  const ulonglong2 g01 = Q[0], g23 = Q[1], g45 = Q[2], g67 = Q[3];
+  const ulonglong2 h01 = Q[4], h23 = Q[5], h45 = Q[6], h67 = Q[7];
+  const uint64_t zero = 0ull;
+  uint64_t An = ffma2(vp.nw2[0], g01.x, zero), Cg = ffma2(vp.w[0], g01.x, zero), B = ffma2(vp.w[0], h01.x, zero);
+  An = ffma2(vp.nw2[1], g01.y, An); Cg = ffma2(vp.w[1], g01.y, Cg); B = ffma2(vp.w[1], h01.y, B);
+  An = ffma2(vp.nw2[2], g23.x, An); Cg = ffma2(vp.w[2], g23.x, Cg); B = ffma2(vp.w[2], h23.x, B);
+  An = ffma2(vp.nw2[3], g23.y, An); Cg = ffma2(vp.w[3], g23.y, Cg); B = ffma2(vp.w[3], h23.y, B);
+  An = ffma2(vp.nw2[4], g45.x, An); Cg = ffma2(vp.w[4], g45.x, Cg); B = ffma2(vp.w[4], h45.x, B);
+  An = ffma2(vp.nw2[5], g45.y, An); Cg = ffma2(vp.w[5], g45.y, Cg); B = ffma2(vp.w[5], h45.y, B);
+  An = ffma2(vp.nw2[6], g67.x, An); Cg = ffma2(vp.w[6], g67.x, Cg); B = ffma2(vp.w[6], h67.x, B);
+  An = ffma2(vp.nw2[7], g67.y, An); Cg = ffma2(vp.w[7], g67.y, Cg); B = ffma2(vp.w[7], h67.y, B);
+  Anp = ffma2(k.p125, vp.nT2, An);
+  Anm = ffma2(k.m125, vp.nT2, An);
+  const uint64_t Bw = ffma2(k.w64, vp.Ws, B);
+  Bp = ffma2(k.p025, Cg, Bw);
+  Bm = ffma2(k.m025, Cg, Bw);
 }
 
 // local scale multipliers: IQ2 alpha_s = d * (2s+1) / 8, IQ1 alpha_s = d * (2s+1) (both exact)
@@ -166,35 +252,56 @@ template <int F> __device__ __forceinline__ float alpha_choice(float d, int c) {
   return alpha_of<F>(d, F == IQ1_S ? (c & 7) : c);
 }
 
-// Sweep 1: per choice, the minimum over the vector's candidates of the scaled score s.
+// Sweep 1: per choice, the minimum over the vector's candidates of the scaled score
+// s = alpha * B + An (the error is Cs + alpha * s).
 template <int F>
 __device__ __forceinline__ void sweep_minima(const Vec &v, const float4 *tab, const float *al, float *m) {
   constexpr int C = Fmt<F>::C, N = Fmt<F>::N;
+  constexpr int NS = Fmt<F>::IQ1 ? 8 : 16;
+  const VecP vp = vec_pack(v);
+  uint64_t alp[NS];
+#pragma unroll
+  for (int s = 0; s < NS; s++) alp[s] = pk2(al[s], al[s]);
 #pragma unroll
   for (int c = 0; c < C; c++) m[c] = INFINITY;
+  const uint64_t *T = reinterpret_cast<const uint64_t *>(tab);
+  if (!Fmt<F>::IQ1) {
 #pragma unroll 2
-  for (int e = 0; e < N; e++) {
-    const float4 *te = tab + 4 * e;
-    if (!Fmt<F>::IQ1) {
-      float An, B;
-      ab2(v.nw2, v.w, te, An, B);
+    for (int pr = 0; pr < N / 2; pr++) {
+      uint64_t An, B;
+      ab2_pair(vp, T + 16 * pr, An, B);
 #pragma unroll
-      for (int c = 0; c < C; c++) m[c] = fminf(m[c], __fmaf_rn(al[c], B, An));
-    } else {
-      float Anp, Bp, Anm, Bm;
-      ab1(v, te, Anp, Bp, Anm, Bm);
-      if (F == IQ1_S) {
+      for (int c = 0; c < C; c++) {
+        const float2 sc = up2(ffma2(alp[c], B, An));
+        m[c] = min3f(m[c], sc.x, sc.y);
+      }
+    }
+  } else {
+    const IQ1Const k = iq1_consts();
+#pragma unroll 1
+    for (int pr = 0; pr < N / 2; pr++) {
+      uint64_t Anp, Bp, Anm, Bm;
+      ab1_pair(vp, k, T + 16 * pr, Anp, Bp, Anm, Bm);
 #pragma unroll
-        for (int s = 0; s < 8; s++) {
-          m[s] = fminf(m[s], __fmaf_rn(al[s], Bp, Anp));
-          m[8 + s] = fminf(m[8 + s], __fmaf_rn(al[s], Bm, Anm));
+      for (int s = 0; s < 8; s++) {
+        const float2 sp = up2(ffma2(alp[s], Bp, Anp)), sm = up2(ffma2(alp[s], Bm, Anm));
+        if (F == IQ1_S) {
+          m[s] = min3f(m[s], sp.x, sp.y);
+          m[8 + s] = min3f(m[8 + s], sm.x, sm.y);
+        } else {
+          m[s] = min3f(min3f(m[s], sp.x, sp.y), sm.x, sm.y);
         }
-      } else {
-#pragma unroll
-        for (int s = 0; s < 8; s++) m[s] = fminf(m[s], fminf(__fmaf_rn(al[s], Bp, Anp), __fmaf_rn(al[s], Bm, Anm)));
       }
     }
   }
+}
+
+// best / runner-up / key over a pair of candidates (keys ka and ka + 1)
+__device__ __forceinline__ void track2(float2 sc, int ka, float &best, float &second, int &key) {
+  const float lo = fminf(sc.x, sc.y), hi = fmaxf(sc.x, sc.y);
+  const int klo = sc.y < sc.x ? ka + 1 : ka;
+  second = min3f(second, hi, fmaxf(best, lo));
+  if (lo < best) { best = lo; key = klo; }
 }
 
 // Sweep 2: under one choice, the best candidate key and the best and runner-up scores.
@@ -204,28 +311,28 @@ __device__ __forceinline__ void sweep_pick(const Vec &v, const float4 *tab, floa
                                            float &second, int &key) {
   constexpr int N = Fmt<F>::N;
   best = INFINITY; second = INFINITY; key = 0;
+  const VecP vp = vec_pack(v);
+  const uint64_t al = pk2(alpha, alpha);
+  const uint64_t *T = reinterpret_cast<const uint64_t *>(tab);
+  if (!Fmt<F>::IQ1) {
 #pragma unroll 2
-  for (int e = 0; e < N; e++) {
-    const float4 *te = tab + 4 * e;
-    if (!Fmt<F>::IQ1) {
-      float An, B;
-      ab2(v.nw2, v.w, te, An, B);
-      const float s = __fmaf_rn(alpha, B, An);
-      second = fminf(second, fmaxf(best, s));
-      if (s < best) { best = s; key = e; }
-    } else {
-      float Anp, Bp, Anm, Bm;
-      ab1(v, te, Anp, Bp, Anm, Bm);
+    for (int pr = 0; pr < N / 2; pr++) {
+      uint64_t An, B;
+      ab2_pair(vp, T + 16 * pr, An, B);
+      track2(up2(ffma2(al, B, An)), 2 * pr, best, second, key);
+    }
+  } else {
+    const IQ1Const k = iq1_consts();
+#pragma unroll 1
+    for (int pr = 0; pr < N / 2; pr++) {
+      uint64_t Anp, Bp, Anm, Bm;
+      ab1_pair(vp, k, T + 16 * pr, Anp, Bp, Anm, Bm);
       if (F == IQ1_S) {
-        const float s = dbit_fixed ? __fmaf_rn(alpha, Bm, Anm) : __fmaf_rn(alpha, Bp, Anp);
-        second = fminf(second, fmaxf(best, s));
-        if (s < best) { best = s; key = e; }
+        const uint64_t sc = dbit_fixed ? ffma2(al, Bm, Anm) : ffma2(al, Bp, Anp);
+        track2(up2(sc), 2 * pr, best, second, key);
       } else {
-        const float s0 = __fmaf_rn(alpha, Bp, Anp), s1 = __fmaf_rn(alpha, Bm, Anm);
-        second = fminf(second, fmaxf(best, s0));
-        if (s0 < best) { best = s0; key = e; }
-        second = fminf(second, fmaxf(best, s1));
-        if (s1 < best) { best = s1; key = N + e; }
+        track2(up2(ffma2(al, Bp, Anp)), 2 * pr, best, second, key);
+        track2(up2(ffma2(al, Bm, Anm)), N + 2 * pr, best, second, key);
       }
     }
   }
@@ -423,16 +530,14 @@ __global__ void __launch_bounds__(THREADS, 1) encode_kernel(EncArgs a, EncWs ws)
 // ---------------------------------------------------------------------------------------------
 // Exact rescoring of flagged groups.
 template <int F>
-__device__ __forceinline__ double exact_err(const float *x, const float *w, const float4 *te, float d, int s, int sgn,
+__device__ __forceinline__ double exact_err(const float *x, const float *w, const Entry &en, float d, int s, int sgn,
                                             int dbit) {
-  const float4 g0 = __ldg(te), g1 = __ldg(te + 1);
-  const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   double acc = 0.0;
   if (!Fmt<F>::IQ1) {
     const float dl = __fmul_rn(__fmul_rn(d, (float)(2 * s + 1)), 0.125f);
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-      float q = __fmul_rn(dl, g[i]);
+      float q = __fmul_rn(dl, en.g[i]);
       q = ((sgn >> i) & 1) ? -q : q;
       const double df = __dsub_rn((double)x[i], (double)q);
       acc = __dadd_rn(acc, __dmul_rn((double)w[i], __dmul_rn(df, df)));
@@ -442,7 +547,7 @@ __device__ __forceinline__ double exact_err(const float *x, const float *w, cons
     const float delta = dbit ? -0.125f : 0.125f;
 #pragma unroll
     for (int i = 0; i < 8; i++) {
-      const float q = __fmul_rn(dl, __fadd_rn(g[i], delta));
+      const float q = __fmul_rn(dl, __fadd_rn(en.g[i], delta));
       const double df = __dsub_rn((double)x[i], (double)q);
       acc = __dadd_rn(acc, __dmul_rn((double)w[i], __dmul_rn(df, df)));
     }
@@ -465,16 +570,16 @@ __device__ __forceinline__ Vec shfl_vec(const Vec &v, int src) {
   return r;
 }
 
-// the fp32 score of candidate (entry e, delta bit db) under alpha, computed exactly as the sweep does
+// the fp32 score of candidate (entry en, delta bit db) under alpha, computed exactly as the sweep does
 template <int F>
-__device__ __forceinline__ float cand_score(const Vec &v, const float4 *te, float alpha, int db) {
+__device__ __forceinline__ float cand_score(const Vec &v, const Entry &en, float alpha, int db) {
   if (!Fmt<F>::IQ1) {
     float An, B;
-    ab2(v.nw2, v.w, te, An, B);
+    ab2(v.nw2, v.w, en, An, B);
     return __fmaf_rn(alpha, B, An);
   } else {
     float Anp, Bp, Anm, Bm;
-    ab1(v, te, Anp, Bp, Anm, Bm);
+    ab1(v, en, Anp, Bp, Anm, Bm);
     return db ? __fmaf_rn(alpha, Bm, Anm) : __fmaf_rn(alpha, Bp, Anp);
   }
 }
@@ -532,14 +637,16 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
 #pragma unroll
         for (int c = 0; c < C; c++) lm[c] = INFINITY;
         for (int e = lane; e < N; e += 32) {
+          Entry en;
+          load_entry(tab, e, en);
 #pragma unroll
           for (int c = 0; c < C; c++) {
             if (MODE == MODE_FIXED && c != cfix) continue;
             int s, db0, db1;
             cand_of_choice<F>(c, s, db0, db1);
             const float al = alpha_of<F>(d, s);
-            lm[c] = fminf(lm[c], cand_score<F>(u, tab + 4 * e, al, db0));
-            if (db1 != db0) lm[c] = fminf(lm[c], cand_score<F>(u, tab + 4 * e, al, db1));
+            lm[c] = fminf(lm[c], cand_score<F>(u, en, al, db0));
+            if (db1 != db0) lm[c] = fminf(lm[c], cand_score<F>(u, en, al, db1));
           }
         }
 #pragma unroll
@@ -579,11 +686,13 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
           double bestE = INFINITY;
           int bestK = 0x7fffffff;
           for (int e = lane; e < N; e += 32) {
+            Entry en;
+            load_entry(tab, e, en);
             for (int db = db0; db <= db1; db++) {
-              const float sc = cand_score<F>(u, tab + 4 * e, al, db);
+              const float sc = cand_score<F>(u, en, al, db);
               const float ec = __fmul_rn(al, sc);
               if (__fsub_rn(ec, emin) <= kMargin * (4.0f * u.Cs + emin + ec)) {
-                const double E = exact_err<F>(u.x, u.w, tab + 4 * e, d, s, u.sgn, db);
+                const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
                 const int kk = (F == IQ1_M ? db * N : 0) + e;
                 if (E < bestE || (E == bestE && kk < bestK)) { bestE = E; bestK = kk; }
               }

@@ -12,16 +12,20 @@
 //
 // Kernels per call:
 //  route       one CTA per chunk: a bitmap [E][rows/32] of the chunk rows each expert receives
-//              (a token's ids are a set), per-chunk counts, list offsets (an exclusive scan over
-//              experts) and an expert order by descending count;
-//  csr         one warp per (chunk, expert): expands the bitmap into the ascending list of the
-//              expert's chunk-local rows;
+//              (a token's ids are a set) and per-chunk counts; the last chunk CTA to finish ranks
+//              the experts by their count over the whole call (the order consumer warps are dealt
+//              from, the same for every chunk so that each expert's in_sum2 row has one owner);
+//  segments    one CTA per (chunk, 128-row sub-tile): expands the bitmaps into a segment holding,
+//              for every expert, the offset of its rows and the rows themselves (one byte each,
+//              ascending), so a sub-tile's routing travels with its rows;
 //  accumulate  one CTA per column tile (128 bf16 / 64 fp32 columns, 256 bytes of a row) and,
 //              when there are too few tiles to fill the GPU, per chunk as well.  A producer warp
-//              streams the tile's rows through a 3-stage shared-memory ring with 2-D TMA tensor
-//              copies (mbarrier completion, bounded waits); each consumer warp owns up to 8
-//              experts (dealt from the count order so heavy and light experts mix), walks their
-//              row lists and keeps one register accumulator per (expert, column of its lane);
+//              streams the tile's rows through a 3-stage shared-memory ring: each stage is one 2-D
+//              TMA tensor copy of 128 rows plus one bulk copy of the sub-tile's segment, both
+//              completing on the stage's mbarrier (waits bounded by the global timer).  Each
+//              consumer warp owns up to 8 experts (dealt from the count order so heavy and light
+//              experts mix), walks their rows from shared memory only and keeps one register
+//              accumulator per (expert, column of its lane);
 //  combine     (per-chunk mode only) adds the chunk partials to in_sum2 in chunk order.
 // No atomics touch in_sum2, so the sums are the sequential definition above.
 #include <cudaTypedefs.h>
@@ -39,6 +43,7 @@ constexpr int kSlots = 8;           // experts per consumer warp
 constexpr int kMaxConsumers = 16;   // consumer warps per CTA
 constexpr int kBatch = kSlots * kMaxConsumers;  // experts per pass over x
 constexpr int kMinSeqCtas = 112;    // below this many (tile, batch) CTAs, chunks also run in parallel
+constexpr int kMaxTopK = 64;        // bounds the rows a segment holds (kSub * top_k bytes)
 
 template <typename T> struct Col;
 template <> struct Col<__nv_bfloat16> { static constexpr int CPL = 4, TILE = 128; };
@@ -46,20 +51,35 @@ template <> struct Col<float> { static constexpr int CPL = 2, TILE = 64; };
 
 __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
+__host__ __device__ inline int align16(int n) { return (n + 15) & ~15; }
+
+// A segment (one per chunk and 128-row sub-tile): int32 offsets[E + 1] (padded to 16 bytes), then
+// the rows (uint8, relative to the sub-tile) of expert 0, expert 1, ... each run ascending.
+struct SegLayout {
+  int offb;   // bytes of the offset table
+  int bytes;  // segment bytes (multiple of 16)
+};
+__host__ __device__ inline SegLayout seg_layout(int E, int top_k) {
+  SegLayout l;
+  l.offb = align16((E + 1) * 4);
+  l.bytes = l.offb + align16(kSub * (top_k < E ? top_k : E));
+  return l;
+}
+
 struct RouteWs {
-  int32_t *touched;    // [E]   experts this call routed at least one token to
+  int32_t *touched;    // [E]   experts this call routed at least one token to; [E] = chunks done
   uint32_t *bits;      // [nchunks][E][W]
   int32_t *ccount;     // [nchunks][E] tokens per (chunk, expert)
-  int32_t *order;      // [nchunks][E] experts by descending chunk count (ties: lower id)
-  int32_t *loff;       // [nchunks][E] start of the expert's list within the chunk's list
-  uint16_t *list;      // [nchunks][lcap] chunk-local rows, ascending per expert
+  int32_t *order;      // [E] experts by descending count over the call (ties: lower id)
+  uint8_t *seg;        // [nchunks][nsub] segments of seg_bytes
   float *partial;      // [nchunks][E][cols] (per-chunk mode only)
   size_t zero_bytes;   // bytes from the start to clear before the call (touched + bits)
 };
 
 struct Plan {
-  int64_t nchunks, lcap, ntiles, nbatch;
-  int W;
+  int64_t nchunks, ntiles, nbatch;
+  int W, nsub;
+  SegLayout seg;
   bool split;
 };
 
@@ -67,7 +87,8 @@ static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_
   Plan p;
   p.nchunks = (tokens + rpc - 1) / rpc;
   p.W = (int)((rpc + 31) / 32);
-  p.lcap = rpc * (int64_t)(top_k < E ? top_k : E);
+  p.nsub = (int)((rpc + kSub - 1) / kSub);
+  p.seg = seg_layout(E, top_k);
   const int tile = dt == IQ_BF16 ? Col<__nv_bfloat16>::TILE : Col<float>::TILE;
   p.ntiles = (cols + tile - 1) / tile;
   p.nbatch = (E + kBatch - 1) / kBatch;
@@ -78,19 +99,19 @@ static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_
 static RouteWs route_ws(void *ws, const Plan &p, int E, int64_t cols) {
   uint8_t *q = (uint8_t *)ws;
   RouteWs r;
-  r.touched = (int32_t *)q; q += align256((size_t)E * 4);
+  r.touched = (int32_t *)q; q += align256((size_t)(E + 1) * 4);
   r.bits = (uint32_t *)q; q += align256((size_t)p.nchunks * E * p.W * 4);
   r.zero_bytes = (size_t)(q - (uint8_t *)ws);
   r.ccount = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
-  r.order = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
-  r.loff = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
-  r.list = (uint16_t *)q; q += align256((size_t)p.nchunks * p.lcap * 2);
+  r.order = (int32_t *)q; q += align256((size_t)E * 4);
+  r.seg = q; q += align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   r.partial = p.split ? (float *)q : nullptr;
   return r;
 }
 static size_t route_ws_bytes(const Plan &p, int E, int64_t cols) {
-  size_t n = align256((size_t)E * 4) + align256((size_t)p.nchunks * E * p.W * 4) +
-             3 * align256((size_t)p.nchunks * E * 4) + align256((size_t)p.nchunks * p.lcap * 2);
+  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * p.W * 4) +
+             align256((size_t)p.nchunks * E * 4) + align256((size_t)E * 4) +
+             align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   if (p.split) n += align256((size_t)p.nchunks * E * cols * 4);
   return n;
 }
@@ -123,95 +144,142 @@ __global__ void __launch_bounds__(1024) imatrix_route(const int32_t *__restrict_
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int c = cnt[e];
-    int rank = 0;
-    for (int o = 0; o < E; o++) {
-      const int co = cnt[o];
-      rank += (co > c) || (co == c && o < e);
-    }
-    ws.order[(size_t)k * E + rank] = e;
     ws.ccount[(size_t)k * E + e] = c;
     if (c) {
       atomicAdd(&counts[e], (unsigned long long)c);
       ws.touched[e] = 1;
     }
   }
-  // exclusive scan of the chunk counts over expert ids -> list offsets (warp 0)
-  if (threadIdx.x < 32) {
+  if (st && status) atomicOr(status, st);
+  // the last chunk CTA to finish ranks the experts by their count over the whole call
+  __shared__ int last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&ws.touched[E], 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int64_t kk = 0; kk < (int64_t)gridDim.x; kk++) c += *(volatile int32_t *)&ws.ccount[(size_t)kk * E + e];
+    cnt[e] = c;
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const int c = cnt[e];
+    int rank = 0;
+    for (int o = 0; o < E; o++) {
+      const int co = cnt[o];
+      rank += (co > c) || (co == c && o < e);
+    }
+    ws.order[rank] = e;
+  }
+}
+
+// One CTA per (sub-tile s, chunk k): the segment of rows [128 s, 128 s + 128) of chunk k.
+__global__ void __launch_bounds__(1024) imatrix_segments(int E, int W, int nsub, SegLayout sl, RouteWs ws) {
+  __shared__ int cnt[1024 + 32];
+  const int s = blockIdx.x;
+  const int64_t k = blockIdx.y;
+  const int w0 = s * (kSub / 32);
+  const int nw = min(kSub / 32, W - w0);
+  uint8_t *seg = ws.seg + ((size_t)k * nsub + s) * sl.bytes;
+  int32_t *off = reinterpret_cast<int32_t *>(seg);
+  uint8_t *rows = seg + sl.offb;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const uint32_t *b = ws.bits + ((size_t)k * E + e) * W + w0;
+    int c = 0;
+    for (int i = 0; i < nw; i++) c += __popc(b[i]);
+    cnt[e] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {   // exclusive scan over experts (warp 0), offsets written to the segment
     const int lane = threadIdx.x;
     int run = 0;
     for (int base = 0; base < E; base += 32) {
       const int v = base + lane < E ? cnt[base + lane] : 0;
       int incl = v;
 #pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
       }
-      if (base + lane < E) ws.loff[(size_t)k * E + base + lane] = run + incl - v;
+      if (base + lane < E) { off[base + lane] = run + incl - v; cnt[base + lane] = run + incl - v; }
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
+    if (lane == 0) off[E] = run;
   }
-  if (st && status) atomicOr(status, st);
-}
-
-__global__ void __launch_bounds__(256) imatrix_csr(int E, int W, int64_t lcap, RouteWs ws) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int64_t k = blockIdx.y;
-  if (e >= E) return;
-  const uint32_t *bits = ws.bits + ((size_t)k * E + e) * W;
-  uint16_t *list = ws.list + (size_t)k * lcap + ws.loff[(size_t)k * E + e];
-  int pos = 0;
-  for (int w0 = 0; w0 < W; w0 += 32) {
-    uint32_t word = w0 + lane < W ? bits[w0 + lane] : 0u;
-    const int n = __popc(word);
-    int incl = n;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const uint32_t *b = ws.bits + ((size_t)k * E + e) * W + w0;
+    int p = cnt[e];
+    for (int i = 0; i < nw; i++) {
+      uint32_t word = b[i];
+      while (word) {
+        const int bit = __ffs(word) - 1;
+        word &= word - 1;
+        rows[p++] = (uint8_t)(i * 32 + bit);
+      }
     }
-    int p = pos + incl - n;
-    while (word) {
-      const int b = __ffs(word) - 1;
-      word &= word - 1;
-      list[p++] = (uint16_t)((w0 + lane) * 32 + b);
-    }
-    pos += __shfl_sync(0xffffffffu, incl, 31);
   }
 }
 
 // ---------------------------------------------------------------------------------------------
 struct AccArgs {
-  int64_t tokens, cols, rpc, nchunks, lcap;
-  int E, nconsumers;
+  int64_t tokens, cols, rpc, nchunks;
+  int E, nconsumers, nsub, stage_bytes;
+  SegLayout sl;
   RouteWs ws;
   float *in_sum2;
   int32_t *status;
 };
 
-// acc[0..CPL) += x^2 for the CPL values of this lane at `p` (shared memory), one rounding each.
-__device__ __forceinline__ void sq_acc(float *acc, const uint8_t *p, __nv_bfloat16) {
-  const uint2 u = *reinterpret_cast<const uint2 *>(p);
+// Shared-memory loads through 32-bit shared-window addresses (explicitly the shared state space;
+// volatile so they stay after the stage's mbarrier wait).
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int lds_s32(uint32_t a) {
+  int v;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+// acc[0..CPL) += x^2 for the CPL values of this lane (shared-window address a), each exact square
+// added with one rounding.  For bf16 the mixed-precision FMA takes the two halves of a 32-bit
+// register directly (one instruction per value).
+__device__ __forceinline__ void sq_acc(float *acc, uint32_t a, __nv_bfloat16) {
+  const uint2 u = lds_v2(a);
   asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %4;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n"
       " mov.b32 {l, h}, %5;\n fma.rn.f32.bf16 %2, l, l, %2;\n fma.rn.f32.bf16 %3, h, h, %3;\n}\n"
       : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
       : "r"(u.x), "r"(u.y));
 }
-__device__ __forceinline__ void sq_acc(float *acc, const uint8_t *p, float) {
-  const float2 v = *reinterpret_cast<const float2 *>(p);
-  acc[0] = __fmaf_rn(v.x, v.x, acc[0]);
-  acc[1] = __fmaf_rn(v.y, v.y, acc[1]);
+__device__ __forceinline__ void sq_acc(float *acc, uint32_t a, float) {
+  const uint2 u = lds_v2(a);
+  const float x0 = __uint_as_float(u.x), x1 = __uint_as_float(u.y);
+  acc[0] = __fmaf_rn(x0, x0, acc[0]);
+  acc[1] = __fmaf_rn(x1, x1, acc[1]);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_kernel(
     const __grid_constant__ CUtensorMap tmap, AccArgs a) {
   constexpr int CPL = Col<T>::CPL, TILE = Col<T>::TILE;
-  constexpr uint32_t kStageBytes = kSub * kRowBytes;
+  constexpr uint32_t kTileBytes = kSub * kRowBytes;
+  constexpr uint32_t kSegOff = kTileBytes + kRowBytes;   // after the tile and its zero row
+  const uint32_t kStageBytes = (uint32_t)a.stage_bytes;  // tile + zero row + segment, multiple of 128
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // stage buffers start on a 128-byte boundary (one spare 128 bytes is allocated for this)
   uint8_t *smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
+  const uint32_t smem_s = smem_u32(smem);
   __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
   __shared__ int abort_flag;
 
@@ -228,6 +296,10 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
     abort_flag = 0;
     mbar_fence_init();
   }
+  // row kSub of every stage is a zero row: a group of row indices is padded with it (adding +0 to
+  // a sum of squares leaves it unchanged)
+  for (int i = threadIdx.x; i < kStages * kRowBytes / 4; i += blockDim.x)
+    reinterpret_cast<uint32_t *>(smem + (size_t)(i / (kRowBytes / 4)) * kStageBytes + kTileBytes)[i % (kRowBytes / 4)] = 0u;
   __syncthreads();
 
   if (warp == NW) {
@@ -242,9 +314,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
           const int st = (int)(q % kStages);
           if (q >= kStages) ok = mbar_wait_bounded(&empty_bar[st], (uint32_t)((q / kStages - 1) & 1));
           if (!ok || *(volatile int *)&abort_flag) { ok = false; break; }
-          mbar_expect_tx(&full_bar[st], kStageBytes);
-          tma_load_2d(smem + (size_t)st * kStageBytes, &tmap, (int)col0, (int)(k * a.rpc + (int64_t)sub * kSub),
-                      &full_bar[st]);
+          uint8_t *dst = smem + (size_t)st * kStageBytes;
+          mbar_expect_tx(&full_bar[st], kTileBytes + (uint32_t)a.sl.bytes);
+          tma_load_2d(dst, &tmap, (int)col0, (int)(k * a.rpc + (int64_t)sub * kSub), &full_bar[st]);
+          bulk_copy_g2s(dst + kSegOff, a.ws.seg + ((size_t)k * a.nsub + sub) * a.sl.bytes, (uint32_t)a.sl.bytes,
+                        &full_bar[st]);
         }
       }
       if (!ok) {
@@ -264,47 +338,42 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
     for (int64_t k = kbeg; k < kend && ok; k++) {
       const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
       const int nsub = (int)((rows + kSub - 1) / kSub);
-      int e_[kSlots], cnt_[kSlots], lb_[kSlots], cur_[kSlots];
+      int e_[kSlots], cnt_[kSlots];
       float acc[kSlots][CPL];
 #pragma unroll
       for (int s = 0; s < kSlots; s++) {
         const int je = s * NW + ((s & 1) ? NW - 1 - warp : warp);
-        e_[s] = je < ne ? a.ws.order[(size_t)k * a.E + eb + je] : -1;
-        cnt_[s] = e_[s] >= 0 ? a.ws.ccount[(size_t)k * a.E + e_[s]] : 0;
-        lb_[s] = e_[s] >= 0 ? a.ws.loff[(size_t)k * a.E + e_[s]] : 0;
-        cur_[s] = 0;
+        e_[s] = je < ne ? a.ws.order[eb + je] : -1;
 #pragma unroll
         for (int c = 0; c < CPL; c++) acc[s][c] = 0.0f;
       }
-      const uint16_t *list = a.ws.list + (size_t)k * a.lcap;
+#pragma unroll
+      for (int s = 0; s < kSlots; s++) cnt_[s] = e_[s] >= 0 ? a.ws.ccount[(size_t)k * a.E + e_[s]] : 0;
       for (int sub = 0; sub < nsub; sub++, q++) {
         const int st = (int)(q % kStages);
         if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((q / kStages) & 1)) || *(volatile int *)&abort_flag) {
           ok = false;
           break;
         }
-        const uint8_t *tile = smem + (size_t)st * kStageBytes + lane * (CPL * sizeof(T));
-        const int rlo = sub * kSub, rhi = rlo + kSub;
+        const uint32_t stage = smem_s + (uint32_t)st * kStageBytes;
+        const uint32_t tile = stage + lane * (uint32_t)(CPL * sizeof(T));
+        const uint32_t soff = stage + kSegOff, srow = soff + (uint32_t)a.sl.offb;
 #pragma unroll
         for (int s = 0; s < kSlots; s++) {
-          while (cur_[s] < cnt_[s]) {
-            const int i = cur_[s] + lane;
-            const int r = i < cnt_[s] ? (int)list[lb_[s] + i] : 0x7fffffff;
-            const int n = __popc(__ballot_sync(0xffffffffu, r < rhi));
-            const int rl = r - rlo;
-            int j = 0;
+          if (cnt_[s] == 0) continue;
+          const int beg = lds_s32(soff + 4 * e_[s]), end = lds_s32(soff + 4 * (e_[s] + 1));
+          // groups of 4 rows: all row indices, then all loads, then the 4 ordered additions (a
+          // short group is padded with the zero row)
 #pragma unroll 1
-            for (; j + 4 <= n; j += 4) {
-              const int r0 = __shfl_sync(0xffffffffu, rl, j), r1 = __shfl_sync(0xffffffffu, rl, j + 1);
-              const int r2 = __shfl_sync(0xffffffffu, rl, j + 2), r3 = __shfl_sync(0xffffffffu, rl, j + 3);
-              sq_acc(acc[s], tile + r0 * kRowBytes, T());
-              sq_acc(acc[s], tile + r1 * kRowBytes, T());
-              sq_acc(acc[s], tile + r2 * kRowBytes, T());
-              sq_acc(acc[s], tile + r3 * kRowBytes, T());
+          for (int j = beg; j < end; j += 4) {
+            uint32_t r[4];
+#pragma unroll
+            for (int i = 0; i < 4; i++) {
+              const uint32_t v = lds_u8(srow + (uint32_t)min(j + i, end - 1));
+              r[i] = j + i < end ? v : (uint32_t)kSub;
             }
-            for (; j < n; j++) sq_acc(acc[s], tile + __shfl_sync(0xffffffffu, rl, j) * kRowBytes, T());
-            cur_[s] += n;
-            if (n < 32) break;
+#pragma unroll
+            for (int i = 0; i < 4; i++) sq_acc(acc[s], tile + r[i] * kRowBytes, T());
           }
         }
         __syncwarp();
@@ -315,14 +384,22 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
 #pragma unroll
       for (int s = 0; s < kSlots; s++) {
         if (cnt_[s] == 0 || !col_ok) continue;
+        const float *v = acc[s];
         if (split) {
           float *dst = a.ws.partial + ((size_t)k * a.E + e_[s]) * a.cols + mycol;
-#pragma unroll
-          for (int c = 0; c < CPL; c++) dst[c] = acc[s][c];
+          if (CPL == 4) *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+          else *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
         } else {
           float *dst = a.in_sum2 + (size_t)e_[s] * a.cols + mycol;
-#pragma unroll
-          for (int c = 0; c < CPL; c++) dst[c] = __fadd_rn(dst[c], acc[s][c]);
+          if (CPL == 4) {
+            float4 o = *reinterpret_cast<float4 *>(dst);
+            o.x = __fadd_rn(o.x, v[0]); o.y = __fadd_rn(o.y, v[1]); o.z = __fadd_rn(o.z, v[2]); o.w = __fadd_rn(o.w, v[3]);
+            *reinterpret_cast<float4 *>(dst) = o;
+          } else {
+            float2 o = *reinterpret_cast<float2 *>(dst);
+            o.x = __fadd_rn(o.x, v[0]); o.y = __fadd_rn(o.y, v[1]);
+            *reinterpret_cast<float2 *>(dst) = o;
+          }
         }
       }
     }
@@ -395,7 +472,7 @@ static bool make_tmap(CUtensorMap *m, const void *x, iq_dtype dt, int64_t tokens
 
 template <typename T>
 static int launch_accumulate(const CUtensorMap &tm, const AccArgs &a, const Plan &p, cudaStream_t st) {
-  const size_t smem = (size_t)kStages * kSub * kRowBytes + 128;
+  const size_t smem = (size_t)kStages * a.stage_bytes + 128;
   auto kern = imatrix_accumulate_kernel<T>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
@@ -411,7 +488,7 @@ using namespace iqk;
 extern "C" int iq_imatrix_workspace_size(int64_t tokens, int64_t cols, iq_dtype dt, int num_experts, int top_k,
                                          int64_t rows_per_chunk, size_t *bytes) {
   if (!bytes || tokens < 0 || cols <= 0 || (dt != IQ_F32 && dt != IQ_BF16) || num_experts <= 0 ||
-      num_experts > 1024 || top_k < 1 || rows_per_chunk <= 0 || rows_per_chunk > 4096)
+      num_experts > 1024 || top_k < 1 || top_k > kMaxTopK || rows_per_chunk <= 0 || rows_per_chunk > 4096)
     return IQ_ERR_ARG;
   const Plan p = make_plan(tokens, cols, dt, num_experts, top_k, rows_per_chunk);
   *bytes = route_ws_bytes(p, num_experts, cols);
@@ -423,7 +500,8 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
                                      float *in_sum2, int64_t *counts, int32_t *status, void *workspace,
                                      size_t workspace_bytes, void *stream) {
   if (dt != IQ_F32 && dt != IQ_BF16) return IQ_ERR_ARG;
-  if (tokens < 0 || tokens > INT32_MAX || cols <= 0 || cols % 64 || top_k < 1 || num_experts < top_k ||
+  if (tokens < 0 || tokens > INT32_MAX || cols <= 0 || cols % 64 || top_k < 1 || top_k > kMaxTopK ||
+      num_experts < top_k ||
       num_experts > 1024 || rows_per_chunk < 1 || rows_per_chunk > 4096 ||
       (tokens + rows_per_chunk - 1) / rows_per_chunk > 65535)
     return IQ_ERR_ARG;
@@ -443,12 +521,13 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
   imatrix_route<<<(unsigned)p.nchunks, 1024, 0, st>>>(expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.W,
                                                      ws, (unsigned long long *)counts, status);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
-  imatrix_csr<<<dim3((unsigned)((num_experts + 7) / 8), (unsigned)p.nchunks), 256, 0, st>>>(num_experts, p.W, p.lcap,
-                                                                                           ws);
+  imatrix_segments<<<dim3((unsigned)p.nsub, (unsigned)p.nchunks), 1024, 0, st>>>(num_experts, p.W, p.nsub, p.seg,
+                                                                                 ws);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   AccArgs a;
-  a.tokens = tokens; a.cols = cols; a.rpc = rows_per_chunk; a.nchunks = p.nchunks; a.lcap = p.lcap;
-  a.E = num_experts;
+  a.tokens = tokens; a.cols = cols; a.rpc = rows_per_chunk; a.nchunks = p.nchunks;
+  a.E = num_experts; a.nsub = p.nsub; a.sl = p.seg;
+  a.stage_bytes = (kSub * kRowBytes + kRowBytes + p.seg.bytes + 127) & ~127;
   const int ne = num_experts < kBatch ? num_experts : kBatch;
   a.nconsumers = (ne + kSlots - 1) / kSlots;
   a.ws = ws; a.in_sum2 = in_sum2; a.status = status;

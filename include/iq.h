@@ -112,8 +112,8 @@ IQ_API int iq_format_info(iq_format f, iq_format_info_t *out);
  *   in_sum2      device, [num_experts, cols] fp32, accumulated in place (16-byte aligned)
  *   counts       device, [num_experts] int64, accumulated in place
  *   workspace    device scratch of iq_imatrix_workspace_size bytes (256-byte aligned)
- *   requires cols % 64 == 0, 1 <= top_k <= num_experts <= 1024, 1 <= rows_per_chunk <= 4096,
- *   tokens < 2^31 and at most 65535 chunks.
+ *   requires cols % 64 == 0, 1 <= top_k <= min(num_experts, 64), num_experts <= 1024,
+ *   1 <= rows_per_chunk <= 4096, tokens < 2^31 and at most 65535 chunks.
  * Results are bit-identical to the sequential definition above, whatever the launch layout. */
 IQ_API int iq_imatrix_workspace_size(int64_t tokens, int64_t cols, iq_dtype dt, int num_experts, int top_k,
                               int64_t rows_per_chunk, size_t *bytes);
@@ -195,7 +195,8 @@ IQ_API int iq_encode_static_scratch(iq_format f, const void *W, iq_dtype dt, int
 
 /* ---- decoder ([formats]: the value rule above) ------------------------------------------------
  * out[rows, cols] (device; IQ_F32, or IQ_BF16 rounded to nearest even) from payload [B,
- * block_bytes].  fp32 output is exact.  out must be 16-byte aligned. */
+ * block_bytes].  fp32 output is exact.  payload must be 4-byte aligned, grid and out 16-byte
+ * aligned. */
 IQ_API int iq_decode(iq_format f, const uint8_t *payload, int64_t rows, int64_t cols, const float *grid, void *out,
               iq_dtype out_dtype, void *stream);
 

@@ -83,10 +83,12 @@ def test_decode_hand_assembled_fixtures():
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("T,C,E,K,R", [(2500, 192, 16, 4, 1024), (777, 64, 5, 2, 300), (4096, 128, 128, 8, 1024),
                                        (300, 256, 200, 3, 64), (600, 14336, 16, 2, 256), (301, 7168, 9, 3, 128),
-                                       (130, 14400, 1, 1, 1024)])
+                                       (130, 14400, 1, 1, 1024), (1500, 14336, 16, 3, 256)])
 def test_imatrix_bit_exact(dtype, T, C, E, K, R):
     """Both launch layouts: few column tiles (chunks in parallel, partials combined in chunk order)
-    and many tiles (one CTA walks a tile's chunks in order); ragged chunks and column tiles."""
+    and many tiles (one CTA walks a tile's chunks in order); ragged chunks and column tiles; many
+    chunks of two stages each, where consumer warps drift a whole chunk apart (each expert's sums
+    must keep one owner warp so their chunk-order additions stay ordered)."""
     x32 = synth.activations(T, C, seed=T + C)
     store, xv = synth.as_dtype(x32, dtype)
     ids = synth.router(T, E, K, idle=max(1, E // 16) if E > 1 else 0, seed=E + K)

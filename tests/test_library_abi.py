@@ -39,3 +39,24 @@ def test_format_info_matches_oracle(orc):
             (o["block_bytes"], o["groups"], o["num_choices"], o["entries"], o["vectors_per_group"])
         assert a["block_bytes"] * 8 / 256 == {"IQ2_XXS": 2.0625, "IQ2_XS": 2.3125, "IQ2_S": 2.5625,
                                               "IQ1_S": 1.5625, "IQ1_M": 1.75}[fmt]
+
+
+def test_host_only_size_queries_and_argument_checks():
+    """Workspace and capacity queries run on the host alone; bad arguments are refused with
+    IQ_ERR_ARG (-1) before any device work."""
+    from ggml_iq_codebook_accumulate_b300 import api
+    L = api.lib()
+    n = ctypes.c_size_t()
+    assert L.iq_imatrix_workspace_size(4096, 17408, api.IQ_BF16, 128, 8, 1024, ctypes.byref(n)) == 0 and n.value > 0
+    assert L.iq_imatrix_workspace_size(4096, 17408, api.IQ_BF16, 128, 65, 1024, ctypes.byref(n)) == -1  # top_k > 64
+    assert L.iq_imatrix_workspace_size(4096, 17408, api.IQ_BF16, 1025, 8, 1024, ctypes.byref(n)) == -1  # > 1024 experts
+    assert L.iq_imatrix_workspace_size(4096, 17408, api.IQ_BF16, 128, 8, 4097, ctypes.byref(n)) == -1  # chunk too big
+    assert L.iq_encode_workspace_size(0, 5632, 2048, ctypes.byref(n)) == 0 and n.value >= 256 + 256 * 64
+    assert L.iq_encode_workspace_size(0, 5632, 2000, ctypes.byref(n)) == -1                           # cols % 256
+    assert L.iq_encode_workspace_size(7, 1, 256, ctypes.byref(n)) == -1                               # no such format
+    caps = {f: api.encode_static_scratch_capacity(f) for f in api.FORMATS}
+    assert caps["IQ1_S"] == caps["IQ1_M"] == 114656 and caps["IQ2_XXS"] == 128992
+    # the capacity is exactly what fits in the 1 MiB array
+    for f in api.FORMATS:
+        assert L.iq_encode_workspace_size(api.FMT_ID[f], caps[f], 256, ctypes.byref(n)) == 0 and n.value <= 1 << 20
+        assert L.iq_encode_workspace_size(api.FMT_ID[f], caps[f] + 1, 256, ctypes.byref(n)) == 0 and n.value > 1 << 20
