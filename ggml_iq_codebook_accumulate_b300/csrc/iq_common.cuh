@@ -208,11 +208,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *m, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete sleeps (up to the hint,
+// waking early when the phase completes) instead of spinning on issue slots other warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *m, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(m)), "r"(parity), "r"(20000u)
+      : "memory");
+  return ok != 0;
+}
 // Waits for the phase of parity `parity` to complete; false after kWaitLimitNs.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *m, uint32_t parity) {
   if (mbar_try_wait(m, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(m, parity))
+  while (!mbar_try_wait_sleep(m, parity))
     if (global_timer_ns() - t0 > kWaitLimitNs) return false;
   return true;
 }

@@ -11,21 +11,21 @@
 // fl(in_sum2[e][j] + partial[e][j]), chunk by chunk.
 //
 // Kernels per call:
-//  route       one CTA per chunk: a bitmap [E][rows/32] of the chunk rows each expert receives
-//              (a token's ids are a set) and per-chunk counts; the last chunk CTA to finish ranks
-//              the experts by their count over the whole call (the order consumer warps are dealt
-//              from, the same for every chunk so that each expert's in_sum2 row has one owner);
-//  segments    one CTA per (chunk, 128-row sub-tile): expands the bitmaps into a segment holding,
-//              for every expert, the offset of its rows and the rows themselves (one byte each,
-//              ascending), so a sub-tile's routing travels with its rows;
+//  route       one CTA per (chunk, 128-row sub-tile): builds the sub-tile's expert bitmap in shared
+//              memory (a token's ids are a set) and writes the sub-tile's segment: for every expert
+//              the offset of its rows and the rows themselves (as 16-bit byte offsets into a staged
+//              tile, ascending, each run padded to a multiple of 4 with the offset of a zero row);
+//              per-chunk counts are added atomically, and the last CTA to finish ranks the experts
+//              by their count over the whole call (the order consumer warps are dealt from, the same
+//              for every chunk so that each expert's in_sum2 row has one owner);
 //  accumulate  one CTA per column tile (128 bf16 / 64 fp32 columns, 256 bytes of a row) and,
 //              when there are too few tiles to fill the GPU, per chunk as well.  A producer warp
 //              streams the tile's rows through a 3-stage shared-memory ring: each stage is one 2-D
 //              TMA tensor copy of 128 rows plus one bulk copy of the sub-tile's segment, both
 //              completing on the stage's mbarrier (waits bounded by the global timer).  Each
 //              consumer warp owns up to 8 experts (dealt from the count order so heavy and light
-//              experts mix), walks their rows from shared memory only and keeps one register
-//              accumulator per (expert, column of its lane);
+//              experts mix), walks their rows 4 at a time from shared memory only and keeps one
+//              register accumulator per (expert, column of its lane);
 //  combine     (per-chunk mode only) adds the chunk partials to in_sum2 in chunk order.
 // No atomics touch in_sum2, so the sums are the sequential definition above.
 #include <cudaTypedefs.h>
@@ -54,7 +54,9 @@ __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~(size
 __host__ __device__ inline int align16(int n) { return (n + 15) & ~15; }
 
 // A segment (one per chunk and 128-row sub-tile): int32 offsets[E + 1] (padded to 16 bytes), then
-// the rows (uint8, relative to the sub-tile) of expert 0, expert 1, ... each run ascending.
+// the rows of expert 0, expert 1, ... as uint16 byte offsets (row * 256) into the staged tile, each
+// run ascending and padded to a multiple of 4 entries with the zero row's offset (kSub * 256).
+constexpr uint16_t kZeroOff = (uint16_t)(kSub * kRowBytes);
 struct SegLayout {
   int offb;   // bytes of the offset table
   int bytes;  // segment bytes (multiple of 16)
@@ -62,23 +64,22 @@ struct SegLayout {
 __host__ __device__ inline SegLayout seg_layout(int E, int top_k) {
   SegLayout l;
   l.offb = align16((E + 1) * 4);
-  l.bytes = l.offb + align16(kSub * (top_k < E ? top_k : E));
+  l.bytes = l.offb + align16(2 * (kSub * (top_k < E ? top_k : E) + 3 * E));
   return l;
 }
 
 struct RouteWs {
-  int32_t *touched;    // [E]   experts this call routed at least one token to; [E] = chunks done
-  uint32_t *bits;      // [nchunks][E][W]
+  int32_t *touched;    // [E]   experts this call routed at least one token to; [E] = CTAs done
   int32_t *ccount;     // [nchunks][E] tokens per (chunk, expert)
   int32_t *order;      // [E] experts by descending count over the call (ties: lower id)
   uint8_t *seg;        // [nchunks][nsub] segments of seg_bytes
   float *partial;      // [nchunks][E][cols] (per-chunk mode only)
-  size_t zero_bytes;   // bytes from the start to clear before the call (touched + bits)
+  size_t zero_bytes;   // bytes from the start to clear before the call (touched + ccount)
 };
 
 struct Plan {
   int64_t nchunks, ntiles, nbatch;
-  int W, nsub;
+  int nsub;
   SegLayout seg;
   bool split;
 };
@@ -86,7 +87,6 @@ struct Plan {
 static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_k, int64_t rpc) {
   Plan p;
   p.nchunks = (tokens + rpc - 1) / rpc;
-  p.W = (int)((rpc + 31) / 32);
   p.nsub = (int)((rpc + kSub - 1) / kSub);
   p.seg = seg_layout(E, top_k);
   const int tile = dt == IQ_BF16 ? Col<__nv_bfloat16>::TILE : Col<float>::TILE;
@@ -100,68 +100,106 @@ static RouteWs route_ws(void *ws, const Plan &p, int E, int64_t cols) {
   uint8_t *q = (uint8_t *)ws;
   RouteWs r;
   r.touched = (int32_t *)q; q += align256((size_t)(E + 1) * 4);
-  r.bits = (uint32_t *)q; q += align256((size_t)p.nchunks * E * p.W * 4);
-  r.zero_bytes = (size_t)(q - (uint8_t *)ws);
   r.ccount = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
+  r.zero_bytes = (size_t)(q - (uint8_t *)ws);
   r.order = (int32_t *)q; q += align256((size_t)E * 4);
   r.seg = q; q += align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   r.partial = p.split ? (float *)q : nullptr;
   return r;
 }
 static size_t route_ws_bytes(const Plan &p, int E, int64_t cols) {
-  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * p.W * 4) +
-             align256((size_t)p.nchunks * E * 4) + align256((size_t)E * 4) +
+  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * 4) + align256((size_t)E * 4) +
              align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   if (p.split) n += align256((size_t)p.nchunks * E * cols * 4);
   return n;
 }
 
 // ---------------------------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) imatrix_route(const int32_t *__restrict__ ids, int64_t tokens, int top_k,
-                                                      int E, int64_t rpc, int W, RouteWs ws,
-                                                      unsigned long long *__restrict__ counts,
-                                                      int32_t *__restrict__ status) {
-  __shared__ int cnt[1024];
-  const int64_t k = blockIdx.x;
-  const int64_t t0 = k * rpc, t1 = min(tokens, t0 + rpc);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+// One CTA per (sub-tile s, chunk k): rows [128 s, 128 s + 128) of chunk k.
+__global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__ ids, int64_t tokens, int top_k,
+                                                     int E, int64_t rpc, int nsub, SegLayout sl, RouteWs ws,
+                                                     unsigned long long *__restrict__ counts,
+                                                     int32_t *__restrict__ status) {
+  __shared__ uint32_t bm[1024][kSub / 32];   // expert x row bitmap of the sub-tile
+  __shared__ int cnt[1024 + 1], off[1024 + 1];
+  __shared__ int last;
+  const int s = blockIdx.x;
+  const int64_t k = blockIdx.y;
+  const int64_t r0 = k * rpc + (int64_t)s * kSub;
+  const int64_t rend = min(tokens, (k + 1) * rpc);
+  const int rows = (int)max((int64_t)0, min((int64_t)kSub, rend - r0));
+  for (int i = threadIdx.x; i < E * (kSub / 32); i += blockDim.x) bm[i / (kSub / 32)][i % (kSub / 32)] = 0u;
   __syncthreads();
   int st = 0;
-  uint32_t *bits = ws.bits + (size_t)k * E * W;
-  for (int64_t t = t0 + threadIdx.x; t < t1; t += blockDim.x) {
-    const int32_t *row = ids + t * top_k;
-    const int r = (int)(t - t0);
-    for (int a = 0; a < top_k; a++) {
-      const int e = row[a];
-      if (e < 0 || e >= E) { st |= IQ_STATUS_BAD_EXPERT_ID; continue; }
-      bool dup = false;
-      for (int b = 0; b < a; b++) dup |= (row[b] == e);
-      if (dup) { st |= IQ_STATUS_DUP_EXPERT_ID; continue; }
-      atomicOr(&bits[(size_t)e * W + (r >> 5)], 1u << (r & 31));
-      atomicAdd(&cnt[e], 1);
-    }
+  for (int i = threadIdx.x; i < rows * top_k; i += blockDim.x) {
+    const int r = i / top_k, a = i % top_k;
+    const int32_t *row = ids + (r0 + r) * top_k;
+    const int e = row[a];
+    if (e < 0 || e >= E) { st |= IQ_STATUS_BAD_EXPERT_ID; continue; }
+    bool dup = false;
+    for (int b = 0; b < a; b++) dup |= (row[b] == e);
+    if (dup) { st |= IQ_STATUS_DUP_EXPERT_ID; continue; }
+    atomicOr(&bm[e][r >> 5], 1u << (r & 31));
   }
+  if (st && status) atomicOr(status, st);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+#pragma unroll
+    for (int w = 0; w < kSub / 32; w++) c += __popc(bm[e][w]);
+    cnt[e] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {   // exclusive scan of the padded run lengths over experts (warp 0)
+    const int lane = threadIdx.x;
+    int run = 0;
+    for (int base = 0; base < E; base += 32) {
+      const int v = base + lane < E ? (cnt[base + lane] + 3) & ~3 : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (base + lane < E) off[base + lane] = run + incl - v;
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) off[E] = run;
+  }
+  __syncthreads();
+  uint8_t *seg = ws.seg + ((size_t)k * nsub + s) * sl.bytes;
+  int32_t *soff = reinterpret_cast<int32_t *>(seg);
+  uint16_t *srow = reinterpret_cast<uint16_t *>(seg + sl.offb);
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) soff[e] = off[e];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int p = off[e];
+#pragma unroll
+    for (int w = 0; w < kSub / 32; w++) {
+      uint32_t word = bm[e][w];
+      while (word) {
+        const int bit = __ffs(word) - 1;
+        word &= word - 1;
+        srow[p++] = (uint16_t)((w * 32 + bit) * kRowBytes);
+      }
+    }
+    while (p & 3) srow[p++] = kZeroOff;
     const int c = cnt[e];
-    ws.ccount[(size_t)k * E + e] = c;
     if (c) {
+      atomicAdd(&ws.ccount[(size_t)k * E + e], c);
       atomicAdd(&counts[e], (unsigned long long)c);
       ws.touched[e] = 1;
     }
   }
-  if (st && status) atomicOr(status, st);
-  // the last chunk CTA to finish ranks the experts by their count over the whole call
-  __shared__ int last;
+  // the last CTA to finish ranks the experts by their count over the whole call
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(&ws.touched[E], 1) == (int)gridDim.x - 1;
+  if (threadIdx.x == 0) last = atomicAdd(&ws.touched[E], 1) == (int)(gridDim.x * gridDim.y) - 1;
   __syncthreads();
   if (!last) return;
   __threadfence();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int c = 0;
-    for (int64_t kk = 0; kk < (int64_t)gridDim.x; kk++) c += *(volatile int32_t *)&ws.ccount[(size_t)kk * E + e];
+    for (int64_t kk = 0; kk < (int64_t)gridDim.y; kk++) c += *(volatile int32_t *)&ws.ccount[(size_t)kk * E + e];
     cnt[e] = c;
   }
   __syncthreads();
@@ -173,54 +211,6 @@ __global__ void __launch_bounds__(1024) imatrix_route(const int32_t *__restrict_
       rank += (co > c) || (co == c && o < e);
     }
     ws.order[rank] = e;
-  }
-}
-
-// One CTA per (sub-tile s, chunk k): the segment of rows [128 s, 128 s + 128) of chunk k.
-__global__ void __launch_bounds__(1024) imatrix_segments(int E, int W, int nsub, SegLayout sl, RouteWs ws) {
-  __shared__ int cnt[1024 + 32];
-  const int s = blockIdx.x;
-  const int64_t k = blockIdx.y;
-  const int w0 = s * (kSub / 32);
-  const int nw = min(kSub / 32, W - w0);
-  uint8_t *seg = ws.seg + ((size_t)k * nsub + s) * sl.bytes;
-  int32_t *off = reinterpret_cast<int32_t *>(seg);
-  uint8_t *rows = seg + sl.offb;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const uint32_t *b = ws.bits + ((size_t)k * E + e) * W + w0;
-    int c = 0;
-    for (int i = 0; i < nw; i++) c += __popc(b[i]);
-    cnt[e] = c;
-  }
-  __syncthreads();
-  if (threadIdx.x < 32) {   // exclusive scan over experts (warp 0), offsets written to the segment
-    const int lane = threadIdx.x;
-    int run = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int v = base + lane < E ? cnt[base + lane] : 0;
-      int incl = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (base + lane < E) { off[base + lane] = run + incl - v; cnt[base + lane] = run + incl - v; }
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) off[E] = run;
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const uint32_t *b = ws.bits + ((size_t)k * E + e) * W + w0;
-    int p = cnt[e];
-    for (int i = 0; i < nw; i++) {
-      uint32_t word = b[i];
-      while (word) {
-        const int bit = __ffs(word) - 1;
-        word &= word - 1;
-        rows[p++] = (uint8_t)(i * 32 + bit);
-      }
-    }
   }
 }
 
@@ -236,11 +226,6 @@ struct AccArgs {
 
 // Shared-memory loads through 32-bit shared-window addresses (explicitly the shared state space;
 // volatile so they stay after the stage's mbarrier wait).
-__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
-  uint32_t v;
-  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
-  return v;
-}
 __device__ __forceinline__ int lds_s32(uint32_t a) {
   int v;
   asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
@@ -252,21 +237,30 @@ __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   return v;
 }
 
-// acc[0..CPL) += x^2 for the CPL values of this lane (shared-window address a), each exact square
-// added with one rounding.  For bf16 the mixed-precision FMA takes the two halves of a 32-bit
-// register directly (one instruction per value).
-__device__ __forceinline__ void sq_acc(float *acc, uint32_t a, __nv_bfloat16) {
-  const uint2 u = lds_v2(a);
+// acc[0..CPL) += x^2 for the CPL values of this lane (u: the lane's 8 bytes of one row), each exact
+// square added with one rounding.  For bf16 the mixed-precision FMA takes the two halves of a
+// 32-bit register directly (one instruction per value).
+__device__ __forceinline__ void sq_acc(float *acc, uint2 u, __nv_bfloat16) {
   asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %4;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n"
       " mov.b32 {l, h}, %5;\n fma.rn.f32.bf16 %2, l, l, %2;\n fma.rn.f32.bf16 %3, h, h, %3;\n}\n"
       : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
       : "r"(u.x), "r"(u.y));
 }
-__device__ __forceinline__ void sq_acc(float *acc, uint32_t a, float) {
-  const uint2 u = lds_v2(a);
+__device__ __forceinline__ void sq_acc(float *acc, uint2 u, float) {
   const float x0 = __uint_as_float(u.x), x1 = __uint_as_float(u.y);
   acc[0] = __fmaf_rn(x0, x0, acc[0]);
   acc[1] = __fmaf_rn(x1, x1, acc[1]);
+}
+// The 4 rows of a group: their offsets (4 x uint16) in one load, then the rows' values.
+struct Group { uint2 v0, v1, v2, v3; };
+__device__ __forceinline__ Group load_group(uint32_t srow_j, uint32_t tile) {
+  const uint2 o = lds_v2(srow_j);
+  Group g;
+  g.v0 = lds_v2(tile + (o.x & 0xffffu));
+  g.v1 = lds_v2(tile + (o.x >> 16));
+  g.v2 = lds_v2(tile + (o.y & 0xffffu));
+  g.v3 = lds_v2(tile + (o.y >> 16));
+  return g;
 }
 
 template <typename T>
@@ -362,18 +356,19 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
         for (int s = 0; s < kSlots; s++) {
           if (cnt_[s] == 0) continue;
           const int beg = lds_s32(soff + 4 * e_[s]), end = lds_s32(soff + 4 * (e_[s] + 1));
-          // groups of 4 rows: all row indices, then all loads, then the 4 ordered additions (a
-          // short group is padded with the zero row)
+          // 4 rows at a time (runs are padded to a multiple of 4 with the zero row), software
+          // pipelined: the next group's loads are issued before this group's 4 ordered additions
+          if (beg < end) {
+            Group g = load_group(srow + 2 * beg, tile);
 #pragma unroll 1
-          for (int j = beg; j < end; j += 4) {
-            uint32_t r[4];
-#pragma unroll
-            for (int i = 0; i < 4; i++) {
-              const uint32_t v = lds_u8(srow + (uint32_t)min(j + i, end - 1));
-              r[i] = j + i < end ? v : (uint32_t)kSub;
+            for (int j = beg + 4; j < end; j += 4) {
+              const Group n = load_group(srow + 2 * j, tile);
+              sq_acc(acc[s], g.v0, T()); sq_acc(acc[s], g.v1, T());
+              sq_acc(acc[s], g.v2, T()); sq_acc(acc[s], g.v3, T());
+              g = n;
             }
-#pragma unroll
-            for (int i = 0; i < 4; i++) sq_acc(acc[s], tile + r[i] * kRowBytes, T());
+            sq_acc(acc[s], g.v0, T()); sq_acc(acc[s], g.v1, T());
+            sq_acc(acc[s], g.v2, T()); sq_acc(acc[s], g.v3, T());
           }
         }
         __syncwarp();
@@ -518,11 +513,8 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
   cudaStream_t st = (cudaStream_t)stream;
   RouteWs ws = route_ws(workspace, p, num_experts, cols);
   if (cudaMemsetAsync(workspace, 0, ws.zero_bytes, st) != cudaSuccess) return IQ_ERR_CUDA;
-  imatrix_route<<<(unsigned)p.nchunks, 1024, 0, st>>>(expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.W,
-                                                     ws, (unsigned long long *)counts, status);
-  if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
-  imatrix_segments<<<dim3((unsigned)p.nsub, (unsigned)p.nchunks), 1024, 0, st>>>(num_experts, p.W, p.nsub, p.seg,
-                                                                                 ws);
+  imatrix_route<<<dim3((unsigned)p.nsub, (unsigned)p.nchunks), 256, 0, st>>>(
+      expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.nsub, p.seg, ws, (unsigned long long *)counts, status);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   AccArgs a;
   a.tokens = tokens; a.cols = cols; a.rpc = rows_per_chunk; a.nchunks = p.nchunks;
