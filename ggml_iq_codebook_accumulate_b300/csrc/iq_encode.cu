@@ -65,11 +65,11 @@ struct EncArgs {
 };
 
 // ---------------------------------------------------------------------------------------------
-// Prepared codebook, pair-interleaved: entries 2p and 2p+1 occupy 128 bytes as sixteen packed
-// pairs, (g_2p[i], g_2p+1[i]) for i = 0..7, then (h_2p[i], h_2p+1[i]) with h = g^2 (IQ2) or |g|
-// (IQ1).  One fma.rn.f32x2 then advances the dot products of two entries at once.
-__host__ __device__ __forceinline__ int tab_g(int e, int i) { return (e >> 1) * 32 + 2 * i + (e & 1); }
-__host__ __device__ __forceinline__ int tab_h(int e, int i) { return (e >> 1) * 32 + 16 + 2 * i + (e & 1); }
+// Prepared codebook: g [N x 8] then h [N x 8] (h = g^2 for IQ2, |g| for IQ1), each a K-major
+// operand of the tensor-core sweep in the canonical no-swizzle layout (see kmaj below).
+__host__ __device__ __forceinline__ int kmaj(int row, int k) {
+  return (row >> 3) * 64 + (k >> 2) * 32 + (row & 7) * 4 + (k & 3);
+}
 
 template <int F>
 __global__ void prep_codebook(const float *__restrict__ grid, EncWs ws) {
@@ -89,17 +89,18 @@ __global__ void prep_codebook(const float *__restrict__ grid, EncWs ws) {
       ok &= (g[i] >= 1.0f && g[i] <= 127.0f && g[i] == floorf(g[i]));
       h = g[i] * g[i];  // exact: at most 14 bits
     }
-    tf[tab_g(e, i)] = g[i];
-    tf[tab_h(e, i)] = h;
+    tf[kmaj(e, i)] = g[i];
+    tf[Fmt<F>::N * 8 + kmaj(e, i)] = h;
   }
   if (!ok) atomicOr(&ws.hdr[0], 1);
 }
 
 struct Entry { float g[8], h[8]; };
+template <int F>
 __device__ __forceinline__ void load_entry(const float4 *tab, int e, Entry &en) {
   const float *tf = reinterpret_cast<const float *>(tab);
 #pragma unroll
-  for (int i = 0; i < 8; i++) { en.g[i] = tf[tab_g(e, i)]; en.h[i] = tf[tab_h(e, i)]; }
+  for (int i = 0; i < 8; i++) { en.g[i] = tf[kmaj(e, i)]; en.h[i] = tf[Fmt<F>::N * 8 + kmaj(e, i)]; }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -186,61 +187,10 @@ __device__ __forceinline__ void ab1(const Vec &v, const Entry &en, float &Anp, f
   Bm = __fmaf_rn(-0.25f, Cg, Bw);
 }
 
-// Packed per-vector operands of the sweeps: every scalar duplicated into both halves of a pair.
-struct VecP {
-  uint64_t nw2[8], w[8];
-  uint64_t nT2, Ws;
-};
-__device__ __forceinline__ VecP vec_pack(const Vec &v) {
-  VecP p;
-#pragma unroll
-  for (int i = 0; i < 8; i++) { p.nw2[i] = pk2(v.nw2[i], v.nw2[i]); p.w[i] = pk2(v.w[i], v.w[i]); }
-  p.nT2 = pk2(v.nT2, v.nT2);
-  p.Ws = pk2(v.Ws, v.Ws);
-  return p;
-}
-
-// Sums of an entry pair from its 128 bytes of the shared-memory table.
-__device__ __forceinline__ void ab2_pair(const VecP &vp, const uint64_t *T, uint64_t &An, uint64_t &B) {
-  const ulonglong2 *Q = reinterpret_cast<const ulonglong2 *>(T);
-  const ulonglong2 g01 = Q[0], g23 = Q[1], g45 = Q[2], g67 = Q[3];
-  const ulonglong2 h01 = Q[4], h23 = Q[5], h45 = Q[6], h67 = Q[7];
-  const uint64_t zero = 0ull;
-  An = ffma2(vp.nw2[0], g01.x, zero);
-  B = ffma2(vp.w[0], h01.x, zero);
-  An = ffma2(vp.nw2[1], g01.y, An); B = ffma2(vp.w[1], h01.y, B);
-  An = ffma2(vp.nw2[2], g23.x, An); B = ffma2(vp.w[2], h23.x, B);
-  An = ffma2(vp.nw2[3], g23.y, An); B = ffma2(vp.w[3], h23.y, B);
-  An = ffma2(vp.nw2[4], g45.x, An); B = ffma2(vp.w[4], h45.x, B);
-  An = ffma2(vp.nw2[5], g45.y, An); B = ffma2(vp.w[5], h45.y, B);
-  An = ffma2(vp.nw2[6], g67.x, An); B = ffma2(vp.w[6], h67.x, B);
-  An = ffma2(vp.nw2[7], g67.y, An); B = ffma2(vp.w[7], h67.y, B);
-}
 struct IQ1Const { uint64_t p125, m125, p025, m025, w64; };
 __device__ __forceinline__ IQ1Const iq1_consts() {
   return {pk2(0.125f, 0.125f), pk2(-0.125f, -0.125f), pk2(0.25f, 0.25f), pk2(-0.25f, -0.25f),
           pk2(0.015625f, 0.015625f)};
-}
-// IQ1: the An and B sums of the two shifts (An +- nT2/8, B + Ws/64 +- Cg/4) for an entry pair.
-__device__ __forceinline__ void ab1_pair(const VecP &vp, const IQ1Const &k, const uint64_t *T, uint64_t &Anp,
-                                         uint64_t &Bp, uint64_t &Anm, uint64_t &Bm) {
-  const ulonglong2 *Q = reinterpret_cast<const ulonglong2 *>(T);
-  const ulonglong2 g01 = Q[0], g23 = Q[1], g45 = Q[2], g67 = Q[3];
-  const ulonglong2 h01 = Q[4], h23 = Q[5], h45 = Q[6], h67 = Q[7];
-  const uint64_t zero = 0ull;
-  uint64_t An = ffma2(vp.nw2[0], g01.x, zero), Cg = ffma2(vp.w[0], g01.x, zero), B = ffma2(vp.w[0], h01.x, zero);
-  An = ffma2(vp.nw2[1], g01.y, An); Cg = ffma2(vp.w[1], g01.y, Cg); B = ffma2(vp.w[1], h01.y, B);
-  An = ffma2(vp.nw2[2], g23.x, An); Cg = ffma2(vp.w[2], g23.x, Cg); B = ffma2(vp.w[2], h23.x, B);
-  An = ffma2(vp.nw2[3], g23.y, An); Cg = ffma2(vp.w[3], g23.y, Cg); B = ffma2(vp.w[3], h23.y, B);
-  An = ffma2(vp.nw2[4], g45.x, An); Cg = ffma2(vp.w[4], g45.x, Cg); B = ffma2(vp.w[4], h45.x, B);
-  An = ffma2(vp.nw2[5], g45.y, An); Cg = ffma2(vp.w[5], g45.y, Cg); B = ffma2(vp.w[5], h45.y, B);
-  An = ffma2(vp.nw2[6], g67.x, An); Cg = ffma2(vp.w[6], g67.x, Cg); B = ffma2(vp.w[6], h67.x, B);
-  An = ffma2(vp.nw2[7], g67.y, An); Cg = ffma2(vp.w[7], g67.y, Cg); B = ffma2(vp.w[7], h67.y, B);
-  Anp = ffma2(k.p125, vp.nT2, An);
-  Anm = ffma2(k.m125, vp.nT2, An);
-  const uint64_t Bw = ffma2(k.w64, vp.Ws, B);
-  Bp = ffma2(k.p025, Cg, Bw);
-  Bm = ffma2(k.m025, Cg, Bw);
 }
 
 // local scale multipliers: IQ2 alpha_s = d * (2s+1) / 8, IQ1 alpha_s = d * (2s+1) (both exact)
@@ -252,90 +202,12 @@ template <int F> __device__ __forceinline__ float alpha_choice(float d, int c) {
   return alpha_of<F>(d, F == IQ1_S ? (c & 7) : c);
 }
 
-// Sweep 1: per choice, the minimum over the vector's candidates of the scaled score
-// s = alpha * B + An (the error is Cs + alpha * s).
-template <int F>
-__device__ __forceinline__ void sweep_minima(const Vec &v, const float4 *tab, const float *al, float *m) {
-  constexpr int C = Fmt<F>::C, N = Fmt<F>::N;
-  constexpr int NS = Fmt<F>::IQ1 ? 8 : 16;
-  const VecP vp = vec_pack(v);
-  uint64_t alp[NS];
-#pragma unroll
-  for (int s = 0; s < NS; s++) alp[s] = pk2(al[s], al[s]);
-#pragma unroll
-  for (int c = 0; c < C; c++) m[c] = INFINITY;
-  const uint64_t *T = reinterpret_cast<const uint64_t *>(tab);
-  if (!Fmt<F>::IQ1) {
-#pragma unroll 2
-    for (int pr = 0; pr < N / 2; pr++) {
-      uint64_t An, B;
-      ab2_pair(vp, T + 16 * pr, An, B);
-#pragma unroll
-      for (int c = 0; c < C; c++) {
-        const float2 sc = up2(ffma2(alp[c], B, An));
-        m[c] = min3f(m[c], sc.x, sc.y);
-      }
-    }
-  } else {
-    const IQ1Const k = iq1_consts();
-#pragma unroll 1
-    for (int pr = 0; pr < N / 2; pr++) {
-      uint64_t Anp, Bp, Anm, Bm;
-      ab1_pair(vp, k, T + 16 * pr, Anp, Bp, Anm, Bm);
-#pragma unroll
-      for (int s = 0; s < 8; s++) {
-        const float2 sp = up2(ffma2(alp[s], Bp, Anp)), sm = up2(ffma2(alp[s], Bm, Anm));
-        if (F == IQ1_S) {
-          m[s] = min3f(m[s], sp.x, sp.y);
-          m[8 + s] = min3f(m[8 + s], sm.x, sm.y);
-        } else {
-          m[s] = min3f(min3f(m[s], sp.x, sp.y), sm.x, sm.y);
-        }
-      }
-    }
-  }
-}
-
 // best / runner-up / key over a pair of candidates (keys ka and ka + 1)
 __device__ __forceinline__ void track2(float2 sc, int ka, float &best, float &second, int &key) {
   const float lo = fminf(sc.x, sc.y), hi = fmaxf(sc.x, sc.y);
   const int klo = sc.y < sc.x ? ka + 1 : ka;
   second = min3f(second, hi, fmaxf(best, lo));
   if (lo < best) { best = lo; key = klo; }
-}
-
-// Sweep 2: under one choice, the best candidate key and the best and runner-up scores.
-// key = entry (IQ2, IQ1_S) or delta_bit * N + entry (IQ1_M).
-template <int F>
-__device__ __forceinline__ void sweep_pick(const Vec &v, const float4 *tab, float alpha, int dbit_fixed, float &best,
-                                           float &second, int &key) {
-  constexpr int N = Fmt<F>::N;
-  best = INFINITY; second = INFINITY; key = 0;
-  const VecP vp = vec_pack(v);
-  const uint64_t al = pk2(alpha, alpha);
-  const uint64_t *T = reinterpret_cast<const uint64_t *>(tab);
-  if (!Fmt<F>::IQ1) {
-#pragma unroll 2
-    for (int pr = 0; pr < N / 2; pr++) {
-      uint64_t An, B;
-      ab2_pair(vp, T + 16 * pr, An, B);
-      track2(up2(ffma2(al, B, An)), 2 * pr, best, second, key);
-    }
-  } else {
-    const IQ1Const k = iq1_consts();
-#pragma unroll 1
-    for (int pr = 0; pr < N / 2; pr++) {
-      uint64_t Anp, Bp, Anm, Bm;
-      ab1_pair(vp, k, T + 16 * pr, Anp, Bp, Anm, Bm);
-      if (F == IQ1_S) {
-        const uint64_t sc = dbit_fixed ? ffma2(al, Bm, Anm) : ffma2(al, Bp, Anp);
-        track2(up2(sc), 2 * pr, best, second, key);
-      } else {
-        track2(up2(ffma2(al, Bp, Anp)), 2 * pr, best, second, key);
-        track2(up2(ffma2(al, Bm, Anm)), N + 2 * pr, best, second, key);
-      }
-    }
-  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -415,116 +287,391 @@ __device__ __forceinline__ float group_sum(float val, int g0) {
   return s;
 }
 
-template <int F, int MODE, typename TIn, int THREADS>
-__global__ void __launch_bounds__(THREADS, 1) encode_kernel(EncArgs a, EncWs ws) {
-  constexpr int C = Fmt<F>::C, N = Fmt<F>::N, VPG = Fmt<F>::VPG, BB = Fmt<F>::BB;
-  constexpr int NW = THREADS / 32;
-  extern __shared__ __align__(128) uint8_t smem[];
-  float4 *tab = reinterpret_cast<float4 *>(smem);
-  uint32_t *packbuf = reinterpret_cast<uint32_t *>(smem + N * 64);  // [NW][24]
-  __shared__ uint64_t mbar;
+// ---------------------------------------------------------------------------------------------
+// Tensor-core sweep.
+//
+// A CTA encodes 4 blocks (128 vectors) at a time.  The per-entry sums of every vector are the
+// product of a [128 x 8] per-vector operand and the [8 x N] codebook:
+//     An = -2 (w t) . g        B = w . h (h = g^2 or |g|)        Cg = w . g (IQ1)
+// evaluated by tcgen05.mma (kind::tf32, fp32 accumulators in tensor memory), 64 codebook entries
+// per chunk.  The codebook values are small integers, exact in tf32; each fp32 per-vector operand
+// is split into two tf32 parts (hi, lo = x - hi) accumulated into the same tensor-memory column,
+// so every product is exact and the sums carry only accumulation rounding (measured on B300 at
+// most 4.3 units of 2^-24 of sum |a*b|, inside the same rounding margin as an fp32 FMA chain).
+// A control warp issues the MMAs into a double-buffered tensor-memory region and commits each
+// chunk to an mbarrier; 8 consumer warps (2 per tensor-memory lane quarter = block) load their 32
+// columns per chunk with tcgen05.ld and do the per-choice scoring with packed f32x2 FMAs and
+// three-input minima, then release the buffer.  Sweep 1 keeps, per vector and choice, the minimum
+// score; sweep 2 (same MMAs) finds each vector's best candidate and runner-up under the chosen
+// choice.  All waits are bounded.
 
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const bool grid_bad = ws.hdr[0] != 0;
-  bool ok = true;
-  if (!grid_bad) ok = load_codebook(tab, ws.tab, N * 64, &mbar);
-  if (!ok) {
-    if (lane == 0 && a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
-    // give an unfinished copy one more bounded wait before the CTA exits
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(&mbar, 0) && global_timer_ns() - t0 < 2000000000ull) {}
-    return;
+// kmaj(row, k): float offset of (row, k) in a K-major [rows x 8] fp32 operand in the canonical
+// no-swizzle layout: 8-row x 16-byte core matrices of 128 contiguous bytes, K-adjacent core
+// matrices 128 bytes apart (leading byte offset), row-group-adjacent ones 256 bytes apart (stride
+// byte offset).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(256 >> 4) << 32) |
+         (1ull << 46);
+}
+// instruction descriptor: D fp32, A and B tf32, both K-major, M = 128, N = NN
+template <int NN> __host__ __device__ constexpr uint32_t umma_idesc() {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(NN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void umma_tf32(uint32_t d, uint64_t ad, uint64_t bd, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(ad), "l"(bd), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(mbar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// 16 consecutive fp32 columns of the warp's 32 tensor-memory lanes (thread t: lane base + t)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, "
+      "[%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ float tf32_rna(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+__device__ __forceinline__ void named_bar(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+constexpr int kTcConsumers = 8;                      // 2 consumer warps per block of the quad
+constexpr int kTcThreads = (kTcConsumers + 1) * 32;  // + the control warp
+constexpr int kChunk = 64;                           // codebook entries per MMA chunk
+
+template <int F> struct TcCfg {
+  static constexpr int NQ = Fmt<F>::IQ1 ? 3 : 2;       // An, (Cg), B columns per entry
+  static constexpr int NCH = Fmt<F>::N / kChunk;        // chunks per sweep
+  static constexpr int ALLOC = 2 * NQ * kChunk <= 256 ? 256 : 512;  // tensor-memory columns
+  static constexpr size_t SMEM = (size_t)Fmt<F>::N * 64 + 4 * 4096 + 2 * 128 * 16 * 4 + 2 * 128 * 4 * 4 + 4 * 24 * 4;
+};
+
+template <int F, int MODE, typename TIn>
+__global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, EncWs ws, int64_t nquads) {
+  constexpr int C = Fmt<F>::C, N = Fmt<F>::N, VPG = Fmt<F>::VPG, BB = Fmt<F>::BB, G = Fmt<F>::G;
+  constexpr int NQ = TcCfg<F>::NQ, NCH = TcCfg<F>::NCH, NS = Fmt<F>::IQ1 ? 8 : 16;
+  constexpr uint32_t IDESC = umma_idesc<kChunk>();
+  extern __shared__ __align__(1024) uint8_t smem[];
+  float *cb = reinterpret_cast<float *>(smem);              // codebook g [N x 8], then h [N x 8]
+  float *aop = cb + (size_t)N * 16;                         // [4][128 x 8]: nw2 hi, nw2 lo, w hi, w lo
+  float *xchg = aop + 4 * 1024;                             // [2][128][16] per-choice minima
+  float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
+  uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
+  __shared__ uint64_t cb_bar, full_bar[2], empty_bar[2];
+  __shared__ uint32_t tmem_base;
+  __shared__ int abort_flag;
+
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool control = warp == kTcConsumers;
+  const int quarter = warp & 3, sub = warp >> 2;
+  if (threadIdx.x == 0) {
+    mbar_init(&full_bar[0], 1);
+    mbar_init(&full_bar[1], 1);
+    mbar_init(&empty_bar[0], kTcConsumers);
+    mbar_init(&empty_bar[1], kTcConsumers);
+    abort_flag = 0;
+    mbar_fence_init();
   }
+  if (control) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
+                 "r"(TcCfg<F>::ALLOC));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  const bool grid_bad = ws.hdr[0] != 0;
+  const bool ok = grid_bad || load_codebook(reinterpret_cast<float4 *>(cb), ws.tab, N * 64, &cb_bar);
   if (grid_bad && blockIdx.x == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, IQ_STATUS_BAD_GRID);
-  uint32_t *pb = packbuf + wid * 24;
+  __syncthreads();
+
   const int g0 = lane & ~(VPG - 1);
   const int cg = lane / VPG;
+  const int row = 32 * quarter + lane;                      // this lane's vector in the quad
+  const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16);
+  uint32_t cc = 0;                                          // chunk sequence number
+  uint32_t issued = 0;                                      // (control) chunks committed
   int st_acc = 0;
 
-  for (int64_t b = (int64_t)blockIdx.x * NW + wid; b < a.nblocks; b += (int64_t)gridDim.x * NW) {
+  bool okl = ok;                                            // this thread's waits all completed
+  for (int64_t qd = blockIdx.x; qd < nquads; qd += gridDim.x) {
+    // a timeout is published only before the CTA-wide barrier, so all threads read one value after it
+    if (!okl) {
+      abort_flag = 1;
+      if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+    }
+    const int64_t b = qd * 4 + quarter;
+    bool active = false;
+    uint32_t d16 = 0;
     Vec v;
-    load_block_vec<TIn>(a, b, lane, v);
-    int bad = 0;
-    const uint32_t d16 = grid_bad ? 0u : block_scale<F, MODE>(a, b, lane, v, bad);
-    st_acc |= bad;
-    if (d16 == 0) {
-      if (MODE != MODE_TABLE)
-        for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = 0;
-      if (a.table && MODE != MODE_FIXED) {
-        // every choice decodes to zeros: the error is sum w x^2 (NaN for a rejected block)
-        float cs = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; i++) cs = __fmaf_rn(__fmul_rn(v.w[i], v.x[i]), v.x[i], cs);
-        const float e0 = group_sum<VPG>(cs, g0);
-        const float val = (bad || grid_bad) ? __int_as_float(0x7fc00000) : e0;
-        if (lane == g0)
-          for (int c = 0; c < C; c++) a.table[(b * Fmt<F>::G + cg) * C + c] = val;
+    float Cgrp = 0.0f;
+    if (!control) {
+      int bad = 0;
+      const bool has = b < a.nblocks && !grid_bad;
+      if (has) {
+        load_block_vec<TIn>(a, b, lane, v);
+        d16 = block_scale<F, MODE>(a, b, lane, v, bad);
       }
+      if (sub == 0) st_acc |= bad;
+      active = has && d16 != 0;
+      if (active) {
+        vec_setup<F>(v);
+        Cgrp = group_sum<VPG>(v.Cs, g0);
+      } else if (sub == 0 && b < a.nblocks) {
+        // a rejected or zero-scale block: all-zero payload; every choice decodes to zeros
+        if (MODE != MODE_TABLE)
+          for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = 0;
+        if (a.table && MODE != MODE_FIXED) {
+          float cs = 0.0f;
+          if (has) {
+#pragma unroll
+            for (int i = 0; i < 8; i++) cs = __fmaf_rn(__fmul_rn(v.w[i], v.x[i]), v.x[i], cs);
+          }
+          const float e0 = group_sum<VPG>(cs, g0);
+          const float val = (bad || grid_bad) ? __int_as_float(0x7fc00000) : e0;
+          if (lane == g0)
+            for (int c = 0; c < C; c++) a.table[(b * G + cg) * C + c] = val;
+        }
+      }
+      if (sub == 0) {
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const float nw = active ? v.nw2[k] : 0.0f, ww = active ? v.w[k] : 0.0f;
+          const float nh = tf32_rna(nw), wh = tf32_rna(ww);
+          aop[0 * 1024 + kmaj(row, k)] = nh;
+          aop[1 * 1024 + kmaj(row, k)] = tf32_rna(__fsub_rn(nw, nh));
+          aop[2 * 1024 + kmaj(row, k)] = wh;
+          aop[3 * 1024 + kmaj(row, k)] = tf32_rna(__fsub_rn(ww, wh));
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      }
+    }
+    named_bar(1, kTcThreads);  // the quad's operands are in shared memory; the previous quad is done
+    if (*(volatile int *)&abort_flag) break;
+
+    if (control) {
+      // ---- MMA issue: sweep 1 (unless fixed choices) and sweep 2 (unless table only) ---------
+      if (lane == 0) {
+        const int nsweeps = (MODE != MODE_FIXED) + (MODE != MODE_TABLE);
+        const uint32_t sa = smem_u32(aop), sg = smem_u32(cb), sh = sg + N * 32;
+        for (int sw = 0; sw < nsweeps; sw++) {
+          for (int ch = 0; ch < NCH; ch++, issued++) {
+            const uint32_t buf = issued & 1;
+            if (!okl || (issued >= 2 && !mbar_wait_bounded(&empty_bar[buf], ((issued >> 1) - 1) & 1))) {
+              okl = false;  // stop issuing; consumers' waits on the missing chunks time out
+              break;
+            }
+            tc_fence_after();
+            const uint32_t d = tmem + buf * NQ * kChunk;
+            const uint64_t bg = umma_desc(sg + ch * kChunk * 32), bh = umma_desc(sh + ch * kChunk * 32);
+            umma_tf32(d, umma_desc(sa + 0 * 4096), bg, IDESC, 0);          // An = nw2 . g
+            umma_tf32(d, umma_desc(sa + 1 * 4096), bg, IDESC, 1);
+            if (NQ == 3) {
+              umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bg, IDESC, 0);  // Cg = w . g
+              umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bg, IDESC, 1);
+            }
+            umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // B = w . h
+            umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+            umma_commit(&full_bar[buf]);
+          }
+          if (!okl) break;
+        }
+      }
+      okl = __shfl_sync(0xffffffffu, okl, 0);
       continue;
     }
-    const float d = half_bits_to_float((uint16_t)d16);
-    vec_setup<F>(v);
-    const float Cg = group_sum<VPG>(v.Cs, g0);
 
-    int c1;
+    // ---- consumers ---------------------------------------------------------------------------
+    const float d = half_bits_to_float((uint16_t)d16);
+    const IQ1Const kc = iq1_consts();
+    const uint64_t nT2p = pk2(v.nT2, v.nT2), Wsp = pk2(v.Ws, v.Ws);
+    const int ebase0 = 32 * sub;  // this warp's first entry in each chunk
+    // waits for chunk `cc`, hands the warp's 2 x 16 columns to fn(half, An, Cg, B), releases it
+    // (after a timeout the remaining chunks are skipped without waiting)
+    auto run_chunk = [&](auto &&fn) {
+      const uint32_t buf = cc & 1;
+      if (okl && !mbar_wait_bounded(&full_bar[buf], (cc >> 1) & 1)) okl = false;
+      okl = __all_sync(0xffffffffu, okl);
+      tc_fence_after();
+      const uint32_t col = buf * NQ * kChunk + ebase0;
+#pragma unroll
+      for (int h = 0; h < 2; h++) {
+        float An[16], Bq[16], Cq[16];
+        tmem_ld16(taddr + col + 16 * h, An);
+        if (NQ == 3) tmem_ld16(taddr + col + kChunk + 16 * h, Cq);
+        tmem_ld16(taddr + col + (NQ - 1) * kChunk + 16 * h, Bq);
+        tmem_wait_ld();
+        if (active && okl) fn(h, An, Cq, Bq);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty_bar[buf]);
+      cc++;
+    };
+
+    int c1 = 0;
     bool gflag = false;
     if (MODE != MODE_FIXED) {
-      float al[Fmt<F>::IQ1 ? 8 : 16];
-#pragma unroll
-      for (int s = 0; s < (Fmt<F>::IQ1 ? 8 : 16); s++) al[s] = alpha_of<F>(d, s);
       float m[C];
-      sweep_minima<F>(v, tab, al, m);
-      float D1 = INFINITY, D2 = INFINITY;
-      c1 = 0;
 #pragma unroll
-      for (int c = 0; c < C; c++) {
-        const float S = group_sum<VPG>(m[c], g0);
-        const float D = __fmul_rn(al[F == IQ1_S ? (c & 7) : c], S);
-        if (a.table && lane == g0) a.table[(b * Fmt<F>::G + cg) * C + c] = __fadd_rn(Cg, D);
-        D2 = fminf(D2, fmaxf(D1, D));
-        if (D < D1) { D1 = D; c1 = c; }
+      for (int c = 0; c < C; c++) m[c] = INFINITY;
+      uint64_t alp[NS];
+#pragma unroll
+      for (int s = 0; s < NS; s++) { const float al = alpha_of<F>(d, s); alp[s] = pk2(al, al); }
+      for (int ch = 0; ch < NCH; ch++) {
+        run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
+            if (!Fmt<F>::IQ1) {
+#pragma unroll
+              for (int c = 0; c < C; c++) {
+                const float2 sc = up2(ffma2(alp[c], B2, A2));
+                m[c] = min3f(m[c], sc.x, sc.y);
+              }
+            } else {
+              const uint64_t C2 = pk2(Cq[2 * i], Cq[2 * i + 1]);
+              const uint64_t Anp = ffma2(kc.p125, nT2p, A2), Anm = ffma2(kc.m125, nT2p, A2);
+              const uint64_t Bw = ffma2(kc.w64, Wsp, B2);
+              const uint64_t Bp = ffma2(kc.p025, C2, Bw), Bm = ffma2(kc.m025, C2, Bw);
+#pragma unroll
+              for (int s = 0; s < 8; s++) {
+                const float2 sp = up2(ffma2(alp[s], Bp, Anp)), sm = up2(ffma2(alp[s], Bm, Anm));
+                if (F == IQ1_S) {
+                  m[s] = min3f(m[s], sp.x, sp.y);
+                  m[8 + s] = min3f(m[8 + s], sm.x, sm.y);
+                } else {
+                  m[s] = min3f(min3f(m[s], sp.x, sp.y), sm.x, sm.y);
+                }
+              }
+            }
+          }
+        });
       }
-      gflag = __fsub_rn(D2, D1) <= kMargin * (4.0f * Cg + D1 + D2);
-      if (MODE == MODE_TABLE) continue;
-    } else {
-      c1 = a.choices[b * Fmt<F>::G + cg];
+      // minima of the two consumer warps of this block
+#pragma unroll
+      for (int c = 0; c < C; c++) xchg[(sub * 128 + row) * 16 + c] = m[c];
+      named_bar(2, kTcConsumers * 32);
+#pragma unroll
+      for (int c = 0; c < C; c++) m[c] = fminf(xchg[row * 16 + c], xchg[(128 + row) * 16 + c]);
+      if (active) {
+        float D1 = INFINITY, D2 = INFINITY;
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+          const float S = group_sum<VPG>(m[c], g0);
+          const float D = __fmul_rn(alpha_of<F>(d, F == IQ1_S ? (c & 7) : c), S);
+          if (a.table && sub == 0 && lane == g0) a.table[(b * G + cg) * C + c] = __fadd_rn(Cgrp, D);
+          D2 = fminf(D2, fmaxf(D1, D));
+          if (D < D1) { D1 = D; c1 = c; }
+        }
+        gflag = __fsub_rn(D2, D1) <= kMargin * (4.0f * Cgrp + D1 + D2);
+      }
+    } else if (active) {
+      c1 = a.choices[b * G + cg];
     }
-    // entry pick under c1
-    const float alpha = alpha_choice<F>(d, c1);
-    float s1, s2;
-    int key;
-    sweep_pick<F>(v, tab, alpha, F == IQ1_S ? (c1 >> 3) : 0, s1, s2, key);
-    const float e1 = __fmul_rn(alpha, s1), e2 = __fmul_rn(alpha, s2);
-    const bool vflag = __fsub_rn(e2, e1) <= kMargin * (4.0f * v.Cs + e1 + e2);
-    // pack
-    if (lane < 24) pb[lane] = 0u;
-    __syncwarp();
-    const int idx = F == IQ1_M ? (key % N) : key;
-    const Bits lo = f_idx_lo<F>(lane);
-    put_bits(pb, lo, (uint32_t)idx);
-    if (F == IQ2_S || Fmt<F>::IQ1) put_bits(pb, f_idx_hi<F>(lane), (uint32_t)idx >> lo.width);
-    if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)v.sgn);
-    if (F == IQ1_M) {
-      put_bits(pb, f_dbit_vec<F>(lane), (uint32_t)(key / N));
-      if (lane < 4) put_bits(pb, f_d16_nib<F>(lane), (d16 >> (4 * lane)) & 15u);
-    } else if (lane == 0) {
-      put_bits(pb, f_d16<F>(), d16);
-    }
-    if (lane == g0) {
-      put_bits(pb, f_scale<F>(cg), (uint32_t)(F == IQ1_S ? (c1 & 7) : c1));
-      if (F == IQ1_S) put_bits(pb, f_dbit_grp<F>(cg), (uint32_t)(c1 >> 3));
-    }
-    __syncwarp();
-    const uint8_t *pbytes = reinterpret_cast<const uint8_t *>(pb);
-    for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = pbytes[i];
-    __syncwarp();
-    const uint32_t flags = __ballot_sync(0xffffffffu, gflag || vflag);
-    if (flags && lane == 0) {
-      const int slot = atomicAdd(&ws.hdr[1], 1);
-      ws.fb[slot] = make_uint2((uint32_t)b, flags);
+
+    if (MODE != MODE_TABLE) {
+      // ---- sweep 2: best candidate and runner-up under choice c1 ---------------------------
+      const float alpha = alpha_choice<F>(d, c1);
+      const uint64_t al = pk2(alpha, alpha);
+      const int dbit = F == IQ1_S ? (c1 >> 3) : 0;
+      const uint64_t dA = dbit ? kc.m125 : kc.p125, dB = dbit ? kc.m025 : kc.p025;
+      float best = INFINITY, second = INFINITY;
+      int key = 0;
+      for (int ch = 0; ch < NCH; ch++) {
+        const int eb = ch * kChunk + ebase0;
+        run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const int e0 = eb + 16 * h + 2 * i;
+            const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
+            if (!Fmt<F>::IQ1) {
+              track2(up2(ffma2(al, B2, A2)), e0, best, second, key);
+            } else {
+              const uint64_t C2 = pk2(Cq[2 * i], Cq[2 * i + 1]);
+              const uint64_t Bw = ffma2(kc.w64, Wsp, B2);
+              if (F == IQ1_S) {
+                const uint64_t Ad = ffma2(dA, nT2p, A2), Bd = ffma2(dB, C2, Bw);
+                track2(up2(ffma2(al, Bd, Ad)), e0, best, second, key);
+              } else {
+                const uint64_t Anp = ffma2(kc.p125, nT2p, A2), Anm = ffma2(kc.m125, nT2p, A2);
+                const uint64_t Bp = ffma2(kc.p025, C2, Bw), Bm = ffma2(kc.m025, C2, Bw);
+                track2(up2(ffma2(al, Bp, Anp)), e0, best, second, key);
+                track2(up2(ffma2(al, Bm, Anm)), N + e0, best, second, key);
+              }
+            }
+          }
+        });
+      }
+      xchg2[sub * 128 + row] = make_float4(best, second, __int_as_float(key), 0.0f);
+      named_bar(2, kTcConsumers * 32);
+      if (sub == 0 && active) {
+        const float4 o0 = xchg2[row], o1 = xchg2[128 + row];
+        const int k0 = __float_as_int(o0.z), k1 = __float_as_int(o1.z);
+        const bool first = o0.x < o1.x || (o0.x == o1.x && k0 < k1);
+        const float s1 = fminf(o0.x, o1.x);
+        const float s2 = min3f(fmaxf(o0.x, o1.x), o0.y, o1.y);
+        key = first ? k0 : k1;
+        const float e1 = __fmul_rn(alpha, s1), e2 = __fmul_rn(alpha, s2);
+        const bool vflag = __fsub_rn(e2, e1) <= kMargin * (4.0f * v.Cs + e1 + e2);
+        // pack
+        uint32_t *pb = packbuf + quarter * 24;
+        if (lane < 24) pb[lane] = 0u;
+        __syncwarp();
+        const int idx = F == IQ1_M ? (key % N) : key;
+        const Bits lo = f_idx_lo<F>(lane);
+        put_bits(pb, lo, (uint32_t)idx);
+        if (F == IQ2_S || Fmt<F>::IQ1) put_bits(pb, f_idx_hi<F>(lane), (uint32_t)idx >> lo.width);
+        if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)v.sgn);
+        if (F == IQ1_M) {
+          put_bits(pb, f_dbit_vec<F>(lane), (uint32_t)(key / N));
+          if (lane < 4) put_bits(pb, f_d16_nib<F>(lane), (d16 >> (4 * lane)) & 15u);
+        } else if (lane == 0) {
+          put_bits(pb, f_d16<F>(), d16);
+        }
+        if (lane == g0) {
+          put_bits(pb, f_scale<F>(cg), (uint32_t)(F == IQ1_S ? (c1 & 7) : c1));
+          if (F == IQ1_S) put_bits(pb, f_dbit_grp<F>(cg), (uint32_t)(c1 >> 3));
+        }
+        __syncwarp();
+        const uint8_t *pbytes = reinterpret_cast<const uint8_t *>(pb);
+        for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = pbytes[i];
+        __syncwarp();
+        const uint32_t flags = __ballot_sync(0xffffffffu, gflag || vflag);
+        if (flags && lane == 0) {
+          const int slot = atomicAdd(&ws.hdr[1], 1);
+          ws.fb[slot] = make_uint2((uint32_t)b, flags);
+        }
+      }
     }
   }
-  if (st_acc && a.status) atomicOr(a.status, st_acc);
+  if (!okl && a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+  if (st_acc && a.status && lane == 0) atomicOr(a.status, st_acc);
+  // every committed chunk must have completed before tensor memory is released
+  if (control && lane == 0) {
+    for (uint32_t u = issued >= 2 ? issued - 2 : 0; u < issued; u++) mbar_wait_bounded(&full_bar[u & 1], (u >> 1) & 1);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (control) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TcCfg<F>::ALLOC));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -638,7 +785,7 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
         for (int c = 0; c < C; c++) lm[c] = INFINITY;
         for (int e = lane; e < N; e += 32) {
           Entry en;
-          load_entry(tab, e, en);
+          load_entry<F>(tab, e, en);
 #pragma unroll
           for (int c = 0; c < C; c++) {
             if (MODE == MODE_FIXED && c != cfix) continue;
@@ -687,7 +834,7 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
           int bestK = 0x7fffffff;
           for (int e = lane; e < N; e += 32) {
             Entry en;
-            load_entry(tab, e, en);
+            load_entry<F>(tab, e, en);
             for (int db = db0; db <= db1; db++) {
               const float sc = cand_score<F>(u, en, al, db);
               const float ec = __fmul_rn(al, sc);
@@ -778,22 +925,23 @@ static int run_anchor(const void *W, int64_t cols, int64_t nb, uint16_t *d16, in
 template <int F, int MODE, typename TIn>
 static int run_encode(const EncArgs &a, void *workspace, size_t ws_bytes, cudaStream_t st) {
   constexpr int N = Fmt<F>::N;
-  constexpr int THREADS = Fmt<F>::IQ1 ? 512 : 256;
   if (a.nblocks == 0) return IQ_OK;
   EncWs ws = enc_ws(workspace, N);
   if (cudaMemsetAsync(ws.hdr, 0, 256, st) != cudaSuccess) return IQ_ERR_CUDA;
   prep_codebook<F><<<(N + 255) / 256, 256, 0, st>>>(a.grid, ws);
-  const size_t smem = (size_t)N * 64 + (THREADS / 32) * 24 * 4;
-  auto kern = encode_kernel<F, MODE, TIn, THREADS>;
+  const size_t smem = TcCfg<F>::SMEM;
+  auto kern = encode_tc_kernel<F, MODE, TIn>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
   int per_sm = 1;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTcThreads, smem);
   if (per_sm < 1) per_sm = 1;
-  const int64_t want = (a.nblocks + THREADS / 32 - 1) / (THREADS / 32);
+  // tensor memory: at most 512 columns per SM among the resident CTAs
+  if (per_sm * TcCfg<F>::ALLOC > 512) per_sm = 512 / TcCfg<F>::ALLOC;
+  const int64_t nquads = (a.nblocks + 3) / 4;
   const int64_t cap = (int64_t)num_sms() * per_sm;
-  const int grid = (int)(want < cap ? want : cap);
-  kern<<<grid, THREADS, smem, st>>>(a, ws);
+  const int grid = (int)(nquads < cap ? nquads : cap);
+  kern<<<grid, kTcThreads, smem, st>>>(a, ws, nquads);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   if (MODE != MODE_TABLE) {
     rescore_kernel<F, MODE, TIn><<<num_sms() * 2, 256, 0, st>>>(a, ws);
