@@ -43,6 +43,15 @@ CONFIG = {"workload": "encode 5632x2048 bf16 weight in IQ2_XXS/IQ2_XS/IQ2_S/IQ1_
 
 
 MOE_T, MOE_C, MOE_E, MOE_K = 4096, 17408, 128, 8
+DEC_R, DEC_C = 17408, 5120
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the searched encode
+# kernel on this workload, from the ncu captures summarised in profiles/encode_tc_searched_5632x2048.md,
+# and the SHA-256 of the encoder sources they were taken on: the figure is reported only while the
+# sources are unchanged.
+PROFILED_ENCODE_TRAFFIC = {"IQ2_XXS": 23170560, "IQ1_S": 23267328, "IQ1_M": 23273216}
+PROFILED_ENCODE_SHA256 = "298d546b7780ea6fb66cdbcbb552568e983857004298c25a5e9df869747c260c"
+ENCODE_SOURCES = ("ggml_iq_codebook_accumulate_b300/csrc/iq_encode.cu", "ggml_iq_codebook_accumulate_b300/csrc/iq_common.cuh")
 
 
 def measured_peaks():
@@ -55,11 +64,27 @@ def measured_peaks():
         return 6400.0, "fallback"
 
 
+def encode_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for f in ENCODE_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def flops_per_element(fmt):
     """Algorithmic FP32 work of the searched encode per weight element: per codebook entry and
     8-value vector, IQ2 16 FMA for (A, B) + 16 choices x (FMA + min) = 80 flops; IQ1 24 FMA +
     4 shifted-form FMA + 16 x (FMA + min) = 104 flops (FMA = 2, min = 1)."""
     return (10 if fmt.startswith("IQ2") else 13) * ENTRIES[fmt]
+
+
+def cuda_core_flops_per_element(fmt):
+    """The part of the cost model that still runs on the FP32 lanes once the per-entry dot
+    products run on the tensor cores: per entry and vector, 16 choices x (FMA + min) = 48 flops for
+    IQ2; IQ1 adds 5 FMAs for the shifted sums: 58 flops."""
+    return (6.0 if fmt.startswith("IQ2") else 7.25) * ENTRIES[fmt]
 
 
 def fp32_peak_tflops(sms, mhz):
@@ -80,7 +105,7 @@ def run_reference(args):
     import oracle
     oracle.build()
     Wst, Wv, Xst, Xv, grids = inputs()
-    rows = int(os.environ.get("IQ_REF_ROWS", "16"))
+    rows = int(os.environ.get("IQ_REF_ROWS", "128"))
     ids = np.zeros((T_ACT, 1), np.int32)
 
     def step():
@@ -112,7 +137,7 @@ def run_reference(args):
     print(json.dumps(line))
 
 
-def cpu_baseline_sample(Wv, Xv, grids, budget_rows=16):
+def cpu_baseline_sample(Wv, Xv, grids, budget_rows=768):
     import oracle
     oracle.build()
     ids = np.zeros((T_ACT, 1), np.int32)
@@ -178,12 +203,9 @@ class Clocks:
 def run_ours(args):
     import torch
 
-    from ggml_iq_codebook_accumulate_b300 import api
+    from ggml_iq_codebook_accumulate_b300 import api, replicas
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    dist = None
+    rank, world, local = replicas.world_info()
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
@@ -242,6 +264,9 @@ def run_ours(args):
         for _, fn in parts:
             fn()
 
+    if args.only:
+        run_only(args, dev, dict(parts), flush, stream)
+        return
     for _ in range(args.warmup):                       # eager warm-up (loads modules, sets attributes)
         step()
     torch.cuda.synchronize()
@@ -259,8 +284,7 @@ def run_ours(args):
     for _ in range(2):
         g_step.replay()
     torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
+    replicas.barrier()
 
     def timed(g):
         flush.fill_(1)                                 # L2 flushed before every timed replay
@@ -276,23 +300,18 @@ def run_ours(args):
         evs = [timed(g_step) for _ in range(args.steps)]
         torch.cuda.synchronize()
         totals = [a.elapsed_time(b) for a, b in evs]
-    if dist:
-        dist.barrier()
+    replicas.barrier()
     per = {n: [] for n, _ in parts}
     for _ in range(max(3, args.steps)):
         evs = {n: timed(g_part[n]) for n, _ in parts}
         torch.cuda.synchronize()
         for n, (a, b) in evs.items():
             per[n].append(a.elapsed_time(b))
-    ms = float(np.mean(totals))
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = replicas.max_over_ranks(float(np.mean(totals)), device=dev)
     if rank != 0:
         return
     clocks = clk.summary()
-    value = world * 5 * R * C / (ms * 1e-3) / 1e6
+    value = replicas.job_throughput(5 * R * C, ms * 1e-3, world) / 1e6
     # per-kernel figures
     pf = {}
     for f in FORMATS:
@@ -308,6 +327,7 @@ def run_ours(args):
     im_bytes = T_ACT * C * 2 + T_ACT * 4 + 2 * C * 4
     hbm, hbm_src = measured_peaks()
     moe = measure_imatrix_moe(args, dev, flush, hbm)
+    dec_large = measure_decode_large(args, dev, flush, hbm)
     for f in FORMATS:
         pf[f]["decode_frac_hbm"] = round(pf[f]["decode_GB_s"] / hbm, 4)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -315,11 +335,15 @@ def run_ours(args):
     dom_ms = pf[dom]["encode_ms"]
     achieved = R * C * flops_per_element(dom) / (dom_ms * 1e-3) / 1e12
     peak = fp32_peak_tflops(sms, 2032.0)
-    prof_traffic = None
-    roofline = {"kernel": f"encode (searched + every-choice table) {dom}", "bound": "alu",
+    prof_traffic = (PROFILED_ENCODE_TRAFFIC.get(dom) if encode_sources_sha256() == PROFILED_ENCODE_SHA256 else None)
+    achieved_cc = R * C * cuda_core_flops_per_element(dom) / (dom_ms * 1e-3) / 1e12
+    roofline = {"kernel": f"iq_encode call {dom} (prep_codebook + encode_tc_kernel + rescore_kernel; searched + "
+                          "every-choice table)", "bound": "alu",
                 "achieved": round(achieved, 3), "peak": round(peak, 3), "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 4), "traffic": prof_traffic,
-                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flops x 2032 MHz (max SM clock)"}
+                "peak_source": f"{sms} SMs x 128 FP32 lanes x 2 flops x 2032 MHz (max SM clock)",
+                "flops_per_element": flops_per_element(dom),
+                "frac_cuda_core_work": round(achieved_cc / peak, 4)}
     if clocks.get("sm_mhz"):
         roofline["frac_at_observed_clock"] = round(achieved / fp32_peak_tflops(sms, clocks["sm_mhz"]), 4)
     # end to end through the public API with host buffers
@@ -337,8 +361,75 @@ def run_ours(args):
             "per_format": pf,
             "imatrix": {"ms": round(im_ms, 4), "GB_s": round(im_bytes / (im_ms * 1e-3) / 1e9, 1),
                         "frac_hbm": round(im_bytes / (im_ms * 1e-3) / 1e9 / hbm, 4)},
-            "imatrix_moe": moe, "hbm_peak_GB_s": hbm, "hbm_peak_source": hbm_src}
+            "imatrix_moe": moe, "decode_large": dec_large, "hbm_peak_GB_s": hbm, "hbm_peak_source": hbm_src}
     print(json.dumps(line))
+
+
+def run_only(args, dev, fns, flush, stream):
+    """One part of the step on its own (the profiling runs): --warmup untimed eager calls, then
+    --steps calls each timed with CUDA events after an L2 flush.  Parts: imatrix, weights,
+    encode:<fmt>, fixed:<fmt>, decode:<fmt>, imatrix_moe, decode_large."""
+    import torch
+    if args.only in ("imatrix_moe", "decode_large"):
+        hbm, _ = measured_peaks()
+        fn = measure_imatrix_moe if args.only == "imatrix_moe" else measure_decode_large
+        print(json.dumps({"only": args.only, **fn(args, dev, flush, hbm)}))
+        return
+    if args.only not in fns:
+        raise SystemExit(f"--only: unknown part {args.only!r}; one of {sorted(fns) + ['imatrix_moe', 'decode_large']}")
+    fns["imatrix"]()
+    fns["weights"]()
+    fn = fns[args.only]
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(args.steps):
+        flush.fill_(3)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    print(json.dumps({"only": args.only, "steps": args.steps, "warmup": args.warmup,
+                      "ms_mean": round(float(np.mean(times)), 4), "ms_min": round(float(np.min(times)), 4)}))
+
+
+def measure_decode_large(args, dev, flush, hbm):
+    """Decode of one large-layer weight, 17408 x 5120 (Student-t nu=4 x 0.02, bf16), from its
+    searched IQ2_XXS payload to fp32.  The 356.5 MB output is about three times L2, so the kernel
+    writes to HBM.  Algorithmic bytes: the payload read once, the codebook, the output written."""
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api, synth
+    store, _ = synth.as_dtype(synth.weight_t4(DEC_R, DEC_C, seed=4), "bf16")
+    W = torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(dev)
+    g = torch.from_numpy(synth.grid("IQ2_XXS")).to(dev)
+    pay = api.encode("IQ2_XXS", W, g)
+    del W
+    out = torch.empty(DEC_R, DEC_C, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(3):
+        api.decode("IQ2_XXS", pay, DEC_R, DEC_C, g, out=out)
+    torch.cuda.synchronize()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr):
+        api.decode("IQ2_XXS", pay, DEC_R, DEC_C, g, out=out)
+    times = []
+    for _ in range(max(5, args.steps)):
+        flush.fill_(4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        gr.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = float(np.median(times))
+    nbytes = pay.numel() + out.numel() * 4 + g.numel() * 4
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": f"IQ2_XXS payload of a {DEC_R}x{DEC_C} bf16 weight -> fp32", "ms": round(ms, 4),
+            "GB_s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "algorithmic_bytes": int(nbytes)}
 
 
 def measure_imatrix_moe(args, dev, flush, hbm):
@@ -428,6 +519,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--only", default=None,
+                    help="run one part of the step alone and print its time (for profiling runs)")
     args = ap.parse_args()
     if args.impl == "reference":
         if int(os.environ.get("RANK", "0")) != 0:
