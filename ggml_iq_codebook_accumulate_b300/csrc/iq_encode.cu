@@ -528,6 +528,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
 
     int c1 = 0;
     bool gflag = false;
+    float smin = 0.0f;  // searched mode: this vector's minimum score under c1 (from sweep 1)
     if (MODE != MODE_FIXED) {
       float m[C];
 #pragma unroll
@@ -579,7 +580,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           const float D = __fmul_rn(alpha_of<F>(d, F == IQ1_S ? (c & 7) : c), S);
           if (a.table && sub == 0 && lane == g0) a.table[(b * G + cg) * C + c] = __fadd_rn(Cgrp, D);
           D2 = fminf(D2, fmaxf(D1, D));
-          if (D < D1) { D1 = D; c1 = c; }
+          if (D < D1) { D1 = D; c1 = c; smin = m[c]; }
         }
         gflag = __fsub_rn(D2, D1) <= kMargin * (4.0f * Cgrp + D1 + D2);
       }
@@ -589,34 +590,66 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
 
     if (MODE != MODE_TABLE) {
       // ---- sweep 2: best candidate and runner-up under choice c1 ---------------------------
+      // Fixed choices: every candidate goes through the best / runner-up tracking.  Searched
+      // mode: sweep 1 already gave the minimum s1 (the same MMAs and the same rounded packed
+      // FMAs reproduce it exactly), so a part of the sweep is tracked only when one of its
+      // scores is at most T, a bound just above s1.  Every candidate that could flag the vector (gap of the
+      // errors alpha * s within the margin) lies below T; the rest cannot be the best and
+      // cannot flag, so skipping them leaves the key and the flag unchanged.
       const float alpha = alpha_choice<F>(d, c1);
       const uint64_t al = pk2(alpha, alpha);
       const int dbit = F == IQ1_S ? (c1 >> 3) : 0;
       const uint64_t dA = dbit ? kc.m125 : kc.p125, dB = dbit ? kc.m025 : kc.p025;
+      // (With 256 or 512 entries nearly every part holds some lane's best, so the small codebooks
+      // track everything.)
+      constexpr bool kFind = MODE == MODE_SEARCH && N >= 1024;
+      float T = INFINITY;
+      if (kFind && active) {
+        // flag iff e2 - e1 <= kMargin (4 Cs + e1 + e2), i.e. e2 - e1 <= kMargin (4 Cs + 2 e1) /
+        // (1 - kMargin); the factors 1.01 and the relative term cover fp32 rounding here
+        const float e1 = __fmul_rn(alpha, smin);
+        const float De = 1.01f * kMargin * fmaxf(4.0f * v.Cs + 2.0f * e1, 0.0f);
+        T = smin + 1.01f * (De / alpha) + 9.5367431640625e-07f * fabsf(smin);
+      }
       float best = INFINITY, second = INFINITY;
       int key = 0;
+      constexpr int PPH = F == IQ1_M ? 16 : 8;  // candidate pairs per half chunk
       for (int ch = 0; ch < NCH; ch++) {
         const int eb = ch * kChunk + ebase0;
         run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
+          uint64_t sc[PPH];  // pair p: entries e0, e0 + 1 (IQ1_M: p >= 8 the minus shift)
 #pragma unroll
           for (int i = 0; i < 8; i++) {
-            const int e0 = eb + 16 * h + 2 * i;
             const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
             if (!Fmt<F>::IQ1) {
-              track2(up2(ffma2(al, B2, A2)), e0, best, second, key);
+              sc[i] = ffma2(al, B2, A2);
             } else {
               const uint64_t C2 = pk2(Cq[2 * i], Cq[2 * i + 1]);
               const uint64_t Bw = ffma2(kc.w64, Wsp, B2);
               if (F == IQ1_S) {
                 const uint64_t Ad = ffma2(dA, nT2p, A2), Bd = ffma2(dB, C2, Bw);
-                track2(up2(ffma2(al, Bd, Ad)), e0, best, second, key);
+                sc[i] = ffma2(al, Bd, Ad);
               } else {
                 const uint64_t Anp = ffma2(kc.p125, nT2p, A2), Anm = ffma2(kc.m125, nT2p, A2);
                 const uint64_t Bp = ffma2(kc.p025, C2, Bw), Bm = ffma2(kc.m025, C2, Bw);
-                track2(up2(ffma2(al, Bp, Anp)), e0, best, second, key);
-                track2(up2(ffma2(al, Bm, Anm)), N + e0, best, second, key);
+                sc[i] = ffma2(al, Bp, Anp);
+                sc[8 + i] = ffma2(al, Bm, Anm);
               }
             }
+          }
+          if (kFind) {
+            float mn = INFINITY;
+#pragma unroll
+            for (int p = 0; p < PPH; p++) {
+              const float2 q = up2(sc[p]);
+              mn = min3f(mn, q.x, q.y);
+            }
+            if (!(mn <= T)) return;
+          }
+#pragma unroll
+          for (int p = 0; p < PPH; p++) {
+            const int e0 = eb + 16 * h + 2 * (p & 7);
+            track2(up2(sc[p]), p < 8 ? e0 : N + e0, best, second, key);
           }
         });
       }
@@ -630,7 +663,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         const float s2 = min3f(fmaxf(o0.x, o1.x), o0.y, o1.y);
         key = first ? k0 : k1;
         const float e1 = __fmul_rn(alpha, s1), e2 = __fmul_rn(alpha, s2);
-        const bool vflag = __fsub_rn(e2, e1) <= kMargin * (4.0f * v.Cs + e1 + e2);
+        // searched mode: no second candidate near the best means no flag; no best found at all
+        // (cannot happen while both sweeps agree) hands the vector to the exact rescoring
+        const bool vflag = !(s1 < INFINITY) ||
+                           (s2 < INFINITY && __fsub_rn(e2, e1) <= kMargin * (4.0f * v.Cs + e1 + e2));
         // pack
         uint32_t *pb = packbuf + quarter * 24;
         if (lane < 24) pb[lane] = 0u;
