@@ -328,6 +328,7 @@ def run_ours(args):
     hbm, hbm_src = measured_peaks()
     moe = measure_imatrix_moe(args, dev, flush, hbm)
     dec_large = measure_decode_large(args, dev, flush, hbm)
+    lhs = measure_local_hessian(args, dev, flush)
     for f in FORMATS:
         pf[f]["decode_frac_hbm"] = round(pf[f]["decode_GB_s"] / hbm, 4)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
@@ -361,22 +362,25 @@ def run_ours(args):
             "per_format": pf,
             "imatrix": {"ms": round(im_ms, 4), "GB_s": round(im_bytes / (im_ms * 1e-3) / 1e9, 1),
                         "frac_hbm": round(im_bytes / (im_ms * 1e-3) / 1e9 / hbm, 4)},
-            "imatrix_moe": moe, "decode_large": dec_large, "hbm_peak_GB_s": hbm, "hbm_peak_source": hbm_src}
+            "imatrix_moe": moe, "decode_large": dec_large, "local_hessian": lhs, "hbm_peak_GB_s": hbm, "hbm_peak_source": hbm_src}
     print(json.dumps(line))
 
 
 def run_only(args, dev, fns, flush, stream):
     """One part of the step on its own (the profiling runs): --warmup untimed eager calls, then
     --steps calls each timed with CUDA events after an L2 flush.  Parts: imatrix, weights,
-    encode:<fmt>, fixed:<fmt>, decode:<fmt>, imatrix_moe, decode_large."""
+    encode:<fmt>, fixed:<fmt>, decode:<fmt>, imatrix_moe, decode_large, local_hessian."""
     import torch
     if args.only in ("imatrix_moe", "decode_large"):
         hbm, _ = measured_peaks()
         fn = measure_imatrix_moe if args.only == "imatrix_moe" else measure_decode_large
         print(json.dumps({"only": args.only, **fn(args, dev, flush, hbm)}))
         return
+    if args.only == "local_hessian":
+        print(json.dumps({"only": args.only, **measure_local_hessian(args, dev, flush)}))
+        return
     if args.only not in fns:
-        raise SystemExit(f"--only: unknown part {args.only!r}; one of {sorted(fns) + ['imatrix_moe', 'decode_large']}")
+        raise SystemExit(f"--only: unknown part {args.only!r}; one of {sorted(fns) + ['imatrix_moe', 'decode_large', 'local_hessian']}")
     fns["imatrix"]()
     fns["weights"]()
     fn = fns[args.only]
@@ -430,6 +434,70 @@ def measure_decode_large(args, dev, flush, hbm):
     gbs = nbytes / (ms * 1e-3) / 1e9
     return {"workload": f"IQ2_XXS payload of a {DEC_R}x{DEC_C} bf16 weight -> fp32", "ms": round(ms, 4),
             "GB_s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4), "algorithmic_bytes": int(nbytes)}
+
+
+LH_R, LH_C = 4096, 2048
+LH_PAGES_MS = {"IQ2_XXS": 4.8, "IQ2_S": 9.0, "IQ1_S": 5.3}   # per 256-column block of 4096 rows, GB300
+
+
+def lh_inputs():
+    """A 4096 x 2048 bf16 weight (Student-t nu=4 x 0.02) and the input Hessian H = X^T X / n of
+    4096 correlated activations (AR(1) along the columns, coefficient 0.85, log-normal column
+    scales), as its 256 x 256 diagonal blocks; importance sqrt(diag(H)) as on the pages."""
+    from ggml_iq_codebook_accumulate_b300 import synth
+    store, _ = synth.as_dtype(synth.weight_t4(LH_R, LH_C, seed=5), "bf16")
+    rng = np.random.default_rng(5)
+    Z = rng.standard_normal((4096, LH_C))
+    X = np.empty_like(Z)
+    X[:, 0] = Z[:, 0]
+    for j in range(1, LH_C):
+        X[:, j] = 0.85 * X[:, j - 1] + np.sqrt(1 - 0.85 ** 2) * Z[:, j]
+    X *= np.exp(0.5 * rng.standard_normal(LH_C))[None, :]
+    H = X.T @ X / X.shape[0]
+    Hb = np.stack([H[256 * j:256 * (j + 1), 256 * j:256 * (j + 1)] for j in range(LH_C // 256)]).astype(np.float32)
+    return store, Hb, np.sqrt(np.diag(H)).astype(np.float32)
+
+
+def measure_local_hessian(args, dev, flush):
+    """Every-choice encode and local-Hessian choice search of a 4096 x 2048 bf16 weight, per
+    256-column block (the pages' unit: GB300, 4096 rows)."""
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api, synth
+    store, Hb, imp = lh_inputs()
+    W = torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(dev)
+    H = torch.from_numpy(Hb).to(dev)
+    w = torch.from_numpy(imp).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    out = {"workload": f"{LH_R}x{LH_C} bf16 weight, H from 4096 correlated activations, perc_damp 0.3"}
+    for f in LH_PAGES_MS:
+        g = torch.from_numpy(synth.grid(f)).to(dev)
+        ws = api.encode_workspace(f, LH_R, LH_C, dev)
+        lws = api.local_hessian_workspace(f, LH_R, LH_C, dev)
+        pay = api.encode_every_choice(f, W, g, importance=w, workspace=ws)
+        ch = api.local_hessian_choices(f, W, g, pay, H, 0.3, workspace=lws)
+
+        def t(fn):
+            fn()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(max(3, args.steps)):
+                flush.fill_(5)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            return float(np.median(ts))
+
+        ec = t(lambda: api.encode_every_choice(f, W, g, importance=w, payloads=pay, workspace=ws))
+        se = t(lambda: api.local_hessian_choices(f, W, g, pay, H, 0.3, choices=ch, workspace=lws))
+        nblk = LH_C // 256
+        out[f] = {"every_choice_ms": round(ec, 4), "search_ms": round(se, 4),
+                  "ms_per_256col_block": round((ec + se) / nblk, 4),
+                  "pages_gb300_ms_per_256col_block": LH_PAGES_MS[f]}
+    return out
 
 
 def measure_imatrix_moe(args, dev, flush, hbm):

@@ -19,7 +19,8 @@ FMT_ID = {n: i for i, n in enumerate(FORMATS)}
 IQ_F32, IQ_BF16 = 0, 1
 EXPORTS = ("iq_format_info", "iq_imatrix_workspace_size", "iq_imatrix_accumulate", "iq_imatrix_weights",
            "iq_anchor_scales", "iq_encode_workspace_size", "iq_encode", "iq_group_errors", "iq_decode",
-           "iq_encode_static_scratch_capacity", "iq_encode_static_scratch")
+           "iq_encode_static_scratch_capacity", "iq_encode_static_scratch",
+           "iq_encode_every_choice", "iq_local_hessian_workspace_size", "iq_local_hessian_choices")
 
 STATUS_BITS = {
     "BAD_CHOICE": 1, "BAD_EXPERT_ID": 2, "NONFINITE_SUM2": 4, "DUP_EXPERT_ID": 8, "BAD_INPUT": 16,
@@ -58,6 +59,9 @@ def lib():
         L.iq_decode.argtypes = [i32, p, i64, i64, p, p, i32, p]
         L.iq_encode_static_scratch_capacity.argtypes = [i32, ctypes.POINTER(i64)]
         L.iq_encode_static_scratch.argtypes = [i32, p, i32, i64, i64, p, i64, p, p, p, p, p, p, p]
+        L.iq_encode_every_choice.argtypes = [i32, p, i32, i64, i64, p, i64, p, p, p, p, p, sz, p]
+        L.iq_local_hessian_workspace_size.argtypes = [i32, i64, i64, ctypes.POINTER(sz)]
+        L.iq_local_hessian_choices.argtypes = [i32, p, i32, i64, i64, p, p, p, ctypes.c_float, p, p, p, sz, p]
         for n in EXPORTS:
             getattr(L, n).restype = ctypes.c_int
         _lib = L
@@ -189,6 +193,53 @@ def group_errors(fmt, W, grid, importance=None, rows_per_expert=0, d16=None, sta
                                  _p(d16), _p(table), _p(status), _p(workspace), workspace.numel(), _stream(dev)),
            "iq_group_errors")
     return table
+
+
+def encode_every_choice(fmt, W, grid, importance=None, rows_per_expert=0, d16=None, status=None, payloads=None,
+                        workspace=None):
+    """Payloads [num_choices, B, block_bytes] uint8: payloads[c] is the forced encode with every
+    group at choice c."""
+    for t, n in ((W, "W"), (grid, "grid"), (importance, "importance"), (d16, "d16")):
+        _cuda(t, n)
+    info = format_info(fmt)
+    R, C = W.shape
+    B = R * (C // 256)
+    dev = W.device
+    if payloads is None:
+        payloads = torch.empty(info["num_choices"], B, info["block_bytes"], dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = encode_workspace(fmt, R, C, dev)
+    _check(lib().iq_encode_every_choice(FMT_ID[fmt], _p(W), _dt(W), R, C, _p(importance), int(rows_per_expert),
+                                        _p(grid), _p(d16), _p(payloads), _p(status), _p(workspace),
+                                        workspace.numel(), _stream(dev)), "iq_encode_every_choice")
+    return payloads
+
+
+def local_hessian_workspace(fmt, rows, cols, device):
+    n = ctypes.c_size_t()
+    _check(lib().iq_local_hessian_workspace_size(FMT_ID[fmt], rows, cols, ctypes.byref(n)),
+           "iq_local_hessian_workspace_size")
+    return _workspace(n.value, device)
+
+
+def local_hessian_choices(fmt, W, grid, payloads, hessian_blocks, perc_damp=0.3, status=None, choices=None,
+                          workspace=None):
+    """Searched choices [B, groups] uint8 from the every-choice payloads and the [cols / 256, 256,
+    256] fp32 diagonal blocks of the input Hessian."""
+    for t, n in ((W, "W"), (grid, "grid"), (payloads, "payloads"), (hessian_blocks, "hessian_blocks")):
+        _cuda(t, n)
+    info = format_info(fmt)
+    R, C = W.shape
+    B = R * (C // 256)
+    dev = W.device
+    if choices is None:
+        choices = torch.empty(B, info["choice_groups"], dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = local_hessian_workspace(fmt, R, C, dev)
+    _check(lib().iq_local_hessian_choices(FMT_ID[fmt], _p(W), _dt(W), R, C, _p(grid), _p(payloads),
+                                          _p(hessian_blocks), float(perc_damp), _p(choices), _p(status),
+                                          _p(workspace), workspace.numel(), _stream(dev)), "iq_local_hessian_choices")
+    return choices
 
 
 def decode(fmt, payload, rows, cols, grid, dtype=torch.float32, out=None):

@@ -14,7 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libiq_b300.so")
-SOURCES = ["iq_decode.cu", "iq_imatrix.cu", "iq_encode.cu"]
+SOURCES = ["iq_decode.cu", "iq_imatrix.cu", "iq_encode.cu", "iq_local_hessian.cu"]
 NVCC = os.environ.get("NVCC", "nvcc")
 FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]

@@ -75,17 +75,24 @@ __global__ void __launch_bounds__(256) decode_kernel(const uint8_t *__restrict__
   const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
   const int64_t total = nblocks * BB;
+  // windows are aligned on the absolute address: with the payload at m bytes past a 4-byte
+  // boundary, the window of a block starts at the boundary below it (the bytes before the payload
+  // that share its first word are read and shifted out; they lie in the same allocation, whose
+  // start is aligned), and any word reaching past the end is read byte by byte
+  const int m = (int)((uintptr_t)payload & 3);
+  const uint8_t *p0 = payload - m;
+  const int64_t end = total + m;
   const int g0 = lane >> 1, g1 = 16 + (lane >> 1), h = lane & 1;
   for (int64_t b = warp; b < nblocks; b += nwarps) {
-    const int64_t base = b * BB, a0 = base & ~(int64_t)3;
+    const int64_t base = b * BB + m, a0 = base & ~(int64_t)3;
     const int64_t at = a0 + 4 * lane;
     uint32_t wv = 0;
-    if (at + 4 <= total) {
-      wv = __ldg(reinterpret_cast<const uint32_t *>(payload + at));
+    if (at + 4 <= end) {
+      wv = __ldg(reinterpret_cast<const uint32_t *>(p0 + at));
     } else {
 #pragma unroll
       for (int k = 0; k < 4; k++)
-        if (at + k < total) wv |= (uint32_t)payload[at + k] << (8 * k);
+        if (at + k < end && at + k >= m) wv |= (uint32_t)p0[at + k] << (8 * k);
     }
     const int sh = (int)(base - a0) * 8;
     float q0[4], q1[4];
@@ -122,7 +129,7 @@ extern "C" int iq_decode(iq_format f, const uint8_t *payload, int64_t rows, int6
   if (out_dtype != IQ_F32 && out_dtype != IQ_BF16) return IQ_ERR_ARG;
   const int64_t nb = rows * (cols / 256);
   if (nb > 0 && (!payload || !grid || !out)) return IQ_ERR_ARG;
-  if (((uintptr_t)payload & 3) || ((uintptr_t)grid & 15) || ((uintptr_t)out & 15)) return IQ_ERR_ARG;
+  if (((uintptr_t)grid & 15) || ((uintptr_t)out & 15)) return IQ_ERR_ARG;
   cudaStream_t st = (cudaStream_t)stream;
   switch (f) {
     case IQ2_XXS: return launch_decode<IQ2_XXS>(payload, nb, grid, out, out_dtype, st);

@@ -58,11 +58,17 @@ struct EncArgs {
   int64_t rows_per_expert;
   const float *grid;
   const uint16_t *d16;
-  const uint8_t *choices;
+  const uint8_t *choices;  // fixed mode: [B][G], or null with every group at uniform_choice
   uint8_t *payload;
   float *table;
   int32_t *status;
+  int uniform_choice;
 };
+
+// the fixed choice of group g of block b
+template <int G> __device__ __forceinline__ int fixed_choice(const EncArgs &a, int64_t b, int g) {
+  return a.choices ? (int)a.choices[b * G + g] : a.uniform_choice;
+}
 
 // ---------------------------------------------------------------------------------------------
 // Prepared codebook: g [N x 8] then h [N x 8] (h = g^2 for IQ2, |g| for IQ1), each a K-major
@@ -272,7 +278,7 @@ __device__ __forceinline__ uint32_t block_scale(const EncArgs &a, int64_t b, int
   if ((d16 & 0x7c00u) == 0x7c00u || ((d16 & 0x8000u) && (d16 & 0x7fffu))) { bad_bits |= IQ_STATUS_BAD_SCALE; return 0; }
   d16 &= 0x7fffu;
   if (MODE == MODE_FIXED) {
-    const int c = lane < G ? (int)a.choices[b * G + lane] : 0;
+    const int c = lane < G ? fixed_choice<G>(a, b, lane) : 0;
     if (__any_sync(0xffffffffu, c >= C)) { bad_bits |= IQ_STATUS_BAD_CHOICE; return 0; }
   }
   return d16;
@@ -585,7 +591,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         gflag = __fsub_rn(D2, D1) <= kMargin * (4.0f * Cgrp + D1 + D2);
       }
     } else if (active) {
-      c1 = a.choices[b * G + cg];
+      c1 = fixed_choice<G>(a, b, cg);
     }
 
     if (MODE != MODE_TABLE) {
@@ -812,7 +818,7 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
       if (!(mask & gm)) continue;
       float Cg = 0.0f;
       // (a) fp32 per-vector minima for every choice (or the fixed one), as the sweep computes them
-      int cfix = MODE == MODE_FIXED ? (int)a.choices[b * G + g] : -1;
+      int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : -1;
       for (int k = 0; k < VPG; k++) {
         const Vec u = shfl_vec(v, g * VPG + k);
         Cg = k == 0 ? u.Cs : __fadd_rn(Cg, u.Cs);
@@ -1057,7 +1063,7 @@ extern "C" int iq_encode(iq_format f, const void *W, iq_dtype dt, int64_t rows, 
   size_t need = 0;
   iq_encode_workspace_size(f, rows, cols, &need);
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
-  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, choices, payload, group_errors, status};
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, choices, payload, group_errors, status, 0};
   cudaStream_t st = (cudaStream_t)stream;
   if (choices)
     return dt == IQ_BF16 ? dispatch_encode<MODE_FIXED, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
@@ -1078,10 +1084,37 @@ extern "C" int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t 
   size_t need = 0;
   iq_encode_workspace_size(f, rows, cols, &need);
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
-  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, nullptr, group_errors, status};
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, nullptr, group_errors, status, 0};
   cudaStream_t st = (cudaStream_t)stream;
   return dt == IQ_BF16 ? dispatch_encode<MODE_TABLE, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
                        : dispatch_encode<MODE_TABLE, float>(f, a, workspace, workspace_bytes, st);
+}
+
+// Every-choice payloads (PR #3159): payload c is the forced encode with every group at choice c,
+// one fixed-choice pass per choice (each pass's near ties are rescored exactly, so every payload is
+// byte-identical to the forced encode).
+extern "C" int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                                      const float *importance, int64_t rows_per_expert, const float *grid,
+                                      const uint16_t *d16, uint8_t *payloads, int32_t *status, void *workspace,
+                                      size_t workspace_bytes, void *stream) {
+  int rc = check_common(f, W, dt, rows, cols, importance, rows_per_expert, grid);
+  if (rc) return rc;
+  const int64_t nb = rows * (cols / 256);
+  if (nb > 0 && !payloads) return IQ_ERR_ARG;
+  size_t need = 0;
+  iq_encode_workspace_size(f, rows, cols, &need);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
+  iq_format_info_t info;
+  iq_format_info(f, &info);
+  cudaStream_t st = (cudaStream_t)stream;
+  for (int c = 0; c < info.num_choices; c++) {
+    EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr,
+              payloads + (size_t)c * nb * info.block_bytes, nullptr, status, c};
+    rc = dt == IQ_BF16 ? dispatch_encode<MODE_FIXED, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
+                       : dispatch_encode<MODE_FIXED, float>(f, a, workspace, workspace_bytes, st);
+    if (rc) return rc;
+  }
+  return IQ_OK;
 }
 
 extern "C" int iq_format_info(iq_format f, iq_format_info_t *out) {

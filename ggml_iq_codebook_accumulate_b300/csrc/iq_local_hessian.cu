@@ -1,0 +1,283 @@
+// Local-Hessian choice search (PR #3158 "local_hessian for GGML IQ", What does this PR do?) over
+// the every-choice payloads (PR #3159 "one-pass every-choice encode").
+//
+// For a block (256 values of one row) and its dequantized values q_c under every choice c,
+// dw_c = x - q_c.  H' = H_bb + perc_damp * mean(diag(H_bb)) * I is the damped 256 x 256 diagonal
+// block of the input Hessian for the block's columns (damped as GPTQ damps).
+//   Step 2: every group g takes argmin_c Q_g(c), Q_g(c) = dw_g(c)^T H'_gg dw_g(c) (lowest c on
+//           equal values).
+//   Step 3: two passes over the groups in ascending order; group g moves to the choice c that
+//           minimises the block error dw^T H' dw with the other groups held, when that is strictly
+//           lower than with its current choice (the lowest c among equal minima).  With
+//           U = H'_{g, other groups} dw_{other groups} the change of the block error is
+//               dE(c) = 2 (dw_g(c) - dw_g(cur)) . U_g + Q_g(c) - Q_g(cur),
+//           so a visit costs one dot product of the group's width per choice, and a move updates
+//           U by the product of the group's Hessian panel with the change of dw_g.
+//
+// Work layout: one CTA per (256-column block j, tile of kLhRows rows), 256 threads; thread i owns
+// column i of the block in the U products.  The damped group-diagonal blocks of H', the tile's x,
+// dw of the current choices, U and the Q_g(c) table live in shared memory; the off-diagonal panels
+// of H' are read from global memory in coalesced rows (every tile of a column block reads the same
+// 256 KB, which stays in L2).  The dequantized values of every choice come from the decoder, written
+// once into the workspace.  All arithmetic is fp32.
+#include <cmath>
+
+#include "iq_common.cuh"
+
+namespace iqk {
+
+constexpr int kLhRows = 16;      // rows per tile
+constexpr int kLhThreads = 256;  // one thread per column of the block
+
+template <int F> struct LhCfg {
+  static constexpr int G = Fmt<F>::G, NC = Fmt<F>::C, GS = 256 / G;
+  static constexpr int GPW = 32 / GS;  // groups a warp handles side by side (1 or 2)
+  // Hgg [256][GS], Qe [kLhRows][G][NC], Xs / DWt / U [256][kLhRows], Dl [GS][kLhRows], cur [kLhRows][G]
+  static constexpr size_t SMEM =
+      4 * ((size_t)256 * GS + (size_t)kLhRows * G * NC + 3 * 256 * kLhRows + GS * kLhRows + kLhRows * G) + 64;
+};
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <int F, typename TIn>
+__global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__restrict__ W, int64_t rows, int64_t cols,
+                                                               const float *__restrict__ Q,
+                                                               const float *__restrict__ H, float perc_damp,
+                                                               uint8_t *__restrict__ choices,
+                                                               int32_t *__restrict__ status) {
+  using Cfg = LhCfg<F>;
+  constexpr int G = Cfg::G, NC = Cfg::NC, GS = Cfg::GS, GPW = Cfg::GPW, R = kLhRows;
+  extern __shared__ __align__(16) float sm[];
+  float *Hgg = sm;                      // Hgg[(g*GS + b)*GS + a] = H'[g*GS + b][g*GS + a]
+  float *Qe = Hgg + 256 * GS;           // [R][G][NC]
+  float *Xs = Qe + R * G * NC;          // [256][R] x
+  float *DWt = Xs + 256 * R;            // [256][R] dw of the current choices
+  float *U = DWt + 256 * R;             // [256][R] off-diagonal products
+  float *Dl = U + 256 * R;              // [GS][R] change of dw_g after a move
+  int *cur = reinterpret_cast<int *>(Dl + GS * R);  // [R][G]
+  __shared__ float red[kLhThreads / 32];
+  __shared__ int moved;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int64_t nb = cols / 256;
+  const int64_t j = blockIdx.x;
+  const float *Hj = H + (size_t)j * 256 * 256;
+  const int64_t ntiles = (rows + R - 1) / R;
+
+  // damping: lambda = perc_damp * mean(diag(H_bb))
+  float dsum = Hj[(size_t)tid * 257];
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, off);
+  if (lane == 0) red[warp] = dsum;
+  __syncthreads();
+  float tot = 0.0f;
+#pragma unroll
+  for (int w = 0; w < kLhThreads / 32; w++) tot += red[w];
+  const float lam = perc_damp * (tot * (1.0f / 256.0f));
+  if (!isfinite(lam)) {
+    if (tid == 0 && blockIdx.y == 0 && status) atomicOr(status, IQ_STATUS_BAD_INPUT);
+  }
+  {  // damped group-diagonal blocks (column tid = g*GS + a)
+    const int g = tid / GS, a = tid % GS;
+    for (int b = 0; b < GS; b++) {
+      const float h = Hj[(size_t)(g * GS + b) * 256 + g * GS + a];
+      Hgg[(g * GS + b) * GS + a] = b == a ? __fadd_rn(h, lam) : h;
+    }
+  }
+  __syncthreads();
+
+  for (int64_t tile = blockIdx.y; tile < ntiles; tile += gridDim.y) {
+    const int64_t r0 = tile * R;
+    const int nr = (int)min((int64_t)R, rows - r0);
+    // ---- x of the tile ---------------------------------------------------------------------
+    for (int r = 0; r < R; r++)
+      Xs[tid * R + r] = r < nr ? to_f(W[(size_t)(r0 + r) * cols + j * 256 + tid]) : 0.0f;
+    __syncthreads();
+    // ---- step 2: Q_g(c) for every (row, group, choice) -------------------------------------
+    for (int u = warp; u < R * (G / GPW); u += kLhThreads / 32) {
+      const int r = u / (G / GPW);
+      const int g = (u % (G / GPW)) * GPW + lane / GS, a = lane % GS;
+      const int i = g * GS + a;
+      if (r < nr) {
+        const float x = Xs[i * R + r];
+        for (int c = 0; c < NC; c++) {
+          const float dw = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
+          float y = 0.0f;
+#pragma unroll
+          for (int b = 0; b < GS; b++) y = __fmaf_rn(Hgg[(g * GS + b) * GS + a], __shfl_sync(0xffffffffu, dw, b, GS), y);
+          float p = __fmul_rn(dw, y);
+#pragma unroll
+          for (int off = GS / 2; off >= 1; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off, GS));
+          if (a == 0) Qe[(r * G + g) * NC + c] = p;
+        }
+      }
+    }
+    __syncthreads();
+    if (tid < R * G) {
+      const int r = tid / G, g = tid % G;
+      const float *q = Qe + (r * G + g) * NC;
+      float best = q[0];
+      int bc = 0;
+      for (int c = 1; c < NC; c++)
+        if (q[c] < best) { best = q[c]; bc = c; }
+      cur[r * G + g] = bc;
+    }
+    __syncthreads();
+    {  // dw of the current choices
+      const int g = tid / GS;
+      for (int r = 0; r < R; r++)
+        DWt[tid * R + r] = r < nr ? __fsub_rn(Xs[tid * R + r],
+                                              Q[((size_t)cur[r * G + g] * rows + r0 + r) * cols + j * 256 + tid])
+                                  : 0.0f;
+    }
+    __syncthreads();
+    // ---- U = H'_offdiag dw: thread tid owns column tid ---------------------------------------
+    {
+      const int gi = tid / GS;
+      float acc[R];
+#pragma unroll
+      for (int r = 0; r < R; r++) acc[r] = 0.0f;
+      for (int k = 0; k < 256; k++) {
+        if (k / GS == gi) continue;
+        const float h = __ldg(Hj + (size_t)k * 256 + tid);
+        const float4 *d4 = reinterpret_cast<const float4 *>(DWt + k * R);
+#pragma unroll
+        for (int q = 0; q < R / 4; q++) {
+          const float4 d = d4[q];
+          acc[4 * q] = __fmaf_rn(h, d.x, acc[4 * q]);
+          acc[4 * q + 1] = __fmaf_rn(h, d.y, acc[4 * q + 1]);
+          acc[4 * q + 2] = __fmaf_rn(h, d.z, acc[4 * q + 2]);
+          acc[4 * q + 3] = __fmaf_rn(h, d.w, acc[4 * q + 3]);
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < R; r++) U[tid * R + r] = acc[r];
+    }
+    __syncthreads();
+    // ---- step 3: two revisits ------------------------------------------------------------------
+    for (int pass = 0; pass < 2; pass++) {
+      for (int g = 0; g < G; g++) {
+        if (tid == 0) moved = 0;
+        __syncthreads();
+        // (a) every row's best move for group g: a warp per row, GPW choices side by side
+        for (int r = warp; r < R; r += kLhThreads / 32) {
+          const int a = lane % GS, i = g * GS + a;
+          const int cc = r < nr ? cur[r * G + g] : 0;
+          float bestd = 0.0f;
+          int bestc = cc;
+          if (r < nr) {
+            const float x = Xs[i * R + r], dcur = DWt[i * R + r], uu = U[i * R + r];
+            const float qcur = Qe[(r * G + g) * NC + cc];
+            for (int c0 = 0; c0 < NC; c0 += GPW) {
+              const int c = c0 + lane / GS;
+              const float dwc = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
+              float t = __fmul_rn(__fsub_rn(dwc, dcur), uu);
+#pragma unroll
+              for (int off = GS / 2; off >= 1; off >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off, GS));
+              const float dE = __fadd_rn(__fmul_rn(2.0f, t), __fsub_rn(Qe[(r * G + g) * NC + c], qcur));
+              // choices in ascending order: segment 0 holds c0, segment 1 (GPW = 2) c0 + 1
+#pragma unroll
+              for (int s = 0; s < GPW; s++) {
+                const float v = __shfl_sync(0xffffffffu, dE, s * GS);
+                if (v < bestd) { bestd = v; bestc = c0 + s; }
+              }
+            }
+          }
+          // (b) apply the move: new dw_g, its change, the choice
+          if (r < nr && bestc != cc) {
+            if (lane < GS) {
+              const float x = Xs[i * R + r];
+              const float dwn = __fsub_rn(x, Q[((size_t)bestc * rows + r0 + r) * cols + j * 256 + i]);
+              Dl[a * R + r] = __fsub_rn(dwn, DWt[i * R + r]);
+              DWt[i * R + r] = dwn;
+            }
+            if (lane == 0) { cur[r * G + g] = bestc; moved = 1; }
+          } else if (lane < GS) {
+            Dl[a * R + r] = 0.0f;
+          }
+        }
+        __syncthreads();
+        // (c) U of the other groups' columns += H'[., g panel] * change
+        if (moved && tid / GS != g) {
+          for (int k = 0; k < GS; k++) {
+            const float h = __ldg(Hj + (size_t)(g * GS + k) * 256 + tid);
+#pragma unroll
+            for (int r = 0; r < R; r++) U[tid * R + r] = __fmaf_rn(h, Dl[k * R + r], U[tid * R + r]);
+          }
+        }
+        __syncthreads();
+      }
+    }
+    // ---- the tile's choices ------------------------------------------------------------------
+    if (tid < R * G) {
+      const int r = tid / G, g = tid % G;
+      if (r < nr) choices[((size_t)(r0 + r) * nb + j) * G + g] = (uint8_t)cur[r * G + g];
+    }
+    __syncthreads();
+  }
+}
+
+template <int F, typename TIn>
+static int run_lh(const void *W, int64_t rows, int64_t cols, const float *Q, const float *H, float perc_damp,
+                  uint8_t *choices, int32_t *status, cudaStream_t st) {
+  const size_t smem = LhCfg<F>::SMEM;
+  auto kern = lh_search_kernel<F, TIn>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return IQ_ERR_CUDA;
+  const int64_t ntiles = (rows + kLhRows - 1) / kLhRows;
+  const dim3 grid((unsigned)(cols / 256), (unsigned)(ntiles < 65535 ? ntiles : 65535));
+  kern<<<grid, kLhThreads, smem, st>>>((const TIn *)W, rows, cols, Q, H, perc_damp, choices, status);
+  return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+}
+
+}  // namespace iqk
+
+using namespace iqk;
+
+static int lh_num_choices(iq_format f) { return f == IQ1_M ? 8 : 16; }
+
+extern "C" int iq_local_hessian_workspace_size(iq_format f, int64_t rows, int64_t cols, size_t *bytes) {
+  if ((unsigned)f > IQ1_M || rows < 0 || cols <= 0 || cols % 256 || !bytes) return IQ_ERR_ARG;
+  *bytes = (size_t)lh_num_choices(f) * (size_t)rows * (size_t)cols * sizeof(float);
+  return IQ_OK;
+}
+
+extern "C" int iq_local_hessian_choices(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                                        const float *grid, const uint8_t *payloads, const float *hessian,
+                                        float perc_damp, uint8_t *choices, int32_t *status, void *workspace,
+                                        size_t workspace_bytes, void *stream) {
+  if ((unsigned)f > IQ1_M || (dt != IQ_F32 && dt != IQ_BF16) || rows < 0 || cols <= 0 || cols % 256)
+    return IQ_ERR_ARG;
+  if (cols / 256 > 65535) return IQ_ERR_ARG;
+  if (!(perc_damp >= 0.0f) || !std::isfinite(perc_damp)) return IQ_ERR_ARG;
+  const int64_t nb = rows * (cols / 256);
+  if (nb == 0) return IQ_OK;
+  if (!W || !grid || !payloads || !hessian || !choices) return IQ_ERR_ARG;
+  if (((uintptr_t)W & 15) || ((uintptr_t)grid & 15) || ((uintptr_t)hessian & 15)) return IQ_ERR_ARG;
+  size_t need = 0;
+  iq_local_hessian_workspace_size(f, rows, cols, &need);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int NC = lh_num_choices(f);
+  const size_t bb = (size_t)fmt_block_bytes(f);
+  float *Q = (float *)workspace;
+  for (int c = 0; c < NC; c++) {
+    const int rc = iq_decode(f, payloads + (size_t)c * nb * bb, rows, cols, grid, Q + (size_t)c * rows * cols, IQ_F32,
+                             stream);
+    if (rc) return rc;
+  }
+  switch (f) {
+#define LH_CASE(FMT)                                                                                      \
+  case FMT:                                                                                               \
+    return dt == IQ_BF16 ? run_lh<FMT, __nv_bfloat16>(W, rows, cols, Q, hessian, perc_damp, choices, status, st) \
+                         : run_lh<FMT, float>(W, rows, cols, Q, hessian, perc_damp, choices, status, st);
+    LH_CASE(IQ2_XXS)
+    LH_CASE(IQ2_XS)
+    LH_CASE(IQ2_S)
+    LH_CASE(IQ1_S)
+    LH_CASE(IQ1_M)
+#undef LH_CASE
+  }
+  return IQ_ERR_ARG;
+}

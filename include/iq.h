@@ -22,8 +22,9 @@
  *             (PR #2735), "What imatrix does" and its unit-test list.
  *  [coverage] "MoE expert coverage in imatrix calibration", Facts.
  *  [formats]  PR #2513: the IQ2_XXS, IQ2_S and IQ1_M commit texts and the IQ1_M description.
- *  [choices]  PR #3157 "[1/5] Let the GGML IQ encoders take fixed per-group choices", and PR #3159
- *             "one-pass every-choice encode" (same page).
+ *  [choices]  PR #3157 "[1/5] Let the GGML IQ encoders take fixed per-group choices", PR #3159
+ *             "one-pass every-choice encode" and PR #3158 "local_hessian for GGML IQ" (same
+ *             page).
  *  [iq1m-cuda] the IQ1_M CUDA-encoder commit message on the recipes-folder page.
  */
 #ifndef IQ_B300_IQ_H
@@ -146,7 +147,9 @@ IQ_API int iq_anchor_scales(iq_format f, const void *W, iq_dtype dt, int64_t row
  * its best candidate under it (lowest (delta bit, entry) on equal error).  IQ2_XXS/XS first flip
  * the sign of argmin_i w_i x_i^2 when an odd number of x_i are negative (even parity); IQ2_S keeps
  * the input signs.  Decisions equal those of an exact evaluation: candidates the fp32 sweep cannot
- * separate from the best within its proven rounding bound are rescored in fp64.
+ * separate from the best within its rounding bound are rescored in fp64 (the bound is proven for
+ * the rescoring's fp32 FMA chains; for the sweep's tensor-core sums it rests on the measured
+ * accumulation error of the MMAs, about a third of what it allows).
  *   W            device [rows, cols], dtype dt; 16-byte aligned
  *   importance   device fp32, NULL (w = 1), [cols] (rows_per_expert == 0) or [E, cols] with row r
  *                using expert r / rows_per_expert ([coverage]: global row / rows per expert)
@@ -172,6 +175,45 @@ IQ_API int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows
                     float *group_errors, int32_t *status, void *workspace, size_t workspace_bytes,
                     void *stream);
 
+/* Every-choice payloads ([choices] PR #3159, What does this PR do? and Usage): payloads[c] is the
+ * payload of the forced encode with every group at choice c, byte-identical to iq_encode with
+ * choices = c everywhere (each choice is one fixed-choice pass, near ties rescored exactly).
+ *   payloads  device uint8 [num_choices, B, block_bytes] output (any alignment)
+ *   other arguments as in iq_encode (workspace: iq_encode_workspace_size bytes, reused by every
+ *   pass); a zero-scale block is all zero under every choice. */
+IQ_API int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                                  const float *importance, int64_t rows_per_expert, const float *grid,
+                                  const uint16_t *d16, uint8_t *payloads, int32_t *status, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/* ---- local-Hessian choice search ([choices] PR #3158, What does this PR do?) -------------------
+ * Picks every group's choice by the layer-output error dw H' dw^T over the block's 256-column
+ * diagonal block of the input Hessian, given the every-choice payloads:
+ *   H' = H_bb + perc_damp * mean(diag(H_bb)) * I            (damped as GPTQ damps; pages: 0.3)
+ *   dw_c = x - q_c, q_c the decoded block of payloads[c]
+ *   1. each group takes argmin_c dw_g(c)^T H'_gg dw_g(c)      (lowest c on equal values)
+ *   2. two passes over the groups in ascending order: a group moves to the choice that minimises
+ *      the block error with the other groups held, if that is strictly lower than with its current
+ *      choice (lowest c among equal minima).
+ * The payload under the searched choices is iq_encode(..., choices).  The pages use
+ * importance = sqrt(diag(H)) for the every-choice encode.  Arithmetic is fp32; a pick can differ
+ * from an exact evaluation only where two choices' errors are within fp32 rounding of each other.
+ *   W          device [rows, cols] of dtype dt, 16-byte aligned (the weight being encoded)
+ *   grid       device fp32 [grid_entries, 8], 16-byte aligned
+ *   payloads   device uint8 [num_choices, B, block_bytes] (iq_encode_every_choice)
+ *   hessian    device fp32 [cols / 256, 256, 256]: the diagonal blocks of the symmetric input
+ *              Hessian, block j for columns 256 j ... 256 j + 255; 16-byte aligned
+ *   perc_damp  finite, >= 0
+ *   choices    device uint8 [B, choice_groups] output
+ *   status     IQ_STATUS_BAD_INPUT when a block's damping term is not finite
+ *   workspace  device scratch of iq_local_hessian_workspace_size bytes (num_choices * rows * cols
+ *              fp32: every choice's decoded weight), 256-byte aligned */
+IQ_API int iq_local_hessian_workspace_size(iq_format f, int64_t rows, int64_t cols, size_t *bytes);
+IQ_API int iq_local_hessian_choices(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                                    const float *grid, const uint8_t *payloads, const float *hessian,
+                                    float perc_damp, uint8_t *choices, int32_t *status, void *workspace,
+                                    size_t workspace_bytes, void *stream);
+
 /* ---- encoder without caller-provided scratch --------------------------------------------------
  * No counterpart on the pages: this is an addition for callers that cannot allocate device memory
  * (code running under CUDA-graph stream capture in the global mode, where cudaMalloc is refused;
@@ -195,8 +237,8 @@ IQ_API int iq_encode_static_scratch(iq_format f, const void *W, iq_dtype dt, int
 
 /* ---- decoder ([formats]: the value rule above) ------------------------------------------------
  * out[rows, cols] (device; IQ_F32, or IQ_BF16 rounded to nearest even) from payload [B,
- * block_bytes].  fp32 output is exact.  payload must be 4-byte aligned, grid and out 16-byte
- * aligned. */
+ * block_bytes].  fp32 output is exact.  payload may have any alignment inside an allocation whose
+ * start is 4-byte aligned (any cudaMalloc buffer); grid and out must be 16-byte aligned. */
 IQ_API int iq_decode(iq_format f, const uint8_t *payload, int64_t rows, int64_t cols, const float *grid, void *out,
               iq_dtype out_dtype, void *stream);
 
