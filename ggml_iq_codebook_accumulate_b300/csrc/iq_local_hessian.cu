@@ -32,9 +32,10 @@ constexpr int kLhThreads = 256;  // one thread per column of the block
 template <int F> struct LhCfg {
   static constexpr int G = Fmt<F>::G, NC = Fmt<F>::C, GS = 256 / G;
   static constexpr int GPW = 32 / GS;  // groups a warp handles side by side (1 or 2)
-  // Hgg [256][GS], Qe [kLhRows][G][NC], Xs / DWt / U [256][kLhRows], Dl [GS][kLhRows], cur [kLhRows][G]
-  static constexpr size_t SMEM =
-      4 * ((size_t)256 * GS + (size_t)kLhRows * G * NC + 3 * 256 * kLhRows + GS * kLhRows + kLhRows * G) + 64;
+  // Hgg [256][GS], Qe [kLhRows][G][NC], Xs / DWt / U [256][kLhRows], Dl [GS][kLhRows],
+  // Ds [8 warps][32 lanes][NC], cur [kLhRows][G]
+  static constexpr size_t SMEM = 4 * ((size_t)256 * GS + (size_t)kLhRows * G * NC + 3 * 256 * kLhRows +
+                                      GS * kLhRows + 8 * 32 * NC + kLhRows * G) + 64;
 };
 
 __device__ __forceinline__ float to_f(float v) { return v; }
@@ -55,7 +56,8 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
   float *DWt = Xs + 256 * R;            // [256][R] dw of the current choices
   float *U = DWt + 256 * R;             // [256][R] off-diagonal products
   float *Dl = U + 256 * R;              // [GS][R] change of dw_g after a move
-  int *cur = reinterpret_cast<int *>(Dl + GS * R);  // [R][G]
+  float *Ds = Dl + GS * R;              // [8][32][NC] each warp's dw of every choice, for broadcast
+  int *cur = reinterpret_cast<int *>(Ds + 8 * 32 * NC);  // [R][G]
   __shared__ float red[kLhThreads / 32];
   __shared__ int moved;
 
@@ -100,13 +102,36 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
       const int g = (u % (G / GPW)) * GPW + lane / GS, a = lane % GS;
       const int i = g * GS + a;
       if (r < nr) {
+        // every choice side by side: NC independent multiply-add chains over the group
         const float x = Xs[i * R + r];
-        for (int c = 0; c < NC; c++) {
-          const float dw = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
-          float y = 0.0f;
+        float dw[NC], y[NC];
+        float *ds = Ds + warp * 32 * NC;  // lane's row: the NC values of its element
 #pragma unroll
-          for (int b = 0; b < GS; b++) y = __fmaf_rn(Hgg[(g * GS + b) * GS + a], __shfl_sync(0xffffffffu, dw, b, GS), y);
-          float p = __fmul_rn(dw, y);
+        for (int c = 0; c < NC; c++) {
+          dw[c] = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
+          y[c] = 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < NC; c += 4)
+          *reinterpret_cast<float4 *>(ds + lane * NC + c) = make_float4(dw[c], dw[c + 1], dw[c + 2], dw[c + 3]);
+        __syncwarp();
+        const float *seg = ds + (lane / GS) * GS * NC;  // the lane's group's elements
+#pragma unroll 2
+        for (int b = 0; b < GS; b++) {
+          const float h = Hgg[(g * GS + b) * GS + a];
+#pragma unroll
+          for (int c = 0; c < NC; c += 4) {
+            const float4 v = *reinterpret_cast<const float4 *>(seg + b * NC + c);
+            y[c] = __fmaf_rn(h, v.x, y[c]);
+            y[c + 1] = __fmaf_rn(h, v.y, y[c + 1]);
+            y[c + 2] = __fmaf_rn(h, v.z, y[c + 2]);
+            y[c + 3] = __fmaf_rn(h, v.w, y[c + 3]);
+          }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < NC; c++) {
+          float p = __fmul_rn(dw[c], y[c]);
 #pragma unroll
           for (int off = GS / 2; off >= 1; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off, GS));
           if (a == 0) Qe[(r * G + g) * NC + c] = p;
@@ -132,33 +157,40 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
                                   : 0.0f;
     }
     __syncthreads();
-    // ---- U = H'_offdiag dw: thread tid owns column tid ---------------------------------------
+    // ---- U = H'_offdiag dw: thread tid owns column tid (in registers; the visited group's slice is
+    // published to shared memory before each visit) ----------------------------------------------
+    float ureg[R];
     {
       const int gi = tid / GS;
-      float acc[R];
+      float *acc = ureg;
 #pragma unroll
       for (int r = 0; r < R; r++) acc[r] = 0.0f;
-      for (int k = 0; k < 256; k++) {
-        if (k / GS == gi) continue;
-        const float h = __ldg(Hj + (size_t)k * 256 + tid);
-        const float4 *d4 = reinterpret_cast<const float4 *>(DWt + k * R);
+      for (int kg = 0; kg < G; kg++) {
+        if (kg == gi) continue;
+#pragma unroll 4
+        for (int kk = 0; kk < GS; kk++) {
+          const int k = kg * GS + kk;
+          const float h = __ldg(Hj + (size_t)k * 256 + tid);
+          const float4 *d4 = reinterpret_cast<const float4 *>(DWt + k * R);
 #pragma unroll
-        for (int q = 0; q < R / 4; q++) {
-          const float4 d = d4[q];
-          acc[4 * q] = __fmaf_rn(h, d.x, acc[4 * q]);
-          acc[4 * q + 1] = __fmaf_rn(h, d.y, acc[4 * q + 1]);
-          acc[4 * q + 2] = __fmaf_rn(h, d.z, acc[4 * q + 2]);
-          acc[4 * q + 3] = __fmaf_rn(h, d.w, acc[4 * q + 3]);
+          for (int q = 0; q < R / 4; q++) {
+            const float4 d = d4[q];
+            acc[4 * q] = __fmaf_rn(h, d.x, acc[4 * q]);
+            acc[4 * q + 1] = __fmaf_rn(h, d.y, acc[4 * q + 1]);
+            acc[4 * q + 2] = __fmaf_rn(h, d.z, acc[4 * q + 2]);
+            acc[4 * q + 3] = __fmaf_rn(h, d.w, acc[4 * q + 3]);
+          }
         }
       }
-#pragma unroll
-      for (int r = 0; r < R; r++) U[tid * R + r] = acc[r];
     }
-    __syncthreads();
     // ---- step 3: two revisits ------------------------------------------------------------------
     for (int pass = 0; pass < 2; pass++) {
       for (int g = 0; g < G; g++) {
         if (tid == 0) moved = 0;
+        if (tid / GS == g) {
+#pragma unroll
+          for (int r = 0; r < R; r++) U[tid * R + r] = ureg[r];
+        }
         __syncthreads();
         // (a) every row's best move for group g: a warp per row, GPW choices side by side
         for (int r = warp; r < R; r += kLhThreads / 32) {
@@ -169,18 +201,28 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
           if (r < nr) {
             const float x = Xs[i * R + r], dcur = DWt[i * R + r], uu = U[i * R + r];
             const float qcur = Qe[(r * G + g) * NC + cc];
-            for (int c0 = 0; c0 < NC; c0 += GPW) {
-              const int c = c0 + lane / GS;
-              const float dwc = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
-              float t = __fmul_rn(__fsub_rn(dwc, dcur), uu);
+            constexpr int NS = NC / GPW;  // steps; step s holds choices s * GPW + (lane / GS)
+            float t[NS];
 #pragma unroll
-              for (int off = GS / 2; off >= 1; off >>= 1) t = __fadd_rn(t, __shfl_xor_sync(0xffffffffu, t, off, GS));
-              const float dE = __fadd_rn(__fmul_rn(2.0f, t), __fsub_rn(Qe[(r * G + g) * NC + c], qcur));
-              // choices in ascending order: segment 0 holds c0, segment 1 (GPW = 2) c0 + 1
+            for (int st = 0; st < NS; st++) {
+              const int c = st * GPW + lane / GS;
+              const float dwc = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
+              t[st] = __fmul_rn(__fsub_rn(dwc, dcur), uu);
+            }
+#pragma unroll
+            for (int off = GS / 2; off >= 1; off >>= 1)
+#pragma unroll
+              for (int st = 0; st < NS; st++) t[st] = __fadd_rn(t[st], __shfl_xor_sync(0xffffffffu, t[st], off, GS));
+            // choices in ascending order: segment 0 holds the step's first choice, segment 1 (GPW = 2)
+            // the next one
+#pragma unroll
+            for (int st = 0; st < NS; st++) {
+              const int c = st * GPW + lane / GS;
+              const float dE = __fadd_rn(__fmul_rn(2.0f, t[st]), __fsub_rn(Qe[(r * G + g) * NC + c], qcur));
 #pragma unroll
               for (int s = 0; s < GPW; s++) {
                 const float v = __shfl_sync(0xffffffffu, dE, s * GS);
-                if (v < bestd) { bestd = v; bestc = c0 + s; }
+                if (v < bestd) { bestd = v; bestc = st * GPW + s; }
               }
             }
           }
@@ -200,10 +242,18 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
         __syncthreads();
         // (c) U of the other groups' columns += H'[., g panel] * change
         if (moved && tid / GS != g) {
+#pragma unroll 4
           for (int k = 0; k < GS; k++) {
             const float h = __ldg(Hj + (size_t)(g * GS + k) * 256 + tid);
+            const float4 *d4 = reinterpret_cast<const float4 *>(Dl + k * R);
 #pragma unroll
-            for (int r = 0; r < R; r++) U[tid * R + r] = __fmaf_rn(h, Dl[k * R + r], U[tid * R + r]);
+            for (int q = 0; q < R / 4; q++) {
+              const float4 d = d4[q];
+              ureg[4 * q] = __fmaf_rn(h, d.x, ureg[4 * q]);
+              ureg[4 * q + 1] = __fmaf_rn(h, d.y, ureg[4 * q + 1]);
+              ureg[4 * q + 2] = __fmaf_rn(h, d.z, ureg[4 * q + 2]);
+              ureg[4 * q + 3] = __fmaf_rn(h, d.w, ureg[4 * q + 3]);
+            }
           }
         }
         __syncthreads();
