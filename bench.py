@@ -472,7 +472,7 @@ def measure_local_hessian(args, dev, flush):
     out = {"workload": f"{LH_R}x{LH_C} bf16 weight, H from 4096 correlated activations, perc_damp 0.3"}
     for f in LH_PAGES_MS:
         g = torch.from_numpy(synth.grid(f)).to(dev)
-        ws = api.encode_workspace(f, LH_R, LH_C, dev)
+        ws = api.encode_workspace(f, LH_R * api.format_info(f)["num_choices"], LH_C, dev)
         lws = api.local_hessian_workspace(f, LH_R, LH_C, dev)
         pay = api.encode_every_choice(f, W, g, importance=w, workspace=ws)
         ch = api.local_hessian_choices(f, W, g, pay, H, 0.3, workspace=lws)

@@ -208,7 +208,7 @@ def encode_every_choice(fmt, W, grid, importance=None, rows_per_expert=0, d16=No
     if payloads is None:
         payloads = torch.empty(info["num_choices"], B, info["block_bytes"], dtype=torch.uint8, device=dev)
     if workspace is None:
-        workspace = encode_workspace(fmt, R, C, dev)
+        workspace = encode_workspace(fmt, R * info["num_choices"], C, dev)
     _check(lib().iq_encode_every_choice(FMT_ID[fmt], _p(W), _dt(W), R, C, _p(importance), int(rows_per_expert),
                                         _p(grid), _p(d16), _p(payloads), _p(status), _p(workspace),
                                         workspace.numel(), _stream(dev)), "iq_encode_every_choice")

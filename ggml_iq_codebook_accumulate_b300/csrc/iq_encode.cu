@@ -32,7 +32,8 @@
 
 namespace iqk {
 
-enum { MODE_SEARCH = 0, MODE_FIXED = 1, MODE_TABLE = 2 };
+// searched (+ every-choice table), fixed choices, every-choice table only, every-choice payloads
+enum { MODE_SEARCH = 0, MODE_FIXED = 1, MODE_TABLE = 2, MODE_EVERY = 3 };
 
 __host__ __device__ inline size_t al256(size_t n) { return (n + 255) & ~(size_t)255; }
 
@@ -366,6 +367,9 @@ template <int F> struct TcCfg {
   static constexpr int NCH = Fmt<F>::N / kChunk;        // chunks per sweep
   static constexpr int ALLOC = 2 * NQ * kChunk <= 256 ? 256 : 512;  // tensor-memory columns
   static constexpr size_t SMEM = (size_t)Fmt<F>::N * 64 + 4 * 4096 + 2 * 128 * 16 * 4 + 2 * 128 * 4 * 4 + 4 * 24 * 4;
+  // every-choice payloads: per (warp half, vector, choice) the minimum, the near bound (fp32) and
+  // key | count << 16
+  static constexpr size_t EVERY = 2 * 128 * 16 * 4 * 3;
 };
 
 template <int F, int MODE, typename TIn>
@@ -379,6 +383,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   float *xchg = aop + 4 * 1024;                             // [2][128][16] per-choice minima
   float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
   uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
+  float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][128][16] (every mode)
+  uint32_t *evk = reinterpret_cast<uint32_t *>(evm + 2 * 128 * 16); // [2][128][16] (every mode)
+  float *evt = reinterpret_cast<float *>(evk + 2 * 128 * 16);       // [2][128][16] (every mode)
   __shared__ uint64_t cb_bar, full_bar[2], empty_bar[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
@@ -442,8 +449,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         Cgrp = group_sum<VPG>(v.Cs, g0);
       } else if (sub == 0 && b < a.nblocks) {
         // a rejected or zero-scale block: all-zero payload; every choice decodes to zeros
-        if (MODE != MODE_TABLE)
+        if (MODE == MODE_EVERY) {
+          for (int c = 0; c < C; c++)
+            for (int i = lane; i < BB; i += 32) a.payload[((size_t)c * a.nblocks + b) * BB + i] = 0;
+        } else if (MODE != MODE_TABLE) {
           for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = 0;
+        }
         if (a.table && MODE != MODE_FIXED) {
           float cs = 0.0f;
           if (has) {
@@ -535,13 +546,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
     int c1 = 0;
     bool gflag = false;
     float smin = 0.0f;  // searched mode: this vector's minimum score under c1 (from sweep 1)
+    uint64_t alp[NS];
+#pragma unroll
+    for (int s = 0; s < NS; s++) { const float al = alpha_of<F>(d, s); alp[s] = pk2(al, al); }
     if (MODE != MODE_FIXED) {
       float m[C];
 #pragma unroll
       for (int c = 0; c < C; c++) m[c] = INFINITY;
-      uint64_t alp[NS];
-#pragma unroll
-      for (int s = 0; s < NS; s++) { const float al = alpha_of<F>(d, s); alp[s] = pk2(al, al); }
       for (int ch = 0; ch < NCH; ch++) {
         run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
 #pragma unroll
@@ -578,7 +589,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       named_bar(2, kTcConsumers * 32);
 #pragma unroll
       for (int c = 0; c < C; c++) m[c] = fminf(xchg[row * 16 + c], xchg[(128 + row) * 16 + c]);
-      if (active) {
+      if constexpr (MODE == MODE_EVERY) {
+        // every choice's minimum and the bound above it that holds every candidate whose error
+        // could be within the near-tie margin of the minimum (as in the searched second sweep)
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+          const float al = alpha_choice<F>(d, c);
+          const float e1 = __fmul_rn(al, m[c]);
+          const float De = 1.01f * kMargin * fmaxf(4.0f * v.Cs + 2.0f * e1, 0.0f);
+          evt[(sub * 128 + row) * 16 + c] =
+              active ? m[c] + 1.01f * (De / al) + 9.5367431640625e-07f * fabsf(m[c]) : -INFINITY;
+          evm[(sub * 128 + row) * 16 + c] = m[c];
+          evk[(sub * 128 + row) * 16 + c] = 0xffffu;  // no key yet, no near candidate
+        }
+      } else if (active) {
         float D1 = INFINITY, D2 = INFINITY;
 #pragma unroll
         for (int c = 0; c < C; c++) {
@@ -594,7 +618,138 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       c1 = fixed_choice<G>(a, b, cg);
     }
 
-    if (MODE != MODE_TABLE) {
+    if constexpr (MODE == MODE_EVERY) {
+      // ---- sweep 2 (every choice): each vector's best candidate under every choice ---------
+      // A part of the sweep (16 entries of the warp) goes through the exact bookkeeping for a
+      // choice only when the part's minimum under that choice is at most T[c]: the key of the
+      // minimum (the lowest entry whose score equals it exactly; the same MMAs and rounded packed
+      // FMAs reproduce sweep 1's values) and the number of candidates at most T[c] (two or more
+      // mean a near tie, which the exact rescoring re-decides under that choice).
+      const float *mrow = evm + (sub * 128 + row) * 16;
+      const float *trow = evt + (sub * 128 + row) * 16;
+      uint32_t *krow = evk + (sub * 128 + row) * 16;
+      for (int ch = 0; ch < NCH; ch++) {
+        const int eb = ch * kChunk + ebase0;
+        run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
+          float mn[C];
+#pragma unroll
+          for (int c = 0; c < C; c++) mn[c] = INFINITY;
+#pragma unroll
+          for (int i = 0; i < 8; i++) {
+            const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
+            if (!Fmt<F>::IQ1) {
+#pragma unroll
+              for (int c = 0; c < C; c++) {
+                const float2 sc = up2(ffma2(alp[c], B2, A2));
+                mn[c] = min3f(mn[c], sc.x, sc.y);
+              }
+            } else {
+              const uint64_t C2 = pk2(Cq[2 * i], Cq[2 * i + 1]);
+              const uint64_t Anp = ffma2(kc.p125, nT2p, A2), Anm = ffma2(kc.m125, nT2p, A2);
+              const uint64_t Bw = ffma2(kc.w64, Wsp, B2);
+              const uint64_t Bp = ffma2(kc.p025, C2, Bw), Bm = ffma2(kc.m025, C2, Bw);
+#pragma unroll
+              for (int s = 0; s < 8; s++) {
+                const float2 sp = up2(ffma2(alp[s], Bp, Anp)), sm = up2(ffma2(alp[s], Bm, Anm));
+                if (F == IQ1_S) {
+                  mn[s] = min3f(mn[s], sp.x, sp.y);
+                  mn[8 + s] = min3f(mn[8 + s], sm.x, sm.y);
+                } else {
+                  mn[s] = min3f(min3f(mn[s], sp.x, sp.y), sm.x, sm.y);
+                }
+              }
+            }
+          }
+          uint32_t hits = 0;  // choices whose minimum over this part is within the near bound
+#pragma unroll
+          for (int c = 0; c < C; c += 4) {
+            const float4 t4 = *reinterpret_cast<const float4 *>(trow + c);
+            hits |= (mn[c] <= t4.x ? 1u : 0u) << c | (mn[c + 1] <= t4.y ? 2u : 0u) << c |
+                    (mn[c + 2] <= t4.z ? 4u : 0u) << c | (mn[c + 3] <= t4.w ? 8u : 0u) << c;
+          }
+          while (hits) {
+            const int c = __ffs(hits) - 1;
+            hits &= hits - 1u;
+            const float Tc = trow[c], mc = mrow[c];
+            uint32_t key = krow[c] & 0xffffu, cnt = krow[c] >> 16;
+            const int sc = F == IQ1_S ? (c & 7) : c;
+            const int db = F == IQ1_S ? (c >> 3) : 0;
+            const float alf = alpha_of<F>(d, sc);  // as alp[sc]
+            const uint64_t al2 = pk2(alf, alf);
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+              const int e0 = eb + 16 * h + 2 * i;
+              const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
+              float2 q0, q1 = make_float2(INFINITY, INFINITY);
+              if (!Fmt<F>::IQ1) {
+                q0 = up2(ffma2(al2, B2, A2));
+              } else {
+                const uint64_t C2 = pk2(Cq[2 * i], Cq[2 * i + 1]);
+                const uint64_t Bw = ffma2(kc.w64, Wsp, B2);
+                if (F == IQ1_S) {
+                  const uint64_t Ad = ffma2(db ? kc.m125 : kc.p125, nT2p, A2);
+                  const uint64_t Bd = ffma2(db ? kc.m025 : kc.p025, C2, Bw);
+                  q0 = up2(ffma2(al2, Bd, Ad));
+                } else {
+                  const uint64_t Anp = ffma2(kc.p125, nT2p, A2), Anm = ffma2(kc.m125, nT2p, A2);
+                  const uint64_t Bp = ffma2(kc.p025, C2, Bw), Bm = ffma2(kc.m025, C2, Bw);
+                  q0 = up2(ffma2(al2, Bp, Anp));
+                  q1 = up2(ffma2(al2, Bm, Anm));
+                }
+              }
+              const float vv[4] = {q0.x, q0.y, q1.x, q1.y};
+              const uint32_t kk[4] = {(uint32_t)e0, (uint32_t)e0 + 1u, (uint32_t)(N + e0), (uint32_t)(N + e0) + 1u};
+#pragma unroll
+              for (int t = 0; t < (F == IQ1_M ? 4 : 2); t++) {
+                if (vv[t] <= Tc) {
+                  cnt++;
+                  if (vv[t] == mc && kk[t] < key) key = kk[t];
+                }
+              }
+            }
+            krow[c] = key | (min(cnt, 3u) << 16);
+          }
+        });
+      }
+      named_bar(2, kTcConsumers * 32);  // both warps' keys and counts are in shared memory
+      if (sub == 0 && active) {
+        uint32_t *pb = packbuf + quarter * 24;
+        for (int c = 0; c < C; c++) {
+          const uint32_t w0 = evk[row * 16 + c], w1 = evk[(128 + row) * 16 + c];
+          const uint32_t key = min(w0 & 0xffffu, w1 & 0xffffu);
+          const uint32_t cnt = (w0 >> 16) + (w1 >> 16);
+          // near ties under choice c: one item (block | c << 27, vectors) for the exact rescoring
+          const uint32_t vflags = __ballot_sync(0xffffffffu, cnt >= 2 || key == 0xffffu);
+          if (vflags && lane == 0) {
+            const int slot = atomicAdd(&ws.hdr[1], 1);
+            ws.fb[slot] = make_uint2((uint32_t)b | ((uint32_t)c << 27), vflags);
+          }
+          if (lane < 24) pb[lane] = 0u;
+          __syncwarp();
+          const int k = key == 0xffffu ? 0 : (int)key;
+          const int idx = F == IQ1_M ? (k % N) : k;
+          const Bits lo = f_idx_lo<F>(lane);
+          put_bits(pb, lo, (uint32_t)idx);
+          if (F == IQ2_S || Fmt<F>::IQ1) put_bits(pb, f_idx_hi<F>(lane), (uint32_t)idx >> lo.width);
+          if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)v.sgn);
+          if (F == IQ1_M) {
+            put_bits(pb, f_dbit_vec<F>(lane), (uint32_t)(k / N));
+            if (lane < 4) put_bits(pb, f_d16_nib<F>(lane), (d16 >> (4 * lane)) & 15u);
+          } else if (lane == 0) {
+            put_bits(pb, f_d16<F>(), d16);
+          }
+          if (lane == g0) {
+            put_bits(pb, f_scale<F>(cg), (uint32_t)(F == IQ1_S ? (c & 7) : c));
+            if (F == IQ1_S) put_bits(pb, f_dbit_grp<F>(cg), (uint32_t)(c >> 3));
+          }
+          __syncwarp();
+          const uint8_t *pbytes = reinterpret_cast<const uint8_t *>(pb);
+          uint8_t *dst = a.payload + ((size_t)c * a.nblocks + b) * BB;
+          for (int i = lane; i < BB; i += 32) dst[i] = pbytes[i];
+          __syncwarp();
+        }
+      }
+    } else if (MODE != MODE_TABLE) {
       // ---- sweep 2: best candidate and runner-up under choice c1 ---------------------------
       // Fixed choices: every candidate goes through the best / runner-up tracking.  Searched
       // mode: sweep 1 already gave the minimum s1 (the same MMAs and the same rounded packed
@@ -795,14 +950,20 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
   RescoreSmem &sm = sm_all[wid];
   const int nflag = ws.hdr[1];
   const float4 *tab = ws.tab;
+  // an item is (block, flagged vectors); every-choice payloads: (block | choice << 27, flagged
+  // vectors), re-decided as a fixed-choice block in that choice's payload
+  constexpr bool kFixedLike = MODE == MODE_FIXED || MODE == MODE_EVERY;
   for (int it = blockIdx.x * 8 + wid; it < nflag; it += gridDim.x * 8) {
-    const uint2 item = ws.fb[it];
-    const int64_t b = item.x;
+   const uint2 item = ws.fb[it];
+   {
+    const int cpass = MODE == MODE_EVERY ? (int)(item.x >> 27) : 0;
+    const int64_t b = MODE == MODE_EVERY ? (int64_t)(item.x & ((1u << 27) - 1u)) : (int64_t)item.x;
     const uint32_t mask = item.y;
+    uint8_t *payb = a.payload + (MODE == MODE_EVERY ? (size_t)cpass * a.nblocks * BB : 0) + b * BB;
     Vec v;
     load_block_vec<TIn>(a, b, lane, v);
     uint8_t *pbytes = reinterpret_cast<uint8_t *>(sm.pay);
-    for (int i = lane; i < BB; i += 32) pbytes[i] = a.payload[b * BB + i];
+    for (int i = lane; i < BB; i += 32) pbytes[i] = payb[i];
     uint32_t d16;
     if (F == IQ1_M) {
       d16 = 0;
@@ -818,7 +979,7 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
       if (!(mask & gm)) continue;
       float Cg = 0.0f;
       // (a) fp32 per-vector minima for every choice (or the fixed one), as the sweep computes them
-      int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : -1;
+      int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : MODE == MODE_EVERY ? cpass : -1;
       for (int k = 0; k < VPG; k++) {
         const Vec u = shfl_vec(v, g * VPG + k);
         Cg = k == 0 ? u.Cs : __fadd_rn(Cg, u.Cs);
@@ -830,7 +991,7 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
           load_entry<F>(tab, e, en);
 #pragma unroll
           for (int c = 0; c < C; c++) {
-            if (MODE == MODE_FIXED && c != cfix) continue;
+            if (kFixedLike && c != cfix) continue;
             int s, db0, db1;
             cand_of_choice<F>(c, s, db0, db1);
             const float al = alpha_of<F>(d, s);
@@ -853,7 +1014,7 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
       float D[C];
       float D1 = INFINITY;
       for (int c = 0; c < C; c++) {
-        if (MODE == MODE_FIXED && c != cfix) { D[c] = INFINITY; continue; }
+        if (kFixedLike && c != cfix) { D[c] = INFINITY; continue; }
         float S = sm.mh[0][c];
         for (int k = 1; k < VPG; k++) S = __fadd_rn(S, sm.mh[k][c]);
         D[c] = __fmul_rn(alpha_choice<F>(d, c), S);
@@ -922,8 +1083,9 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
       }
       __syncwarp();
     }
-    for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = pbytes[i];
+    for (int i = lane; i < BB; i += 32) payb[i] = pbytes[i];
     __syncwarp();
+   }
   }
 }
 
@@ -971,7 +1133,7 @@ static int run_encode(const EncArgs &a, void *workspace, size_t ws_bytes, cudaSt
   EncWs ws = enc_ws(workspace, N);
   if (cudaMemsetAsync(ws.hdr, 0, 256, st) != cudaSuccess) return IQ_ERR_CUDA;
   prep_codebook<F><<<(N + 255) / 256, 256, 0, st>>>(a.grid, ws);
-  const size_t smem = TcCfg<F>::SMEM;
+  const size_t smem = TcCfg<F>::SMEM + (MODE == MODE_EVERY ? TcCfg<F>::EVERY : 0);
   auto kern = encode_tc_kernel<F, MODE, TIn>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
@@ -1091,8 +1253,9 @@ extern "C" int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t 
 }
 
 // Every-choice payloads (PR #3159): payload c is the forced encode with every group at choice c,
-// one fixed-choice pass per choice (each pass's near ties are rescored exactly, so every payload is
-// byte-identical to the forced encode).
+// from one pass: sweep 1 gives every choice's minimum per vector, sweep 2 the entry that attains it
+// under every choice, and near ties are rescored exactly per (block, choice), so every payload is
+// byte-identical to the forced encode.
 extern "C" int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
                                       const float *importance, int64_t rows_per_expert, const float *grid,
                                       const uint16_t *d16, uint8_t *payloads, int32_t *status, void *workspace,
@@ -1101,20 +1264,16 @@ extern "C" int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, i
   if (rc) return rc;
   const int64_t nb = rows * (cols / 256);
   if (nb > 0 && !payloads) return IQ_ERR_ARG;
-  size_t need = 0;
-  iq_encode_workspace_size(f, rows, cols, &need);
-  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
+  if (nb >= ((int64_t)1 << 27)) return IQ_ERR_TOO_LARGE;  // flag items carry the block in 27 bits
   iq_format_info_t info;
   iq_format_info(f, &info);
+  size_t need = 0;
+  iq_encode_workspace_size(f, rows * info.num_choices, cols, &need);  // a flag list entry per (block, choice)
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
-  for (int c = 0; c < info.num_choices; c++) {
-    EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr,
-              payloads + (size_t)c * nb * info.block_bytes, nullptr, status, c};
-    rc = dt == IQ_BF16 ? dispatch_encode<MODE_FIXED, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
-                       : dispatch_encode<MODE_FIXED, float>(f, a, workspace, workspace_bytes, st);
-    if (rc) return rc;
-  }
-  return IQ_OK;
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, payloads, nullptr, status, 0};
+  return dt == IQ_BF16 ? dispatch_encode<MODE_EVERY, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
+                       : dispatch_encode<MODE_EVERY, float>(f, a, workspace, workspace_bytes, st);
 }
 
 extern "C" int iq_format_info(iq_format f, iq_format_info_t *out) {

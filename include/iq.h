@@ -177,10 +177,13 @@ IQ_API int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows
 
 /* Every-choice payloads ([choices] PR #3159, What does this PR do? and Usage): payloads[c] is the
  * payload of the forced encode with every group at choice c, byte-identical to iq_encode with
- * choices = c everywhere (each choice is one fixed-choice pass, near ties rescored exactly).
- *   payloads  device uint8 [num_choices, B, block_bytes] output (any alignment)
- *   other arguments as in iq_encode (workspace: iq_encode_workspace_size bytes, reused by every
- *   pass); a zero-scale block is all zero under every choice. */
+ * choices = c everywhere.
+ * One pass: the first sweep gives every (vector, choice) minimum, the second the entry attaining
+ * it under every choice, and near ties are rescored exactly per (block, choice).
+ *   payloads   device uint8 [num_choices, B, block_bytes] output (any alignment)
+ *   workspace  device scratch of iq_encode_workspace_size(f, rows * num_choices, cols) bytes
+ *   other arguments as in iq_encode; a zero-scale block is all zero under every choice.
+ * IQ_ERR_TOO_LARGE for B >= 2^27 blocks. */
 IQ_API int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
                                   const float *importance, int64_t rows_per_expert, const float *grid,
                                   const uint16_t *d16, uint8_t *payloads, int32_t *status, void *workspace,
