@@ -20,7 +20,8 @@ IQ_F32, IQ_BF16 = 0, 1
 EXPORTS = ("iq_format_info", "iq_imatrix_workspace_size", "iq_imatrix_accumulate", "iq_imatrix_weights",
            "iq_anchor_scales", "iq_encode_workspace_size", "iq_encode", "iq_group_errors", "iq_decode",
            "iq_encode_static_scratch_capacity", "iq_encode_static_scratch",
-           "iq_encode_every_choice", "iq_local_hessian_workspace_size", "iq_local_hessian_choices")
+           "iq_encode_every_choice", "iq_local_hessian_workspace_size", "iq_local_hessian_choices",
+           "iq_imatrix_merge", "iq_imatrix_neutral_entries", "iq_imatrix_coverage", "iq_encode_write_back")
 
 STATUS_BITS = {
     "BAD_CHOICE": 1, "BAD_EXPERT_ID": 2, "NONFINITE_SUM2": 4, "DUP_EXPERT_ID": 8, "BAD_INPUT": 16,
@@ -62,6 +63,10 @@ def lib():
         L.iq_encode_every_choice.argtypes = [i32, p, i32, i64, i64, p, i64, p, p, p, p, p, sz, p]
         L.iq_local_hessian_workspace_size.argtypes = [i32, i64, i64, ctypes.POINTER(sz)]
         L.iq_local_hessian_choices.argtypes = [i32, p, i32, i64, i64, p, p, p, ctypes.c_float, p, p, p, sz, p]
+        L.iq_imatrix_merge.argtypes = [p, p, p, p, i32, i64, p, p]
+        L.iq_imatrix_neutral_entries.argtypes = [p, p, i32, i64, p]
+        L.iq_imatrix_coverage.argtypes = [p, i32, p, p]
+        L.iq_encode_write_back.argtypes = [i32, p, i32, i64, i64, p, i64, p, p, p, p, p, p, sz, p]
         for n in EXPORTS:
             getattr(L, n).restype = ctypes.c_int
         _lib = L
@@ -240,6 +245,50 @@ def local_hessian_choices(fmt, W, grid, payloads, hessian_blocks, perc_damp=0.3,
                                           _p(hessian_blocks), float(perc_damp), _p(choices), _p(status),
                                           _p(workspace), workspace.numel(), _stream(dev)), "iq_local_hessian_choices")
     return choices
+
+
+def imatrix_merge(in_sum2, counts, src_in_sum2, src_counts, status=None):
+    """in_sum2 += src_in_sum2 and counts += src_counts, in place."""
+    for t, n in ((in_sum2, "in_sum2"), (counts, "counts"), (src_in_sum2, "src_in_sum2"), (src_counts, "src_counts")):
+        _cuda(t, n)
+    E, C = in_sum2.shape
+    _check(lib().iq_imatrix_merge(_p(in_sum2), _p(counts), _p(src_in_sum2), _p(src_counts), E, C, _p(status),
+                                  _stream(in_sum2.device)), "iq_imatrix_merge")
+    return in_sum2, counts
+
+
+def imatrix_neutral_entries(in_sum2, counts):
+    """Zero-count experts get in_sum2 = 1 and count 1, in place."""
+    E, C = in_sum2.shape
+    _check(lib().iq_imatrix_neutral_entries(_p(in_sum2), _p(counts), E, C, _stream(in_sum2.device)),
+           "iq_imatrix_neutral_entries")
+    return in_sum2, counts
+
+
+def imatrix_coverage(counts):
+    """Device int64 [4]: experts with tokens, total tokens, least and largest count."""
+    out = torch.empty(4, dtype=torch.int64, device=counts.device)
+    _check(lib().iq_imatrix_coverage(_p(counts), counts.numel(), _p(out), _stream(counts.device)), "iq_imatrix_coverage")
+    return out
+
+
+def encode_write_back(fmt, W, grid, importance=None, rows_per_expert=0, d16=None, choices=None, status=None,
+                      payload=None, workspace=None):
+    """Encodes W and overwrites it with the decoded payload (its own dtype).  Returns the payload."""
+    for t, n in ((W, "W"), (grid, "grid"), (importance, "importance"), (d16, "d16"), (choices, "choices")):
+        _cuda(t, n)
+    info = format_info(fmt)
+    R, C = W.shape
+    B = R * (C // 256)
+    dev = W.device
+    if payload is None:
+        payload = torch.empty(B, info["block_bytes"], dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = encode_workspace(fmt, R, C, dev)
+    _check(lib().iq_encode_write_back(FMT_ID[fmt], _p(W), _dt(W), R, C, _p(importance), int(rows_per_expert),
+                                      _p(grid), _p(d16), _p(choices), _p(payload), _p(status), _p(workspace),
+                                      workspace.numel(), _stream(dev)), "iq_encode_write_back")
+    return payload
 
 
 def decode(fmt, payload, rows, cols, grid, dtype=torch.float32, out=None):

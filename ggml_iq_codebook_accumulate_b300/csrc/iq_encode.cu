@@ -1234,6 +1234,19 @@ extern "C" int iq_encode(iq_format f, const void *W, iq_dtype dt, int64_t rows, 
                        : dispatch_encode<MODE_SEARCH, float>(f, a, workspace, workspace_bytes, st);
 }
 
+// Encode and write the decoded weight back ("Add imatrix calibration for the GGML formats ...",
+// What imatrix does: the encoder encodes each weight with its statistic, writes the decoded weight
+// back and pins the payload): iq_encode, then the decoder from the payload into W in W's dtype.
+extern "C" int iq_encode_write_back(iq_format f, void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                                    const float *importance, int64_t rows_per_expert, const float *grid,
+                                    const uint16_t *d16, const uint8_t *choices, uint8_t *payload, int32_t *status,
+                                    void *workspace, size_t workspace_bytes, void *stream) {
+  const int rc = iq_encode(f, W, dt, rows, cols, importance, rows_per_expert, grid, d16, choices, payload, nullptr,
+                           status, workspace, workspace_bytes, stream);
+  if (rc) return rc;
+  return iq_decode(f, payload, rows, cols, grid, W, dt, stream);
+}
+
 extern "C" int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
                                const float *importance, int64_t rows_per_expert, const float *grid, const uint16_t *d16,
                                float *group_errors, int32_t *status, void *workspace, size_t workspace_bytes,

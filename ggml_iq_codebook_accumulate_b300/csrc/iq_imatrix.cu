@@ -30,6 +30,7 @@
 // No atomics touch in_sum2, so the sums are the sequential definition above.
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <mutex>
 
 #include "iq_common.cuh"
@@ -557,5 +558,107 @@ extern "C" int iq_imatrix_weights(const float *in_sum2, const int64_t *counts, i
   const int64_t blocks = (n + 255) / 256;
   iqk::imatrix_weights_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, (cudaStream_t)stream>>>(
       in_sum2, counts, num_experts, cols, floor, w);
+  return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Merging, neutral entries and coverage ("MoE expert coverage in imatrix calibration", Facts: the
+// GGUF imatrix format stores in_sum2 and counts per tensor so that files can be merged; the legacy
+// writer stores a zero-count expert as value 1 with count 1, a neutral entry, matching the weight
+// 1 the reader gives it; saving logs the share of experts with data ("partial data (xx.xx%)") and
+// "no data" when no expert has any).
+namespace iqk {
+// in_sum2 += src (one rounding per value); counts += src counts
+__global__ void imatrix_merge_kernel(float *__restrict__ s2, int64_t *__restrict__ counts,
+                                     const float *__restrict__ src, const int64_t *__restrict__ src_counts, int E,
+                                     int64_t cols, int32_t *__restrict__ status) {
+  const int64_t n = (int64_t)E * cols;
+  int bad = 0;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float v = __fadd_rn(s2[i], src[i]);
+    s2[i] = v;
+    bad |= !isfinite(v);
+    if (i < E) counts[i] += src_counts[i];
+  }
+  if (status && __any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(status, IQ_STATUS_NONFINITE_SUM2);
+}
+
+// zero-count experts: every channel's sum becomes 1 (the count is set by a second launch, after
+// every channel has read it)
+__global__ void imatrix_neutral_sums_kernel(float *__restrict__ s2, const int64_t *__restrict__ counts, int E,
+                                            int64_t cols) {
+  const int64_t n = (int64_t)E * cols;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    if (counts[i / cols] == 0) s2[i] = 1.0f;
+}
+__global__ void imatrix_neutral_counts_kernel(int64_t *__restrict__ counts, int E) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x)
+    if (counts[e] == 0) counts[e] = 1;
+}
+
+// out[0] experts with at least one token, out[1] tokens over all experts, out[2] least and out[3]
+// largest count (one CTA)
+__global__ void __launch_bounds__(1024) imatrix_coverage_kernel(const int64_t *__restrict__ counts, int E,
+                                                                int64_t *__restrict__ out) {
+  __shared__ long long r_touched[32], r_total[32], r_min[32], r_max[32];
+  long long touched = 0, total = 0, mn = LLONG_MAX, mx = LLONG_MIN;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const long long c = counts[e];
+    touched += c > 0;
+    total += c;
+    mn = c < mn ? c : mn;
+    mx = c > mx ? c : mx;
+  }
+  for (int off = 16; off >= 1; off >>= 1) {
+    touched += __shfl_xor_sync(0xffffffffu, touched, off);
+    total += __shfl_xor_sync(0xffffffffu, total, off);
+    const long long om = __shfl_xor_sync(0xffffffffu, mn, off), ox = __shfl_xor_sync(0xffffffffu, mx, off);
+    mn = om < mn ? om : mn;
+    mx = ox > mx ? ox : mx;
+  }
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) { r_touched[w] = touched; r_total[w] = total; r_min[w] = mn; r_max[w] = mx; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int k = 1; k < (int)(blockDim.x >> 5); k++) {
+      touched += r_touched[k];
+      total += r_total[k];
+      mn = r_min[k] < mn ? r_min[k] : mn;
+      mx = r_max[k] > mx ? r_max[k] : mx;
+    }
+    out[0] = touched;
+    out[1] = total;
+    out[2] = mn;
+    out[3] = mx;
+  }
+}
+}  // namespace iqk
+
+extern "C" int iq_imatrix_merge(float *in_sum2, int64_t *counts, const float *src_in_sum2, const int64_t *src_counts,
+                                int num_experts, int64_t cols, int32_t *status, void *stream) {
+  if (num_experts <= 0 || cols <= 0 || !in_sum2 || !counts || !src_in_sum2 || !src_counts) return IQ_ERR_ARG;
+  if (src_in_sum2 == in_sum2 || src_counts == counts) return IQ_ERR_ARG;
+  const int64_t n = (int64_t)num_experts * cols;
+  const int64_t blocks = (n + 255) / 256;
+  iqk::imatrix_merge_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, (cudaStream_t)stream>>>(
+      in_sum2, counts, src_in_sum2, src_counts, num_experts, cols, status);
+  return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+}
+
+extern "C" int iq_imatrix_neutral_entries(float *in_sum2, int64_t *counts, int num_experts, int64_t cols,
+                                          void *stream) {
+  if (num_experts <= 0 || cols <= 0 || !in_sum2 || !counts) return IQ_ERR_ARG;
+  const int64_t n = (int64_t)num_experts * cols;
+  const int64_t blocks = (n + 255) / 256;
+  cudaStream_t st = (cudaStream_t)stream;
+  iqk::imatrix_neutral_sums_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(in_sum2, counts,
+                                                                                          num_experts, cols);
+  iqk::imatrix_neutral_counts_kernel<<<(num_experts + 255) / 256, 256, 0, st>>>(counts, num_experts);
+  return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
+}
+
+extern "C" int iq_imatrix_coverage(const int64_t *counts, int num_experts, int64_t *out, void *stream) {
+  if (num_experts <= 0 || !counts || !out) return IQ_ERR_ARG;
+  iqk::imatrix_coverage_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(counts, num_experts, out);
   return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
 }

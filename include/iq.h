@@ -130,6 +130,21 @@ IQ_API int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens, int
 IQ_API int iq_imatrix_weights(const float *in_sum2, const int64_t *counts, int num_experts, int64_t cols,
                        float floor, float *w, void *stream);
 
+/* ---- merging, neutral entries, coverage ([coverage] Facts) --------------------------------------
+ * iq_imatrix_merge: in_sum2 += src_in_sum2 (fp32, one rounding per value) and counts += src_counts,
+ *   the merge of two statistics of the same tensor (GGUF imatrix files keep in_sum2 and counts so
+ *   that they can be merged).  Sums that become non-finite set IQ_STATUS_NONFINITE_SUM2.  Sources
+ *   must not alias the destinations.  All device pointers, [num_experts, cols] and [num_experts].
+ * iq_imatrix_neutral_entries: every expert whose count is 0 gets in_sum2 = 1 on every channel and
+ *   count 1, the legacy writer's neutral entry (its weight stays 1).
+ * iq_imatrix_coverage: out (device int64 [4]) = experts with at least one token, tokens over all
+ *   experts, least count, largest count; out[0] / num_experts is the "partial data" share of the
+ *   saving log, out[0] == 0 its "no data". */
+IQ_API int iq_imatrix_merge(float *in_sum2, int64_t *counts, const float *src_in_sum2, const int64_t *src_counts,
+                            int num_experts, int64_t cols, int32_t *status, void *stream);
+IQ_API int iq_imatrix_neutral_entries(float *in_sum2, int64_t *counts, int num_experts, int64_t cols, void *stream);
+IQ_API int iq_imatrix_coverage(const int64_t *counts, int num_experts, int64_t *out, void *stream);
+
 /* ---- super-block scale anchor ([formats]: "single-pass grid search at a fixed anchored
  * super-block scale"; IQ1_S flat 0.61; IQ1_M clamp(0.58 + 0.035 * peak_to_rms, 0.65, 0.95)) -----
  * d16[b] = fp16 (round to nearest even, saturated at 65504) of (ratio * amax) / K, amax = max |x|
@@ -168,6 +183,15 @@ IQ_API int iq_encode(iq_format f, const void *W, iq_dtype dt, int64_t rows, int6
               int64_t rows_per_expert, const float *grid, const uint16_t *d16, const uint8_t *choices,
               uint8_t *payload, float *group_errors, int32_t *status, void *workspace,
               size_t workspace_bytes, void *stream);
+
+/* Encode and write back ([imatrix] What imatrix does: the encoder encodes each weight with its
+ * statistic, writes the decoded weight back and pins the payload): iq_encode (no table), then W is
+ * overwritten in place with the decoded payload in its own dtype (bf16: rounded to nearest even;
+ * fp32: exact).  Blocks the encoder rejected decode to zeros.  Arguments as in iq_encode. */
+IQ_API int iq_encode_write_back(iq_format f, void *W, iq_dtype dt, int64_t rows, int64_t cols,
+                                const float *importance, int64_t rows_per_expert, const float *grid,
+                                const uint16_t *d16, const uint8_t *choices, uint8_t *payload, int32_t *status,
+                                void *workspace, size_t workspace_bytes, void *stream);
 
 /* Every-choice error table only (same sweep, no payload): group_errors as in iq_encode. */
 IQ_API int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,

@@ -90,3 +90,17 @@ def test_local_hessian_host_checks():
     assert call(ws=fake + 16) == -3                  # workspace not 256-byte aligned
     assert L.iq_encode_every_choice(0, fake, api.IQ_BF16, 4, 500, None, 0, fake, None, fake, None, fake, 1 << 30,
                                     None) == -1      # cols % 256
+
+
+def test_imatrix_tools_and_write_back_host_checks():
+    """Refused on the host: bad sizes, missing or aliasing pointers (never dereferenced)."""
+    from ggml_iq_codebook_accumulate_b300 import api
+    L = api.lib()
+    a, b = 1 << 20, 1 << 21
+    assert L.iq_imatrix_merge(a, a + 64, b, b + 64, 0, 256, None, None) == -1          # no experts
+    assert L.iq_imatrix_merge(a, a + 64, a, b + 64, 4, 256, None, None) == -1          # source aliases destination
+    assert L.iq_imatrix_merge(None, a + 64, b, b + 64, 4, 256, None, None) == -1
+    assert L.iq_imatrix_neutral_entries(a, a + 64, 4, 0, None) == -1                   # no columns
+    assert L.iq_imatrix_coverage(a, 0, b, None) == -1 and L.iq_imatrix_coverage(None, 4, b, None) == -1
+    assert L.iq_encode_write_back(0, a, api.IQ_BF16, 4, 500, None, 0, b, None, None, a, None, b, 1 << 30,
+                                  None) == -1                                          # cols % 256
