@@ -366,11 +366,27 @@ template <int F> struct TcCfg {
   static constexpr int NQ = Fmt<F>::IQ1 ? 3 : 2;       // An, (Cg), B columns per entry
   static constexpr int NCH = Fmt<F>::N / kChunk;        // chunks per sweep
   static constexpr int ALLOC = 2 * NQ * kChunk <= 256 ? 256 : 512;  // tensor-memory columns
-  static constexpr size_t SMEM = (size_t)Fmt<F>::N * 64 + 4 * 4096 + 2 * 128 * 16 * 4 + 2 * 128 * 4 * 4 + 4 * 24 * 4;
+  // shared memory besides the per-vector operands (tc_na below, 4 KB each)
+  static constexpr size_t SMEM = (size_t)Fmt<F>::N * 64 + 2 * 128 * 16 * 4 + 2 * 128 * 4 * 4 + 4 * 24 * 4;
   // every-choice payloads: per (warp half, vector, choice) the minimum, the near bound (fp32) and
   // key | count << 16
   static constexpr size_t EVERY = 2 * 128 * 16 * 4 * 3;
 };
+
+// Per-vector [128 x 8] tf32 operands: nw2 hi, nw2 lo, w hi, w lo; and for the IQ1_M second sweep of
+// the searched and fixed modes, w/4 hi, w/4 lo, -w/4 hi, -w/4 lo (the shifted sums' MMAs, below).
+template <int F, int MODE> __host__ __device__ constexpr int tc_na() {
+  return F == IQ1_M && (MODE == MODE_SEARCH || MODE == MODE_FIXED) ? 8 : 4;
+}
+// Second-sweep layout of IQ1_M in those modes: the shifted sums are split into the entry-dependent
+// part, Bp' = w . h + (w/4) . g = B + Cg/4 and Bm' = B - Cg/4 from the tensor cores, and a part
+// the same for every entry, K(alpha, delta) = alpha Ws/64 + delta nT2, added to a vector's best
+// and runner-up only (fl(x + K) is monotone in x).  The first sweep keeps An, Cg, B.  (IQ1_S, whose
+// shift is one per group, gains nothing from it: its per-lane choice of column costs what the
+// packed shift FMAs cost.)
+template <int F, int MODE> __host__ __device__ constexpr bool tc_deferred(int sweep) {
+  return F == IQ1_M && (MODE == MODE_FIXED || (MODE == MODE_SEARCH && sweep == 1));
+}
 
 template <int F, int MODE, typename TIn>
 __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, EncWs ws, int64_t nquads) {
@@ -379,8 +395,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   constexpr uint32_t IDESC = umma_idesc<kChunk>();
   extern __shared__ __align__(1024) uint8_t smem[];
   float *cb = reinterpret_cast<float *>(smem);              // codebook g [N x 8], then h [N x 8]
-  float *aop = cb + (size_t)N * 16;                         // [4][128 x 8]: nw2 hi, nw2 lo, w hi, w lo
-  float *xchg = aop + 4 * 1024;                             // [2][128][16] per-choice minima
+  constexpr int NA = tc_na<F, MODE>();
+  float *aop = cb + (size_t)N * 16;                         // [NA][128 x 8] per-vector operands
+  float *xchg = aop + NA * 1024;                            // [2][128][16] per-choice minima
   float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
   uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
   float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][128][16] (every mode)
@@ -474,8 +491,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           const float nh = tf32_rna(nw), wh = tf32_rna(ww);
           aop[0 * 1024 + kmaj(row, k)] = nh;
           aop[1 * 1024 + kmaj(row, k)] = tf32_rna(__fsub_rn(nw, nh));
+          const float wl = tf32_rna(__fsub_rn(ww, wh));
           aop[2 * 1024 + kmaj(row, k)] = wh;
-          aop[3 * 1024 + kmaj(row, k)] = tf32_rna(__fsub_rn(ww, wh));
+          aop[3 * 1024 + kmaj(row, k)] = wl;
+          if (NA == 8) {  // exact power-of-two scalings of the tf32 parts
+            aop[4 * 1024 + kmaj(row, k)] = 0.25f * wh;
+            aop[5 * 1024 + kmaj(row, k)] = 0.25f * wl;
+            aop[6 * 1024 + kmaj(row, k)] = -0.25f * wh;
+            aop[7 * 1024 + kmaj(row, k)] = -0.25f * wl;
+          }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       }
@@ -500,12 +524,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
             const uint64_t bg = umma_desc(sg + ch * kChunk * 32), bh = umma_desc(sh + ch * kChunk * 32);
             umma_tf32(d, umma_desc(sa + 0 * 4096), bg, IDESC, 0);          // An = nw2 . g
             umma_tf32(d, umma_desc(sa + 1 * 4096), bg, IDESC, 1);
-            if (NQ == 3) {
-              umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bg, IDESC, 0);  // Cg = w . g
-              umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bg, IDESC, 1);
+            if (tc_deferred<F, MODE>(sw)) {
+              umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);      // Bp' = w . h
+              umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+              umma_tf32(d + kChunk, umma_desc(sa + 4 * 4096), bg, IDESC, 1);      //      + (w/4) . g
+              umma_tf32(d + kChunk, umma_desc(sa + 5 * 4096), bg, IDESC, 1);
+              umma_tf32(d + 2 * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // Bm' = w . h
+              umma_tf32(d + 2 * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+              umma_tf32(d + 2 * kChunk, umma_desc(sa + 6 * 4096), bg, IDESC, 1);  //      - (w/4) . g
+              umma_tf32(d + 2 * kChunk, umma_desc(sa + 7 * 4096), bg, IDESC, 1);
+            } else {
+              if (NQ == 3) {
+                umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bg, IDESC, 0);  // Cg = w . g
+                umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bg, IDESC, 1);
+              }
+              umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // B = w . h
+              umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
             }
-            umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // B = w . h
-            umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
             umma_commit(&full_bar[buf]);
           }
           if (!okl) break;
@@ -519,6 +554,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
     const float d = half_bits_to_float((uint16_t)d16);
     const IQ1Const kc = iq1_consts();
     const uint64_t nT2p = pk2(v.nT2, v.nT2), Wsp = pk2(v.Ws, v.Ws);
+    const float w64 = 0.015625f * v.Ws, t8 = 0.125f * v.nT2;  // exact power-of-two scalings
     const int ebase0 = 32 * sub;  // this warp's first entry in each chunk
     // waits for chunk `cc`, hands the warp's 2 x 16 columns to fn(half, An, Cg, B), releases it
     // (after a timeout the remaining chunks are skipped without waiting)
@@ -761,19 +797,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       const uint64_t al = pk2(alpha, alpha);
       const int dbit = F == IQ1_S ? (c1 >> 3) : 0;
       const uint64_t dA = dbit ? kc.m125 : kc.p125, dB = dbit ? kc.m025 : kc.p025;
+      // IQ1_M (deferred second-sweep layout): raw scores alpha Bd' + An per shift; the shift's K
+      // is added to the tracked best and runner-up at the end
+      float Kp = 0.0f, Km = 0.0f;
+      if (F == IQ1_M && active) { Kp = __fmaf_rn(alpha, w64, t8); Km = __fmaf_rn(alpha, w64, -t8); }
       // (With 256 or 512 entries nearly every part holds some lane's best, so the small codebooks
       // track everything.)
       constexpr bool kFind = MODE == MODE_SEARCH && N >= 1024;
       float T = INFINITY;
       if (kFind && active) {
         // flag iff e2 - e1 <= kMargin (4 Cs + e1 + e2), i.e. e2 - e1 <= kMargin (4 Cs + 2 e1) /
-        // (1 - kMargin); the factors 1.01 and the relative term cover fp32 rounding here
+        // (1 - kMargin); the factors 1.01 and the relative term cover fp32 rounding here.  IQ1_M's
+        // second sweep evaluates the shifted scores in another order of rounding than the first
+        // (each within the rounding bound of the margin), so its bound is twice as wide.
+        constexpr float kW = F == IQ1_M ? 2.02f : 1.01f;
+        constexpr float kR = F == IQ1_M ? 1.9073486328125e-06f : 9.5367431640625e-07f;
         const float e1 = __fmul_rn(alpha, smin);
         const float De = 1.01f * kMargin * fmaxf(4.0f * v.Cs + 2.0f * e1, 0.0f);
-        T = smin + 1.01f * (De / alpha) + 9.5367431640625e-07f * fabsf(smin);
+        T = smin + kW * (De / alpha) + kR * fabsf(smin);
       }
-      float best = INFINITY, second = INFINITY;
-      int key = 0;
+      float best = INFINITY, second = INFINITY, bestm = INFINITY, secondm = INFINITY;
+      int key = 0, keym = 0;
       constexpr int PPH = F == IQ1_M ? 16 : 8;  // candidate pairs per half chunk
       for (int ch = 0; ch < NCH; ch++) {
         const int eb = ch * kChunk + ebase0;
@@ -784,35 +828,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
             const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
             if (!Fmt<F>::IQ1) {
               sc[i] = ffma2(al, B2, A2);
-            } else {
+            } else if (F == IQ1_S) {
               const uint64_t C2 = pk2(Cq[2 * i], Cq[2 * i + 1]);
               const uint64_t Bw = ffma2(kc.w64, Wsp, B2);
-              if (F == IQ1_S) {
-                const uint64_t Ad = ffma2(dA, nT2p, A2), Bd = ffma2(dB, C2, Bw);
-                sc[i] = ffma2(al, Bd, Ad);
-              } else {
-                const uint64_t Anp = ffma2(kc.p125, nT2p, A2), Anm = ffma2(kc.m125, nT2p, A2);
-                const uint64_t Bp = ffma2(kc.p025, C2, Bw), Bm = ffma2(kc.m025, C2, Bw);
-                sc[i] = ffma2(al, Bp, Anp);
-                sc[8 + i] = ffma2(al, Bm, Anm);
-              }
+              const uint64_t Ad = ffma2(dA, nT2p, A2), Bd = ffma2(dB, C2, Bw);
+              sc[i] = ffma2(al, Bd, Ad);
+            } else {
+              // deferred layout: the second column holds Bp', the third Bm'
+              const uint64_t P2 = pk2(Cq[2 * i], Cq[2 * i + 1]);
+              sc[i] = ffma2(al, P2, A2);
+              sc[8 + i] = ffma2(al, B2, A2);
             }
           }
           if (kFind) {
-            float mn = INFINITY;
+            float mn = INFINITY, mnm = INFINITY;
 #pragma unroll
-            for (int p = 0; p < PPH; p++) {
+            for (int p = 0; p < 8; p++) {
               const float2 q = up2(sc[p]);
               mn = min3f(mn, q.x, q.y);
+              if (F == IQ1_M) { const float2 r = up2(sc[8 + p]); mnm = min3f(mnm, r.x, r.y); }
             }
-            if (!(mn <= T)) return;
+            const bool hit = F == IQ1_M ? (__fadd_rn(mn, Kp) <= T || __fadd_rn(mnm, Km) <= T) : mn <= T;
+            if (!hit) return;
           }
 #pragma unroll
-          for (int p = 0; p < PPH; p++) {
-            const int e0 = eb + 16 * h + 2 * (p & 7);
-            track2(up2(sc[p]), p < 8 ? e0 : N + e0, best, second, key);
+          for (int p = 0; p < 8; p++) {
+            const int e0 = eb + 16 * h + 2 * p;
+            track2(up2(sc[p]), e0, best, second, key);
+            if (F == IQ1_M) track2(up2(sc[8 + p]), N + e0, bestm, secondm, keym);
           }
         });
+      }
+      if (F == IQ1_M) {  // back to full scores (INFINITY stays INFINITY)
+        best = __fadd_rn(best, Kp);
+        second = __fadd_rn(second, Kp);
+        const float bm = __fadd_rn(bestm, Km), sm2 = __fadd_rn(secondm, Km);
+        const bool takem = bm < best;  // equal scores keep the plus shift (its keys are lower)
+        second = min3f(second, sm2, takem ? best : bm);
+        if (takem) { best = bm; key = keym; }
       }
       xchg2[sub * 128 + row] = make_float4(best, second, __int_as_float(key), 0.0f);
       named_bar(2, kTcConsumers * 32);
@@ -1133,7 +1186,7 @@ static int run_encode(const EncArgs &a, void *workspace, size_t ws_bytes, cudaSt
   EncWs ws = enc_ws(workspace, N);
   if (cudaMemsetAsync(ws.hdr, 0, 256, st) != cudaSuccess) return IQ_ERR_CUDA;
   prep_codebook<F><<<(N + 255) / 256, 256, 0, st>>>(a.grid, ws);
-  const size_t smem = TcCfg<F>::SMEM + (MODE == MODE_EVERY ? TcCfg<F>::EVERY : 0);
+  const size_t smem = TcCfg<F>::SMEM + (size_t)tc_na<F, MODE>() * 4096 + (MODE == MODE_EVERY ? TcCfg<F>::EVERY : 0);
   auto kern = encode_tc_kernel<F, MODE, TIn>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
