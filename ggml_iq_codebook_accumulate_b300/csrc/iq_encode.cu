@@ -1036,20 +1036,32 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
       for (int k = 0; k < VPG; k++) {
         const Vec u = shfl_vec(v, g * VPG + k);
         Cg = k == 0 ? u.Cs : __fadd_rn(Cg, u.Cs);
-        float lm[C];
+        float lm[C], alc[C];
 #pragma unroll
-        for (int c = 0; c < C; c++) lm[c] = INFINITY;
+        for (int c = 0; c < C; c++) {
+          lm[c] = INFINITY;
+          int s, db0, db1;
+          cand_of_choice<F>(c, s, db0, db1);
+          alc[c] = alpha_of<F>(d, s);
+        }
         for (int e = lane; e < N; e += 32) {
           Entry en;
           load_entry<F>(tab, e, en);
+          // the entry's sums once, then every choice's score as cand_score forms it
+          float An = 0.0f, Bs = 0.0f, Anp = 0.0f, Bp = 0.0f, Anm = 0.0f, Bm = 0.0f;
+          if (!Fmt<F>::IQ1) ab2(u.nw2, u.w, en, An, Bs);
+          else ab1(u, en, Anp, Bp, Anm, Bm);
 #pragma unroll
           for (int c = 0; c < C; c++) {
             if (kFixedLike && c != cfix) continue;
             int s, db0, db1;
             cand_of_choice<F>(c, s, db0, db1);
-            const float al = alpha_of<F>(d, s);
-            lm[c] = fminf(lm[c], cand_score<F>(u, en, al, db0));
-            if (db1 != db0) lm[c] = fminf(lm[c], cand_score<F>(u, en, al, db1));
+            if (!Fmt<F>::IQ1) {
+              lm[c] = fminf(lm[c], __fmaf_rn(alc[c], Bs, An));
+            } else {
+              lm[c] = fminf(lm[c], db0 ? __fmaf_rn(alc[c], Bm, Anm) : __fmaf_rn(alc[c], Bp, Anp));
+              if (db1 != db0) lm[c] = fminf(lm[c], db1 ? __fmaf_rn(alc[c], Bm, Anm) : __fmaf_rn(alc[c], Bp, Anp));
+            }
           }
         }
 #pragma unroll

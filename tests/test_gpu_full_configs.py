@@ -1,5 +1,6 @@
 """GPU parity at the full sizes of the workloads the library is measured on, in the launch
-configuration the benchmark uses, checked on sampled outputs the oracle computes one by one.
+configuration the benchmark uses, checked on sampled outputs the oracle computes one by one (the
+small 256 x 1024 case in full).
 
 * MoE expert encode: 128 experts x a fused gate/up weight [1536, 2048] bf16 (Student-t nu=4 x 0.02)
   in IQ2_XXS and IQ1_M, each expert weighted by its own imatrix (4096 routed tokens, top-8 from a
@@ -7,6 +8,8 @@ configuration the benchmark uses, checked on sampled outputs the oracle computes
 * Large layers: [17408, 5120] and [5120, 17408] bf16 in all five formats, searched with the
   every-choice error table.
 * The imatrix at its largest supported shape: 1024 experts, top-64, 4096-row chunks.
+* The small case: a 256 x 1024 fp32 weight ~ N(0, 0.02) in IQ2_XXS, importance from 512 x 1024
+  fp32 activations, every block against the oracle.
 """
 import numpy as np
 import pytest
@@ -107,3 +110,26 @@ def test_imatrix_largest_supported_shape():
     assert np.array_equal(cn.cpu().numpy(), ref_c)
     assert np.array_equal(s2.cpu().numpy().view(np.uint32), ref_s.view(np.uint32))
     assert int(st.item()) == ref_st == 0
+
+
+def test_small_case_256x1024_whole_payload():
+    """IQ2_XXS of a 256 x 1024 fp32 weight ~ N(0, 0.02) (seed 0); importance sqrt(in_sum2 / count)
+    per column from 512 x 1024 fp32 activations (N(0, 1) x log-normal column scales, one expert
+    every token reaches), through the GPU imatrix; the whole payload and its decode against the
+    oracle."""
+    R, C, T = 256, 1024, 512
+    W = synth.weight_normal(R, C, seed=0)
+    xs, xv = synth.as_dtype(synth.activations(T, C, seed=0), "f32")
+    ids = np.zeros((T, 1), np.int32)
+    s2, cn = api.imatrix_accumulate(torch.from_numpy(xs).to(DEV), torch.from_numpy(ids).to(DEV), 1)
+    w = api.imatrix_weights(s2, cn)
+    ref_s, ref_c, _ = oracle.imatrix_accumulate(xv, ids, 1)
+    ref_w = oracle.imatrix_weights(ref_s, ref_c)
+    assert np.array_equal(w.cpu().numpy().view(np.uint32), ref_w.view(np.uint32))
+    grid = synth.grid("IQ2_XXS")
+    g = torch.from_numpy(grid).to(DEV)
+    p = api.encode("IQ2_XXS", torch.from_numpy(W).to(DEV), g, importance=w[0])
+    p_orc, _, det = oracle.encode("IQ2_XXS", W, grid, importance=ref_w[0], details=True)
+    check_payload("IQ2_XXS", W, grid, p.cpu().numpy(), p_orc, det, importance=ref_w[0])
+    q = api.decode("IQ2_XXS", p, R, C, g)
+    assert np.array_equal(q.cpu().numpy(), oracle.decode("IQ2_XXS", p.cpu().numpy(), R, C, grid))
