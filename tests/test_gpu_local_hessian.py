@@ -164,3 +164,31 @@ def test_local_hessian_full_size_sampled_rows():
         p_orc, _, det = oracle.encode(fmt, wv[rows], grid, importance=imp, choices=ch, details=True)
         check_payload(fmt, wv[rows], grid, pay_dev[c], p_orc, det, importance=imp)
     assert check_choices(fmt, wv[rows], grid, pay_dev, Hb, 0.3, got[sel]) <= 3
+
+
+@pytest.mark.parametrize("fmt", ["IQ1_S", "IQ2_XS"])
+def test_every_choice_payloads_full_size_sampled_rows(fmt):
+    """The one-pass every-choice payloads of the 5632 x 2048 weight (importance from the 4096-row
+    imatrix recipe) against the oracle's forced encodes on 16 rows spread over the weight, for
+    every choice."""
+    R, C = 5632, 2048
+    store, wv = synth.as_dtype(synth.weight_t4(R, C, seed=25), "bf16")
+    xs, xv = synth.as_dtype(synth.activations(4096, C, seed=25), "bf16")
+    x = torch.from_numpy(np.ascontiguousarray(xs).view(np.int16)).view(torch.bfloat16).to(DEV)
+    s2, cn = api.imatrix_accumulate(x, torch.zeros(4096, 1, dtype=torch.int32, device=DEV), 1)
+    w = api.imatrix_weights(s2, cn)[0]
+    grid = synth.grid(fmt)
+    g = torch.from_numpy(grid).to(DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    pay = api.encode_every_choice(fmt, dev_bf16(store), g, importance=w, status=st)
+    assert int(st.item()) == 0
+    rows = np.linspace(0, R - 1, 16).astype(np.int64)
+    nb = C // 256
+    sel = (rows[:, None] * nb + np.arange(nb)[None, :]).ravel()
+    pay_dev = pay.cpu().numpy()[:, sel]
+    wh = w.cpu().numpy()
+    info = oracle.format_info(fmt)
+    for c in range(info["num_choices"]):
+        ch = np.full((len(sel), info["groups"]), c, np.uint8)
+        p_orc, _, det = oracle.encode(fmt, wv[rows], grid, importance=wh, choices=ch, details=True)
+        check_payload(fmt, wv[rows], grid, pay_dev[c], p_orc, det, importance=wh)
