@@ -336,6 +336,14 @@ __device__ __forceinline__ void umma_commit(uint64_t *mbar) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// merges a second tracker (b2, s2, k2) into (best, second, key): the lower score wins, the lower
+// key on equal scores
+__device__ __forceinline__ void merge_track(float &best, float &second, int &key, float b2, float s2, int k2) {
+  const bool take = b2 < best || (b2 == best && k2 < key);
+  second = min3f(second, s2, fmaxf(best, b2));
+  if (take) { best = b2; key = k2; }
+}
+
 // 16 consecutive fp32 columns of the warp's 32 tensor-memory lanes (thread t: lane base + t)
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   uint32_t r[16];
@@ -373,19 +381,23 @@ template <int F> struct TcCfg {
   static constexpr size_t EVERY = 2 * 128 * 16 * 4 * 3;
 };
 
-// Per-vector [128 x 8] tf32 operands: nw2 hi, nw2 lo, w hi, w lo; and for the IQ1_M second sweep of
-// the searched and fixed modes, w/4 hi, w/4 lo, -w/4 hi, -w/4 lo (the shifted sums' MMAs, below).
+// Per-vector [128 x 8] tf32 operands: nw2 hi, nw2 lo, w hi, w lo; for the IQ1_M second sweep of
+// the searched and fixed modes, w/4 hi, w/4 lo, -w/4 hi, -w/4 lo; for IQ1_S with fixed choices,
+// sigma w/4 hi, sigma w/4 lo with sigma = +-1 the sign of the group's given shift (the shifted
+// sums' MMAs, below).
 template <int F, int MODE> __host__ __device__ constexpr int tc_na() {
-  return F == IQ1_M && (MODE == MODE_SEARCH || MODE == MODE_FIXED) ? 8 : 4;
+  return F == IQ1_M && (MODE == MODE_SEARCH || MODE == MODE_FIXED) ? 8 : (F == IQ1_S && MODE == MODE_FIXED ? 6 : 4);
 }
-// Second-sweep layout of IQ1_M in those modes: the shifted sums are split into the entry-dependent
-// part, Bp' = w . h + (w/4) . g = B + Cg/4 and Bm' = B - Cg/4 from the tensor cores, and a part
-// the same for every entry, K(alpha, delta) = alpha Ws/64 + delta nT2, added to a vector's best
-// and runner-up only (fl(x + K) is monotone in x).  The first sweep keeps An, Cg, B.  (IQ1_S, whose
-// shift is one per group, gains nothing from it: its per-lane choice of column costs what the
-// packed shift FMAs cost.)
+// Deferred-shift layout of the second sweep: the shifted sums are split into the entry-dependent
+// part from the tensor cores, Bp' = w . h + (w/4) . g = B + Cg/4 and Bm' = B - Cg/4 (IQ1_M, whose
+// shift is searched per vector), or Bd' = B + sigma Cg/4 (IQ1_S with fixed choices, whose shift
+// is known per group before the sweep), and a part the same for every entry of a vector,
+// K(alpha, delta) = alpha Ws/64 + delta nT2, added to its best and runner-up only (fl(x + K) is
+// monotone in x).  The first sweep keeps An, Cg, B.  (Searched IQ1_S learns its shift only from
+// the first sweep.)
 template <int F, int MODE> __host__ __device__ constexpr bool tc_deferred(int sweep) {
-  return F == IQ1_M && (MODE == MODE_FIXED || (MODE == MODE_SEARCH && sweep == 1));
+  return (F == IQ1_M && (MODE == MODE_FIXED || (MODE == MODE_SEARCH && sweep == 1))) ||
+         (F == IQ1_S && MODE == MODE_FIXED);
 }
 
 template <int F, int MODE, typename TIn>
@@ -485,6 +497,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         }
       }
       if (sub == 0) {
+        // IQ1_S with fixed choices: the sign of the group's shift (choice c = scale + 8 * shift bit)
+        const float sig = NA == 6 && active && (fixed_choice<G>(a, b, cg) >> 3) ? -0.25f : 0.25f;
 #pragma unroll
         for (int k = 0; k < 8; k++) {
           const float nw = active ? v.nw2[k] : 0.0f, ww = active ? v.w[k] : 0.0f;
@@ -499,6 +513,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
             aop[5 * 1024 + kmaj(row, k)] = 0.25f * wl;
             aop[6 * 1024 + kmaj(row, k)] = -0.25f * wh;
             aop[7 * 1024 + kmaj(row, k)] = -0.25f * wl;
+          } else if (NA == 6) {
+            aop[4 * 1024 + kmaj(row, k)] = sig * wh;
+            aop[5 * 1024 + kmaj(row, k)] = sig * wl;
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -524,7 +541,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
             const uint64_t bg = umma_desc(sg + ch * kChunk * 32), bh = umma_desc(sh + ch * kChunk * 32);
             umma_tf32(d, umma_desc(sa + 0 * 4096), bg, IDESC, 0);          // An = nw2 . g
             umma_tf32(d, umma_desc(sa + 1 * 4096), bg, IDESC, 1);
-            if (tc_deferred<F, MODE>(sw)) {
+            if (tc_deferred<F, MODE>(sw) && F == IQ1_S) {
+              umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);      // Bd' = w . h
+              umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+              umma_tf32(d + kChunk, umma_desc(sa + 4 * 4096), bg, IDESC, 1);      //      + (sigma w/4) . g
+              umma_tf32(d + kChunk, umma_desc(sa + 5 * 4096), bg, IDESC, 1);
+            } else if (tc_deferred<F, MODE>(sw)) {
               umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);      // Bp' = w . h
               umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
               umma_tf32(d + kChunk, umma_desc(sa + 4 * 4096), bg, IDESC, 1);      //      + (w/4) . g
@@ -556,6 +578,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
     const uint64_t nT2p = pk2(v.nT2, v.nT2), Wsp = pk2(v.Ws, v.Ws);
     const float w64 = 0.015625f * v.Ws, t8 = 0.125f * v.nT2;  // exact power-of-two scalings
     const int ebase0 = 32 * sub;  // this warp's first entry in each chunk
+    constexpr bool kDefS = F == IQ1_S && MODE == MODE_FIXED;  // deferred layout [An | Bd' | -]
     // waits for chunk `cc`, hands the warp's 2 x 16 columns to fn(half, An, Cg, B), releases it
     // (after a timeout the remaining chunks are skipped without waiting)
     auto run_chunk = [&](auto &&fn) {
@@ -569,7 +592,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         float An[16], Bq[16], Cq[16];
         tmem_ld16(taddr + col + 16 * h, An);
         if (NQ == 3) tmem_ld16(taddr + col + kChunk + 16 * h, Cq);
-        tmem_ld16(taddr + col + (NQ - 1) * kChunk + 16 * h, Bq);
+        if (!kDefS) tmem_ld16(taddr + col + (NQ - 1) * kChunk + 16 * h, Bq);  // (IQ1_S fixed: unused)
         tmem_wait_ld();
         if (active && okl) fn(h, An, Cq, Bq);
       }
@@ -797,10 +820,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       const uint64_t al = pk2(alpha, alpha);
       const int dbit = F == IQ1_S ? (c1 >> 3) : 0;
       const uint64_t dA = dbit ? kc.m125 : kc.p125, dB = dbit ? kc.m025 : kc.p025;
-      // IQ1_M (deferred second-sweep layout): raw scores alpha Bd' + An per shift; the shift's K
-      // is added to the tracked best and runner-up at the end
+      // Deferred layouts (IQ1_M; IQ1_S with fixed choices): raw scores alpha Bd' + An per shift;
+      // the shift's K is added to the tracked best and runner-up at the end
       float Kp = 0.0f, Km = 0.0f;
       if (F == IQ1_M && active) { Kp = __fmaf_rn(alpha, w64, t8); Km = __fmaf_rn(alpha, w64, -t8); }
+      if (kDefS && active) Kp = __fmaf_rn(alpha, w64, dbit ? -t8 : t8);
       // (With 256 or 512 entries nearly every part holds some lane's best, so the small codebooks
       // track everything.)
       constexpr bool kFind = MODE == MODE_SEARCH && N >= 1024;
@@ -816,8 +840,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         const float De = 1.01f * kMargin * fmaxf(4.0f * v.Cs + 2.0f * e1, 0.0f);
         T = smin + kW * (De / alpha) + kR * fabsf(smin);
       }
+      // Two trackers per shift, over the even and the odd pairs of each half chunk (two shorter
+      // dependency chains), merged below: the lower score, on equal scores the lower key (each
+      // tracker keeps the first of its equal scores, and its keys only grow).
       float best = INFINITY, second = INFINITY, bestm = INFINITY, secondm = INFINITY;
-      int key = 0, keym = 0;
+      float best1 = INFINITY, second1 = INFINITY, bestm1 = INFINITY, secondm1 = INFINITY;
+      int key = 0, keym = 0, key1 = 0, keym1 = 0;
       constexpr int PPH = F == IQ1_M ? 16 : 8;  // candidate pairs per half chunk
       for (int ch = 0; ch < NCH; ch++) {
         const int eb = ch * kChunk + ebase0;
@@ -825,7 +853,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           uint64_t sc[PPH];  // pair p: entries e0, e0 + 1 (IQ1_M: p >= 8 the minus shift)
 #pragma unroll
           for (int i = 0; i < 8; i++) {
-            const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
+            const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]);
+            if (kDefS) {
+              sc[i] = ffma2(al, pk2(Cq[2 * i], Cq[2 * i + 1]), A2);
+              continue;
+            }
+            const uint64_t B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
             if (!Fmt<F>::IQ1) {
               sc[i] = ffma2(al, B2, A2);
             } else if (F == IQ1_S) {
@@ -852,12 +885,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
             if (!hit) return;
           }
 #pragma unroll
-          for (int p = 0; p < 8; p++) {
+          for (int p = 0; p < 8; p += 2) {
             const int e0 = eb + 16 * h + 2 * p;
             track2(up2(sc[p]), e0, best, second, key);
-            if (F == IQ1_M) track2(up2(sc[8 + p]), N + e0, bestm, secondm, keym);
+            track2(up2(sc[p + 1]), e0 + 2, best1, second1, key1);
+            if (F == IQ1_M) {
+              track2(up2(sc[8 + p]), N + e0, bestm, secondm, keym);
+              track2(up2(sc[9 + p]), N + e0 + 2, bestm1, secondm1, keym1);
+            }
           }
         });
+      }
+      merge_track(best, second, key, best1, second1, key1);
+      if (F == IQ1_M) merge_track(bestm, secondm, keym, bestm1, secondm1, keym1);
+      if (kDefS) {  // back to full scores (INFINITY stays INFINITY)
+        best = __fadd_rn(best, Kp);
+        second = __fadd_rn(second, Kp);
       }
       if (F == IQ1_M) {  // back to full scores (INFINITY stays INFINITY)
         best = __fadd_rn(best, Kp);
