@@ -27,6 +27,7 @@
 // decoded values q, then takes the exact minimum with the lowest (choice) / (delta bit, entry) on
 // equal error.
 #include <mutex>
+#include <type_traits>
 
 #include "iq_common.cuh"
 
@@ -381,23 +382,21 @@ template <int F> struct TcCfg {
   static constexpr size_t EVERY = 2 * 128 * 16 * 4 * 3;
 };
 
-// Per-vector [128 x 8] tf32 operands: nw2 hi, nw2 lo, w hi, w lo; for the IQ1_M second sweep of
-// the searched and fixed modes, w/4 hi, w/4 lo, -w/4 hi, -w/4 lo; for IQ1_S with fixed choices,
-// sigma w/4 hi, sigma w/4 lo with sigma = +-1 the sign of the group's given shift (the shifted
-// sums' MMAs, below).
+// Per-vector [128 x 8] tf32 operands: nw2 hi, nw2 lo, w hi, w lo; for the second sweep of the
+// searched and fixed modes, IQ1_M: w/4 hi, w/4 lo, -w/4 hi, -w/4 lo; IQ1_S: sigma w/4 hi,
+// sigma w/4 lo with sigma = +-1 the sign of the group's shift, given (fixed choices) or chosen by
+// the first sweep (written between the sweeps) (the shifted sums' MMAs, below).
 template <int F, int MODE> __host__ __device__ constexpr int tc_na() {
-  return F == IQ1_M && (MODE == MODE_SEARCH || MODE == MODE_FIXED) ? 8 : (F == IQ1_S && MODE == MODE_FIXED ? 6 : 4);
+  return !Fmt<F>::IQ1 || !(MODE == MODE_SEARCH || MODE == MODE_FIXED) ? 4 : (F == IQ1_M ? 8 : 6);
 }
 // Deferred-shift layout of the second sweep: the shifted sums are split into the entry-dependent
 // part from the tensor cores, Bp' = w . h + (w/4) . g = B + Cg/4 and Bm' = B - Cg/4 (IQ1_M, whose
 // shift is searched per vector), or Bd' = B + sigma Cg/4 (IQ1_S with fixed choices, whose shift
-// is known per group before the sweep), and a part the same for every entry of a vector,
-// K(alpha, delta) = alpha Ws/64 + delta nT2, added to its best and runner-up only (fl(x + K) is
-// monotone in x).  The first sweep keeps An, Cg, B.  (Searched IQ1_S learns its shift only from
-// the first sweep.)
+// is one per group, given or chosen by the first sweep), and a part the same for every entry of a
+// vector, K(alpha, delta) = alpha Ws/64 + delta nT2, added to its best and runner-up only
+// (fl(x + K) is monotone in x).  The first sweep keeps An, Cg, B.
 template <int F, int MODE> __host__ __device__ constexpr bool tc_deferred(int sweep) {
-  return (F == IQ1_M && (MODE == MODE_FIXED || (MODE == MODE_SEARCH && sweep == 1))) ||
-         (F == IQ1_S && MODE == MODE_FIXED);
+  return Fmt<F>::IQ1 && (MODE == MODE_FIXED || (MODE == MODE_SEARCH && sweep == 1));
 }
 
 template <int F, int MODE, typename TIn>
@@ -415,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][128][16] (every mode)
   uint32_t *evk = reinterpret_cast<uint32_t *>(evm + 2 * 128 * 16); // [2][128][16] (every mode)
   float *evt = reinterpret_cast<float *>(evk + 2 * 128 * 16);       // [2][128][16] (every mode)
-  __shared__ uint64_t cb_bar, full_bar[2], empty_bar[2];
+  __shared__ uint64_t cb_bar, full_bar[2], empty_bar[2], op_bar;
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
 
@@ -427,6 +426,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
     mbar_init(&full_bar[1], 1);
     mbar_init(&empty_bar[0], kTcConsumers);
     mbar_init(&empty_bar[1], kTcConsumers);
+    mbar_init(&op_bar, 128);  // searched IQ1_S: the 4 blocks' shifted operands (every writer), per quad
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -444,12 +444,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   if (grid_bad && blockIdx.x == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, IQ_STATUS_BAD_GRID);
   __syncthreads();
 
+  constexpr bool kOpSync = F == IQ1_S && MODE == MODE_SEARCH;  // operands written between the sweeps
   const int g0 = lane & ~(VPG - 1);
   const int cg = lane / VPG;
   const int row = 32 * quarter + lane;                      // this lane's vector in the quad
   const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16);
   uint32_t cc = 0;                                          // chunk sequence number
   uint32_t issued = 0;                                      // (control) chunks committed
+  uint32_t nquad = 0;                                       // (control) quads issued
   int st_acc = 0;
 
   bool okl = ok;                                            // this thread's waits all completed
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       }
       if (sub == 0) {
         // IQ1_S with fixed choices: the sign of the group's shift (choice c = scale + 8 * shift bit)
-        const float sig = NA == 6 && active && (fixed_choice<G>(a, b, cg) >> 3) ? -0.25f : 0.25f;
+        const float sig = MODE == MODE_FIXED && NA == 6 && active && (fixed_choice<G>(a, b, cg) >> 3) ? -0.25f : 0.25f;
 #pragma unroll
         for (int k = 0; k < 8; k++) {
           const float nw = active ? v.nw2[k] : 0.0f, ww = active ? v.w[k] : 0.0f;
@@ -513,7 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
             aop[5 * 1024 + kmaj(row, k)] = 0.25f * wl;
             aop[6 * 1024 + kmaj(row, k)] = -0.25f * wh;
             aop[7 * 1024 + kmaj(row, k)] = -0.25f * wl;
-          } else if (NA == 6) {
+          } else if (NA == 6 && MODE == MODE_FIXED) {
             aop[4 * 1024 + kmaj(row, k)] = sig * wh;
             aop[5 * 1024 + kmaj(row, k)] = sig * wl;
           }
@@ -532,6 +534,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         for (int sw = 0; sw < nsweeps; sw++) {
           for (int ch = 0; ch < NCH; ch++, issued++) {
             const uint32_t buf = issued & 1;
+            // searched IQ1_S: the second sweep's shifted operands are written after the first sweep
+            if (kOpSync && sw == 1 && ch == 0 && okl && !mbar_wait_bounded(&op_bar, nquad & 1)) okl = false;
             if (!okl || (issued >= 2 && !mbar_wait_bounded(&empty_bar[buf], ((issued >> 1) - 1) & 1))) {
               okl = false;  // stop issuing; consumers' waits on the missing chunks time out
               break;
@@ -567,6 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           }
           if (!okl) break;
         }
+        nquad++;
       }
       okl = __shfl_sync(0xffffffffu, okl, 0);
       continue;
@@ -578,10 +583,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
     const uint64_t nT2p = pk2(v.nT2, v.nT2), Wsp = pk2(v.Ws, v.Ws);
     const float w64 = 0.015625f * v.Ws, t8 = 0.125f * v.nT2;  // exact power-of-two scalings
     const int ebase0 = 32 * sub;  // this warp's first entry in each chunk
-    constexpr bool kDefS = F == IQ1_S && MODE == MODE_FIXED;  // deferred layout [An | Bd' | -]
+    // IQ1_S second sweep (fixed or searched choices): deferred layout [An | Bd' | -]
+    constexpr bool kDefS = F == IQ1_S && (MODE == MODE_FIXED || MODE == MODE_SEARCH);
     // waits for chunk `cc`, hands the warp's 2 x 16 columns to fn(half, An, Cg, B), releases it
-    // (after a timeout the remaining chunks are skipped without waiting)
-    auto run_chunk = [&](auto &&fn) {
+    // (after a timeout the remaining chunks are skipped without waiting); two_cols: the chunk has
+    // only the first two columns (the IQ1_S deferred second sweep)
+    auto run_chunk = [&](auto two_cols, auto &&fn) {
       const uint32_t buf = cc & 1;
       if (okl && !mbar_wait_bounded(&full_bar[buf], (cc >> 1) & 1)) okl = false;
       okl = __all_sync(0xffffffffu, okl);
@@ -592,7 +599,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         float An[16], Bq[16], Cq[16];
         tmem_ld16(taddr + col + 16 * h, An);
         if (NQ == 3) tmem_ld16(taddr + col + kChunk + 16 * h, Cq);
-        if (!kDefS) tmem_ld16(taddr + col + (NQ - 1) * kChunk + 16 * h, Bq);  // (IQ1_S fixed: unused)
+        if constexpr (!decltype(two_cols)::value) tmem_ld16(taddr + col + (NQ - 1) * kChunk + 16 * h, Bq);
         tmem_wait_ld();
         if (active && okl) fn(h, An, Cq, Bq);
       }
@@ -613,7 +620,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
 #pragma unroll
       for (int c = 0; c < C; c++) m[c] = INFINITY;
       for (int ch = 0; ch < NCH; ch++) {
-        run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
+        run_chunk(std::false_type{}, [&](int h, const float *An, const float *Cq, const float *Bq) {
 #pragma unroll
           for (int i = 0; i < 8; i++) {
             const uint64_t A2 = pk2(An[2 * i], An[2 * i + 1]), B2 = pk2(Bq[2 * i], Bq[2 * i + 1]);
@@ -676,6 +683,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
     } else if (active) {
       c1 = fixed_choice<G>(a, b, cg);
     }
+    if constexpr (kOpSync) {
+      // the second sweep's shifted operand sigma w/4 (hi, lo) of each vector, sigma the sign of its
+      // group's chosen shift; the control warp issues the second sweep once all 4 blocks are in
+      if (sub == 0) {
+        const float sig = (c1 >> 3) ? -0.25f : 0.25f;
+#pragma unroll
+        for (int k = 0; k < 8; k++) {
+          const float ww = active ? v.w[k] : 0.0f;
+          const float wh = tf32_rna(ww), wl = tf32_rna(__fsub_rn(ww, wh));
+          aop[4 * 1024 + kmaj(row, k)] = sig * wh;
+          aop[5 * 1024 + kmaj(row, k)] = sig * wl;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(&op_bar);
+      }
+    }
 
     if constexpr (MODE == MODE_EVERY) {
       // ---- sweep 2 (every choice): each vector's best candidate under every choice ---------
@@ -689,7 +712,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       uint32_t *krow = evk + (sub * 128 + row) * 16;
       for (int ch = 0; ch < NCH; ch++) {
         const int eb = ch * kChunk + ebase0;
-        run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
+        run_chunk(std::false_type{}, [&](int h, const float *An, const float *Cq, const float *Bq) {
           float mn[C];
 #pragma unroll
           for (int c = 0; c < C; c++) mn[c] = INFINITY;
@@ -831,11 +854,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       float T = INFINITY;
       if (kFind && active) {
         // flag iff e2 - e1 <= kMargin (4 Cs + e1 + e2), i.e. e2 - e1 <= kMargin (4 Cs + 2 e1) /
-        // (1 - kMargin); the factors 1.01 and the relative term cover fp32 rounding here.  IQ1_M's
-        // second sweep evaluates the shifted scores in another order of rounding than the first
-        // (each within the rounding bound of the margin), so its bound is twice as wide.
-        constexpr float kW = F == IQ1_M ? 2.02f : 1.01f;
-        constexpr float kR = F == IQ1_M ? 1.9073486328125e-06f : 9.5367431640625e-07f;
+        // (1 - kMargin); the factors 1.01 and the relative term cover fp32 rounding here.  The IQ1
+        // second sweeps evaluate the shifted scores in another order of rounding than the first
+        // (each within the rounding bound of the margin), so their bound is twice as wide.
+        constexpr float kW = Fmt<F>::IQ1 ? 2.02f : 1.01f;
+        constexpr float kR = Fmt<F>::IQ1 ? 1.9073486328125e-06f : 9.5367431640625e-07f;
         const float e1 = __fmul_rn(alpha, smin);
         const float De = 1.01f * kMargin * fmaxf(4.0f * v.Cs + 2.0f * e1, 0.0f);
         T = smin + kW * (De / alpha) + kR * fabsf(smin);
@@ -849,7 +872,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       constexpr int PPH = F == IQ1_M ? 16 : 8;  // candidate pairs per half chunk
       for (int ch = 0; ch < NCH; ch++) {
         const int eb = ch * kChunk + ebase0;
-        run_chunk([&](int h, const float *An, const float *Cq, const float *Bq) {
+        run_chunk(std::integral_constant<bool, kDefS>{}, [&](int h, const float *An, const float *Cq, const float *Bq) {
           uint64_t sc[PPH];  // pair p: entries e0, e0 + 1 (IQ1_M: p >= 8 the minus shift)
 #pragma unroll
           for (int i = 0; i < 8; i++) {
@@ -881,7 +904,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
               mn = min3f(mn, q.x, q.y);
               if (F == IQ1_M) { const float2 r = up2(sc[8 + p]); mnm = min3f(mnm, r.x, r.y); }
             }
-            const bool hit = F == IQ1_M ? (__fadd_rn(mn, Kp) <= T || __fadd_rn(mnm, Km) <= T) : mn <= T;
+            const bool hit = F == IQ1_M ? (__fadd_rn(mn, Kp) <= T || __fadd_rn(mnm, Km) <= T)
+                                        : (kDefS ? __fadd_rn(mn, Kp) <= T : mn <= T);
             if (!hit) return;
           }
 #pragma unroll
