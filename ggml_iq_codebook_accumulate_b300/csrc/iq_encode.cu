@@ -303,9 +303,10 @@ __device__ __forceinline__ float group_sum(float val, int g0) {
 //     An = -2 (w t) . g        B = w . h (h = g^2 or |g|)        Cg = w . g (IQ1)
 // evaluated by tcgen05.mma (kind::tf32, fp32 accumulators in tensor memory), 64 codebook entries
 // per chunk.  The codebook values are small integers, exact in tf32; each fp32 per-vector operand
-// is split into two tf32 parts (hi, lo = x - hi) accumulated into the same tensor-memory column,
-// so every product is exact and the sums carry only accumulation rounding (measured on B300 at
-// most 4.3 units of 2^-24 of sum |a*b|, inside the same rounding margin as an fp32 FMA chain).
+// is split into two tf32 parts (hi, lo = x - hi, each rounded to tf32) accumulated into the same
+// tensor-memory column: every product of a part is exact, the split leaves at most 2^-22 of each
+// operand, and the sums carry the accumulation rounding (together measured on B300 at most 6.3
+// units of 2^-24 of sum |a*b|, inside the same rounding margin as an fp32 FMA chain).
 // A control warp issues the MMAs into a double-buffered tensor-memory region and commits each
 // chunk to an mbarrier; 8 consumer warps (2 per tensor-memory lane quarter = block) load their 32
 // columns per chunk with tcgen05.ld and do the per-choice scoring with packed f32x2 FMAs and
