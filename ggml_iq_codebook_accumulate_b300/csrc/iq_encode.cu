@@ -1056,20 +1056,225 @@ __device__ __forceinline__ void cand_of_choice(int c, int &s, int &db0, int &db1
   else { s = c; db0 = db1 = 0; }
 }
 
+// Exact rescoring of the flagged items, in one of two layouts chosen by their number.
+//
+// CTA per item (used when the items are fewer than the resident warps): one CTA of 8 warps
+// re-decides one flagged item at a time.  Per flagged group, warp w takes the
+// group's vector w % VPG over entry slice w / VPG (8 / VPG slices of the codebook) for the fp32
+// minima, and the (near choice, vector, slice) units in turn for the exact minima; the partial
+// results meet in shared memory.  Every reduction (a minimum; the least exact error, lowest key on
+// equal errors) gives the same value in any order, so the result does not depend on the split.
+constexpr int kRsWarps = 8;
 struct RescoreSmem {
+  uint32_t pay[24];                  // the item's payload bytes
+  float part[kRsWarps][16];          // (a) per-warp minima over its slice, per choice
+  float mh[4][16];                   // (a) per-vector minima
+  double pex[16][4][4];              // (c) least exact error per (choice, vector, slice)
+  int pkey[16][4][4];                //     and its key
+  double ex[4][16];                  // (c) per (vector, choice)
+  int exkey[4][16];
+};
+
+template <int F, int MODE, typename TIn>
+__device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws, int nflag, RescoreSmem &sm) {
+  constexpr int C = Fmt<F>::C, N = Fmt<F>::N, VPG = Fmt<F>::VPG, BB = Fmt<F>::BB, G = Fmt<F>::G;
+  constexpr int NSL = kRsWarps / VPG;  // entry slices per vector
+  constexpr int SL = N / NSL;          // entries per slice
+  static_assert(kRsWarps % VPG == 0 && SL % 32 == 0 && NSL <= 4 && VPG <= 4, "slices of whole warps");
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int kv = wid % VPG, js = wid / VPG;  // this warp's vector in the group and slice in (a)
+  const float4 *tab = ws.tab;
+  // an item is (block, flagged vectors); every-choice payloads: (block | choice << 27, flagged
+  // vectors), re-decided as a fixed-choice block in that choice's payload
+  constexpr bool kFixedLike = MODE == MODE_FIXED || MODE == MODE_EVERY;
+  uint8_t *pbytes = reinterpret_cast<uint8_t *>(sm.pay);
+  for (int it = blockIdx.x; it < nflag; it += gridDim.x) {
+    const uint2 item = ws.fb[it];
+    const int cpass = MODE == MODE_EVERY ? (int)(item.x >> 27) : 0;
+    const int64_t b = MODE == MODE_EVERY ? (int64_t)(item.x & ((1u << 27) - 1u)) : (int64_t)item.x;
+    const uint32_t mask = item.y;
+    uint8_t *payb = a.payload + (MODE == MODE_EVERY ? (size_t)cpass * a.nblocks * BB : 0) + b * BB;
+    for (int i = threadIdx.x; i < BB; i += blockDim.x) pbytes[i] = payb[i];
+    Vec v;
+    load_block_vec<TIn>(a, b, lane, v);  // every warp holds the whole block
+    __syncthreads();
+    uint32_t d16;
+    if (F == IQ1_M) {
+      d16 = 0;
+      for (int k = 0; k < 4; k++) d16 |= get_bits(pbytes, f_d16_nib<F>(k)) << (4 * k);
+    } else {
+      d16 = get_bits(pbytes, f_d16<F>());
+    }
+    const float d = half_bits_to_float((uint16_t)d16);
+    vec_setup<F>(v);
+    for (int g = 0; g < G; g++) {
+      const uint32_t gm = ((1u << VPG) - 1u) << (g * VPG);
+      if (!(mask & gm)) continue;
+      const int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : MODE == MODE_EVERY ? cpass : -1;
+      float Cg = 0.0f;  // the group's sum of w t^2, in vector order (every thread alike)
+      for (int k = 0; k < VPG; k++) {
+        const float cs = __shfl_sync(0xffffffffu, v.Cs, g * VPG + k);
+        Cg = k == 0 ? cs : __fadd_rn(Cg, cs);
+      }
+      // (a) fp32 minima of vector kv over slice js for every choice (or the fixed one), as the
+      // sweep computes them
+      {
+        const Vec u = shfl_vec(v, g * VPG + kv);
+        float lm[C], alc[C];
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+          lm[c] = INFINITY;
+          int s, db0, db1;
+          cand_of_choice<F>(c, s, db0, db1);
+          alc[c] = alpha_of<F>(d, s);
+        }
+        for (int e = js * SL + lane; e < (js + 1) * SL; e += 32) {
+          Entry en;
+          load_entry<F>(tab, e, en);
+          // the entry's sums once, then every choice's score as cand_score forms it
+          float An = 0.0f, Bs = 0.0f, Anp = 0.0f, Bp = 0.0f, Anm = 0.0f, Bm = 0.0f;
+          if (!Fmt<F>::IQ1) ab2(u.nw2, u.w, en, An, Bs);
+          else ab1(u, en, Anp, Bp, Anm, Bm);
+#pragma unroll
+          for (int c = 0; c < C; c++) {
+            if (kFixedLike && c != cfix) continue;
+            int s, db0, db1;
+            cand_of_choice<F>(c, s, db0, db1);
+            if (!Fmt<F>::IQ1) {
+              lm[c] = fminf(lm[c], __fmaf_rn(alc[c], Bs, An));
+            } else {
+              lm[c] = fminf(lm[c], db0 ? __fmaf_rn(alc[c], Bm, Anm) : __fmaf_rn(alc[c], Bp, Anp));
+              if (db1 != db0) lm[c] = fminf(lm[c], db1 ? __fmaf_rn(alc[c], Bm, Anm) : __fmaf_rn(alc[c], Bp, Anp));
+            }
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < C; c++) {
+          float x = lm[c];
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) x = fminf(x, __shfl_xor_sync(0xffffffffu, x, off));
+          if (lane == 0) sm.part[wid][c] = x;
+        }
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < VPG * C; t += blockDim.x) {
+        const int k = t / C, c = t % C;
+        float x = INFINITY;
+        for (int j = 0; j < NSL; j++) x = fminf(x, sm.part[j * VPG + k][c]);
+        sm.mh[k][c] = x;
+      }
+      __syncthreads();
+      // (b) near set of choices (every thread alike)
+      uint32_t near = 0;
+      {
+        float D[C];
+        float D1 = INFINITY;
+        for (int c = 0; c < C; c++) {
+          if (kFixedLike && c != cfix) { D[c] = INFINITY; continue; }
+          float S = sm.mh[0][c];
+          for (int k = 1; k < VPG; k++) S = __fadd_rn(S, sm.mh[k][c]);
+          D[c] = __fmul_rn(alpha_choice<F>(d, c), S);
+          D1 = fminf(D1, D[c]);
+        }
+        for (int c = 0; c < C; c++)
+          if (D[c] != INFINITY && __fsub_rn(D[c], D1) <= kMargin * (4.0f * Cg + D1 + D[c])) near |= 1u << c;
+      }
+      // (c) exact minimum per (near choice, vector) over the candidates the bound cannot exclude:
+      // units (near choice, vector, slice) dealt to the warps
+      const int nunits = __popc(near) * VPG * NSL;
+      for (int unit = wid; unit < nunits; unit += kRsWarps) {
+        const int ci = unit / (VPG * NSL), k = (unit / NSL) % VPG, j = unit % NSL;
+        uint32_t rest = near;
+        for (int q = 0; q < ci; q++) rest &= rest - 1u;
+        const int c = __ffs(rest) - 1;
+        int s, db0, db1;
+        cand_of_choice<F>(c, s, db0, db1);
+        const float al = alpha_of<F>(d, s);
+        const Vec u = shfl_vec(v, g * VPG + k);
+        const float emin = __fmul_rn(al, sm.mh[k][c]);
+        double bestE = INFINITY;
+        int bestK = 0x7fffffff;
+        for (int e = j * SL + lane; e < (j + 1) * SL; e += 32) {
+          Entry en;
+          load_entry<F>(tab, e, en);
+          for (int db = db0; db <= db1; db++) {
+            const float sc = cand_score<F>(u, en, al, db);
+            const float ec = __fmul_rn(al, sc);
+            if (__fsub_rn(ec, emin) <= kMargin * (4.0f * u.Cs + emin + ec)) {
+              const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
+              const int kk = (F == IQ1_M ? db * N : 0) + e;
+              if (E < bestE || (E == bestE && kk < bestK)) { bestE = E; bestK = kk; }
+            }
+          }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const double oE = __shfl_xor_sync(0xffffffffu, bestE, off);
+          const int oK = __shfl_xor_sync(0xffffffffu, bestK, off);
+          if (oE < bestE || (oE == bestE && oK < bestK)) { bestE = oE; bestK = oK; }
+        }
+        if (lane == 0) { sm.pex[c][k][j] = bestE; sm.pkey[c][k][j] = bestK; }
+      }
+      __syncthreads();
+      for (int t = threadIdx.x; t < VPG * C; t += blockDim.x) {
+        const int k = t / C, c = t % C;
+        if (!((near >> c) & 1)) continue;
+        double E = sm.pex[c][k][0];
+        int K = sm.pkey[c][k][0];
+        for (int j = 1; j < NSL; j++) {
+          const double oE = sm.pex[c][k][j];
+          const int oK = sm.pkey[c][k][j];
+          if (oE < E || (oE == E && oK < K)) { E = oE; K = oK; }
+        }
+        sm.ex[k][c] = E;
+        sm.exkey[k][c] = K;
+      }
+      __syncthreads();
+      // (d) exact choice: least sum over the vectors, lowest choice on equal error; (e) rewrite the
+      // group's fields (keep the sweep's decision if nothing was comparable)
+      if (threadIdx.x == 0) {
+        int cstar = -1;
+        double bestG = INFINITY;
+        for (int c = 0; c < C; c++) {
+          if (!((near >> c) & 1)) continue;
+          double Eg = sm.ex[0][c];
+          for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, sm.ex[k][c]);
+          if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
+        }
+        if (cstar >= 0) {
+          set_bits_bytes(pbytes, f_scale<F>(g), (uint32_t)(F == IQ1_S ? (cstar & 7) : cstar));
+          if (F == IQ1_S) set_bits_bytes(pbytes, f_dbit_grp<F>(g), (uint32_t)(cstar >> 3));
+          for (int k = 0; k < VPG; k++) {
+            const int vv = g * VPG + k;
+            const int key = sm.exkey[k][cstar];
+            const int idx = F == IQ1_M ? key % N : key;
+            const Bits lo = f_idx_lo<F>(vv);
+            set_bits_bytes(pbytes, lo, (uint32_t)idx);
+            if (F == IQ2_S || Fmt<F>::IQ1) set_bits_bytes(pbytes, f_idx_hi<F>(vv), (uint32_t)idx >> lo.width);
+            if (F == IQ1_M) set_bits_bytes(pbytes, f_dbit_vec<F>(vv), (uint32_t)(key / N));
+          }
+        }
+      }
+      __syncthreads();
+    }
+    for (int i = threadIdx.x; i < BB; i += blockDim.x) payb[i] = pbytes[i];
+    __syncthreads();  // the payload bytes are reused by the next item
+  }
+}
+
+struct RescoreWarpSmem {
   float mh[4][16];
   double ex[4][16];
   int exkey[4][16];
   uint32_t pay[24];
 };
 
+// Warp per item: each warp re-decides its own items, so that the warps' load latencies overlap
+// (used when the items outnumber the resident warps).
 template <int F, int MODE, typename TIn>
-__global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
+__device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &ws, int nflag, RescoreWarpSmem &sm) {
   constexpr int C = Fmt<F>::C, N = Fmt<F>::N, VPG = Fmt<F>::VPG, BB = Fmt<F>::BB, G = Fmt<F>::G;
-  __shared__ RescoreSmem sm_all[8];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  RescoreSmem &sm = sm_all[wid];
-  const int nflag = ws.hdr[1];
   const float4 *tab = ws.tab;
   // an item is (block, flagged vectors); every-choice payloads: (block | choice << 27, flagged
   // vectors), re-decided as a fixed-choice block in that choice's payload
@@ -1085,6 +1290,7 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
     load_block_vec<TIn>(a, b, lane, v);
     uint8_t *pbytes = reinterpret_cast<uint8_t *>(sm.pay);
     for (int i = lane; i < BB; i += 32) pbytes[i] = payb[i];
+    __syncwarp();
     uint32_t d16;
     if (F == IQ1_M) {
       d16 = 0;
@@ -1222,6 +1428,15 @@ __global__ void __launch_bounds__(256) rescore_kernel(EncArgs a, EncWs ws) {
   }
 }
 
+template <int F, int MODE, typename TIn>
+__global__ void __launch_bounds__(kRsWarps * 32) rescore_kernel(EncArgs a, EncWs ws) {
+  __shared__ RescoreSmem sm;
+  __shared__ RescoreWarpSmem smw[kRsWarps];
+  const int nflag = ws.hdr[1];  // the same for every CTA, so every CTA takes the same layout
+  if (nflag >= kRsWarps * (int)gridDim.x) rescore_by_warp<F, MODE, TIn>(a, ws, nflag, smw[threadIdx.x >> 5]);
+  else rescore_by_cta<F, MODE, TIn>(a, ws, nflag, sm);
+}
+
 // ---------------------------------------------------------------------------------------------
 template <int F, typename TIn>
 __global__ void __launch_bounds__(256) anchor_kernel(const TIn *__restrict__ W, int64_t cols, int64_t nblocks,
@@ -1281,7 +1496,10 @@ static int run_encode(const EncArgs &a, void *workspace, size_t ws_bytes, cudaSt
   kern<<<grid, kTcThreads, smem, st>>>(a, ws, nquads);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   if (MODE != MODE_TABLE) {
-    rescore_kernel<F, MODE, TIn><<<num_sms() * 2, 256, 0, st>>>(a, ws);
+    auto rk = rescore_kernel<F, MODE, TIn>;
+    int rs_per_sm = 2;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&rs_per_sm, rk, kRsWarps * 32, 0);
+    rk<<<num_sms() * (rs_per_sm > 1 ? rs_per_sm : 1), kRsWarps * 32, 0, st>>>(a, ws);
     if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   }
   return IQ_OK;
