@@ -131,10 +131,13 @@ void or_float_from_half_n(const uint16_t *in, float *out, int64_t n) {
 /* ------------------------------------------------------------------------------------------ */
 /* imatrix: per routed expert, sum of squared activations and token counts.
  * Order (our reading of "squares 1,024 rows at a time"): for each chunk of rows_per_chunk rows, a
- * partial sum per (expert, column) starts at +0 and adds the square x*x of each token of the chunk
- * routed to the expert, in ascending token order, with ONE rounding per token: partial =
- * fl(partial + x*x), the exact square added and rounded once (C's fmaf); then in_sum2 += partial
- * (one rounded fp32 add), chunk by chunk, for experts the chunk routed at least one token to.
+ * partial sum per (expert, column) starts at +0 and adds the square of each token of the chunk
+ * routed to the expert, in ascending token order: the square is one rounded fp32 multiply, sq =
+ * fl(x*x), and it is added with one rounded fp32 add, partial = fl(partial + sq) (the page squares
+ * the rows, then sums them; this file is built without FMA contraction, so the two steps stay
+ * apart); then in_sum2 += partial (one rounded fp32 add), chunk by chunk, for experts the chunk
+ * routed at least one token to.  For bf16 activations the square is exact, so there the result
+ * equals the exact square added with a single rounding.
  * A token's top-k slots are read as a set: a repeated id counts once (and is reported). */
 int or_imatrix_accumulate(const float *x, int64_t tokens, int64_t cols, const int32_t *ids, int top_k,
                           int E, int64_t rows_per_chunk, float *in_sum2, int64_t *counts,
@@ -164,7 +167,10 @@ int or_imatrix_accumulate(const float *x, int64_t tokens, int64_t cols, const in
         touched_call[e] = 1;
         const float *xr = x + t * cols;
         float *pr = partial + (int64_t)e * cols;
-        for (int64_t j = 0; j < cols; j++) pr[j] = fmaf(xr[j], xr[j], pr[j]);
+        for (int64_t j = 0; j < cols; j++) {
+          const float sq = xr[j] * xr[j];
+          pr[j] = pr[j] + sq;
+        }
       }
     }
     for (int e = 0; e < E; e++) {

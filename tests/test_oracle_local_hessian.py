@@ -193,3 +193,52 @@ def test_searched_payload_is_made_of_the_every_choice_payloads(fmt):
         for g in range(G):
             s = slice(g * gs, (g + 1) * gs)
             assert np.array_equal(q[b, s], qc[ch[b, g]][b, s])
+
+
+def test_revisits_on_a_hand_computed_block():
+    """The revisit step (PR #3158: two passes, each group against the others' current choices,
+    moving only to a strictly lower block error) on a block worked out by hand.
+
+    Four groups of 64 columns and three choices; only column 64 g of group g is nonzero, with
+    dw = a[g][c] under choice c (group 3 is all zero), so dw H dw^T is the quadratic form of the
+    3 x 3 matrix M of H's entries at columns 0, 64, 128:
+        a = [[-3, 0, 1], [-3, 2, 3], [-2, -3, 2]],   M = [[5, -2, 2], [-2, 4, -2], [2, -2, 2]]
+        E(v) = 5 v0^2 + 4 v1^2 + 2 v2^2 - 4 v0 v1 + 4 v0 v2 - 4 v1 v2.
+    Own blocks (a^2 M_gg): group 0 (45, 0, 5) -> 1; group 1 (36, 16, 36) -> 1; group 2 (8, 18, 8)
+    -> 0 (lowest choice of two equal); group 3 all 0 -> 0.
+    Revisit 1, start (1, 1, 0):
+      group 0 with v1 = 2, v2 = -2: E = 5 v0^2 - 16 v0 + 40 = (133, 40, 29) -> moves to 2;
+      group 1 with v0 = 1 (group 0's NEW choice), v2 = -2: E = 4 v1^2 + 4 v1 + 5 = (29, 29, 53):
+        choice 0 only ties the current choice 1, so group 1 stays at 1 (with the stale v0 = 0 it
+        would read (20, 40, 68) and move to 0);
+      group 2 with v0 = 1, v1 = 2: E = 2 v2^2 - 4 v2 + 13 = (29, 43, 13) -> moves to 2.
+    Revisit 2, start (2, 1, 2):
+      group 0 with v1 = 2, v2 = 2: E = 5 v0^2 + 8 = (53, 8, 13) -> moves to 1 (only a second pass
+        makes this move);
+      group 1 with v0 = 0, v2 = 2: E = 4 v1^2 - 8 v1 + 8 = (68, 8, 20) -> stays at 1;
+      group 2 with v0 = 0, v1 = 2: E = 2 v2^2 - 8 v2 + 16 = (40, 58, 8) -> stays at 2.
+    Result (1, 1, 2, 0).  One pass would leave (2, 1, 2, 0); moving on equal errors would give
+    group 1 choice 0; revisiting against the step-2 choices would also move group 1."""
+    a = np.array([[-3, 0, 1], [-3, 2, 3], [-2, -3, 2]], np.float64)
+    M = np.array([[5, -2, 2], [-2, 4, -2], [2, -2, 2]], np.float64)
+    cols = [0, 64, 128]
+    dw = np.zeros((3, 256))
+    for g in range(3):
+        dw[:, cols[g]] = a[g]
+    H = np.eye(256)
+    for i in range(3):
+        for j in range(3):
+            H[cols[i], cols[j]] = M[i, j]
+    got, tr = lh.search_block(dw, H, 64, trace=True)
+    assert got.tolist() == [1, 1, 2, 0]
+    own = [t[3] for t in tr if t[0] == "own"]
+    assert own == [1, 1, 0, 0]
+    rev = [t for t in tr if t[0] == "revisit"]
+    assert len(rev) == 8                                  # two passes over four groups
+    assert [t[3] for t in rev] == [2, 1, 2, 0, 1, 1, 2, 0]
+    assert rev[0][2].tolist() == [133, 40, 29]
+    assert rev[1][2].tolist() == [29, 29, 53]
+    assert rev[2][2].tolist() == [29, 43, 13]
+    assert rev[4][2].tolist() == [53, 8, 13]
+    assert rev[5][2].tolist() == [68, 8, 20]
+    assert rev[6][2].tolist() == [40, 58, 8]

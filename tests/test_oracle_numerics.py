@@ -75,9 +75,19 @@ def f32_nearest(q: Fraction) -> np.float32:
     return min(cands, key=lambda v: (abs(Fraction(float(v)) - q), int(np.float32(v).view(np.uint32)) & 1))
 
 
+def running_sum_exact(col):
+    """partial = fl(partial + fl(x*x)) for each x in order, with exact rational arithmetic: the
+    square is correctly rounded to fp32 once, and the addition once more (two roundings a step)."""
+    acc = np.float32(0.0)
+    for x in col:
+        sq = f32_nearest(Fraction(float(x)) ** 2)
+        acc = f32_nearest(Fraction(float(acc)) + Fraction(float(sq)))
+    return acc
+
+
 def fused_running_sum_exact(col):
-    """partial = fl(partial + x*x) for each x in order, with exact rational arithmetic and one
-    correct rounding per step: the definition of the single-rounding running sum."""
+    """The other reading, partial = fl(partial + x*x) with the exact square and one rounding a step
+    (a fused multiply-add), for telling the two apart."""
     acc = np.float32(0.0)
     for x in col:
         acc = f32_nearest(Fraction(float(acc)) + Fraction(float(x)) ** 2)
@@ -86,52 +96,54 @@ def fused_running_sum_exact(col):
 
 def bounded_bf16_acts(tokens, cols, seed):
     """bf16-valued activations with 2^-4 <= |x| < 2^4.  A square then has at most 16 significant
-    bits and lies in [2^-8, 2^8); a running sum of up to 1,024 of them stays below 2^18 with its
-    lowest bit at or above 2^-31, so every step partial + x*x is exact in fp64 (at most 50
-    significant bits) and one fp64 -> fp32 rounding is the single correct rounding."""
+    bits and lies in [2^-8, 2^8), so fl(x*x) = x*x exactly; a running sum of up to 1,024 of them
+    stays below 2^18 with its lowest bit at or above 2^-31, so every step partial + x*x is exact in
+    fp64 (at most 50 significant bits) and one fp64 -> fp32 rounding is the single correct rounding
+    of the addition."""
     x = synth.activations(tokens, cols, seed=seed)
     mag = np.clip(np.abs(x), 2.0 ** -4, 2.0 ** 4 * (1 - 2.0 ** -9))
     x = np.where(x < 0, -mag, mag).astype(np.float32)
     return synth.as_dtype(x, "bf16")[1]
 
 
-def fused_running_sum_f64(rows):
+def running_sum_f64(rows):
     """Vectorised running sum over axis 0, one fp32 rounding per step from an exact fp64 step
-    (valid for the bounded inputs above)."""
+    (valid for the bounded inputs above, whose squares are exact in fp32)."""
     acc = np.zeros(rows.shape[1], np.float32)
     for r in rows:
         acc = (acc.astype(np.float64) + r.astype(np.float64) ** 2).astype(np.float32)
     return acc
 
 
-def test_imatrix_single_rounding_exact_small(orc):
+def test_imatrix_square_then_add_exact_small(orc):
     """Values spanning 1e-22 .. 1e4, fp32-valued, some squares subnormal: each step of the running
-    sum is the exact square added and rounded once (exact rational reference)."""
+    sum rounds the square to fp32, then rounds the addition (exact rational reference)."""
     rng = np.random.default_rng(19)
     x = (rng.standard_normal((48, 40)) * 10.0 ** rng.integers(-22, 4, (48, 40))).astype(np.float32)
     x[5, 0] = np.float32(3e-20)            # square 9e-40: subnormal in fp32
     x[:3, 4] = np.float32(1e-23)           # squares far below the fp32 range, then larger terms
     s2, counts, _ = orc.imatrix_accumulate(x, np.zeros((48, 1), np.int32), 1, rows_per_chunk=1024)
     assert counts[0] == 48
-    ref = np.array([fused_running_sum_exact(x[:, j]) for j in range(40)], np.float32)
+    ref = np.array([running_sum_exact(x[:, j]) for j in range(40)], np.float32)
     assert np.array_equal(s2[0].view(np.uint32), ref.view(np.uint32))
-    # the two-rounding form (fp32 multiply, then fp32 add) differs in some columns, so this pin
-    # tells the two readings apart
-    assert not np.array_equal(s2[0], np.cumsum(x * x, axis=0, dtype=np.float32)[-1])
+    # the single-rounding reading (fused multiply-add) differs in some columns, so this pin tells
+    # the two readings apart
+    fused = np.array([fused_running_sum_exact(x[:, j]) for j in range(40)], np.float32)
+    assert not np.array_equal(s2[0].view(np.uint32), fused.view(np.uint32))
 
 
 def test_imatrix_single_expert_is_sequential_column_sum(orc):
-    """One expert, top-1, one chunk: the sum is the running single-rounding sum of x*x down each
-    column (exact fp64 steps on bounded bf16 inputs)."""
+    """One expert, top-1, one chunk: the sum is the running sum of x*x down each column, one rounding
+    per addition (exact fp64 steps on bounded bf16 inputs, whose squares are exact)."""
     x = bounded_bf16_acts(700, 512, seed=8)
     ids = np.zeros((700, 1), np.int32)
     s2, counts, _ = orc.imatrix_accumulate(x, ids, 1, rows_per_chunk=1024)
     assert counts[0] == 700
-    assert np.array_equal(s2[0], fused_running_sum_f64(x))
+    assert np.array_equal(s2[0], running_sum_f64(x))
 
 
 def test_imatrix_chunks_add_partial_sums(orc):
-    """Chunked: each chunk's per-expert partial (running single-rounding sum over its routed tokens)
+    """Chunked: each chunk's per-expert partial (running sum over its routed tokens)
     is added to the running total (one fp32 add) in chunk order."""
     T, C, E, K, R = 530, 256, 6, 2, 128
     x = bounded_bf16_acts(T, C, seed=9)
@@ -143,7 +155,7 @@ def test_imatrix_chunks_add_partial_sums(orc):
         for e in range(E):
             rows = [t for t in range(sl.start, sl.stop) if e in ids[t]]
             if rows:
-                ref[e] = ref[e] + fused_running_sum_f64(x[rows])
+                ref[e] = ref[e] + running_sum_f64(x[rows])
     assert np.array_equal(s2, ref)
 
 
@@ -244,6 +256,27 @@ def test_anchor_iq1_m_peak_to_rms(orc):
         assert abs(got - exact) <= float(np.spacing(np.float16(exact))), (b, got, exact)
     zero, _ = orc.anchor_scales("IQ1_M", np.zeros((1, 256), np.float32))
     assert zero[0] == 0
+
+
+def test_anchor_iq1_m_sums_squares_in_the_fixed_tree(orc):
+    """The IQ1_M anchor's sum of squares takes 32 sequential sums of 8 consecutive squares, then
+    pairs them (l, l+16), (l, l+8), ..., (l, l+1).  Block A: eight even values whose squares sum to
+    S0 = 33,624,288 (in [2^25, 2^26), where fp32 holds multiples of 4), then 248 ones.  In the tree
+    the first 8-sum is S0 exactly, the other 31 are 8 each, and every pairing adds a multiple of 4
+    below 2^26, so the tree gives the exact S0 + 248.  A sequential sum over the 256 squares rounds
+    each S0 + 1 back to S0 and gives S0.  Block B (the same eight values, then 14, 6 and 4, whose
+    squares add 248) and block C (the eight values alone) have only multiples of 4 below 2^26 in
+    every partial sum, so they give S0 + 248 and S0 in any order.  A must anchor as B, not as C
+    (the two differ in the last fp16 bit at this amax)."""
+    big = np.array([2080, 2080, 2054, 2062, 2054, 2016, 2020, 2034], np.float32)
+    assert int((big.astype(np.int64) ** 2).sum()) == 33624288
+    A = np.ones(256, np.float32); A[:8] = big
+    B = np.zeros(256, np.float32); B[:8] = big; B[8:11] = [14, 6, 4]
+    C = np.zeros(256, np.float32); C[:8] = big
+    d16, st = orc.anchor_scales("IQ1_M", np.concatenate([A, B, C])[None, :])
+    assert st == 0
+    assert d16[1] != d16[2]
+    assert d16[0] == d16[1]
 
 
 def test_anchor_reports_non_finite(orc):
