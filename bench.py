@@ -8,7 +8,10 @@ codebooks.  One step = the whole hot path over that batch:
   everywhere) + decode of the searched payload (fp32).
 value = 5 * 5632 * 2048 weight elements / step time (M elem/s; each element goes through the full
 path once per format).  Per-kernel CUDA-event times give per-format encode M elem/s, decode and
-imatrix GB/s and the roofline of the dominant kernel.
+imatrix GB/s and the roofline of the dominant kernel.  Besides the step, the line reports the
+routed-MoE imatrix (4096 x 17408, 128 experts), the HBM-bound large-layer decode, the MoE expert
+encode (128 x [1536, 2048]), the large-layer encode with every-choice tables ([17408, 5120] and
+[5120, 17408]) and the local-Hessian choice search.
 
 --impl reference times the plain C oracle (the CPU definition of the same path) on a bounded row
 sample of the same workload on this host's cores.
@@ -44,11 +47,16 @@ CONFIG = {"workload": "encode 5632x2048 bf16 weight in IQ2_XXS/IQ2_XS/IQ2_S/IQ1_
 
 MOE_T, MOE_C, MOE_E, MOE_K = 4096, 17408, 128, 8
 DEC_R, DEC_C = 17408, 5120
+EXP_E, EXP_R, EXP_C = 128, 1536, 2048          # MoE expert encode: 128 x gate/up [1536, 2048]
+LARGE_SHAPES = ((17408, 5120), (5120, 17408))  # large-layer encode with the every-choice table
+REF_CONFIG = {"workload": CONFIG["workload"], "rows": R, "cols": C, "activation_rows": T_ACT,
+              "rows_per_chunk": 1024,
+              "timing": "host wall clock over whole steps of the plain C oracle (fp64 direct-form search, "
+                        "OpenMP over blocks) on this host's cores; each step encodes a row sample"}
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the searched encode
-# kernel on this workload, from the ncu captures summarised in profiles/encode_tc_searched_5632x2048.md,
-# and the SHA-256 of the encoder sources they were taken on: the figure is reported only while the
-# sources are unchanged.
+# kernel on this workload, from ncu captures of that launch, and the SHA-256 of the encoder
+# sources they were taken on: the figure is reported only while the sources are unchanged.
 PROFILED_ENCODE_TRAFFIC = {"IQ2_XXS": 23171328, "IQ1_S": 23270912, "IQ1_M": 23268352}
 PROFILED_ENCODE_SHA256 = "b2765104f8e182f714b8a08580036aa4cc42187530ab9fcaa311525a776ca323"
 ENCODE_SOURCES = ("ggml_iq_codebook_accumulate_b300/csrc/iq_encode.cu", "ggml_iq_codebook_accumulate_b300/csrc/iq_common.cuh")
@@ -130,30 +138,52 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "M elem/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": CONFIG,
+            "config": dict(REF_CONFIG, rows_sampled=rows),
             "cpu_baseline": {"value": round(value, 4), "unit": "M elem/s", "cores": cores, "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": "M elem/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 
 
-def cpu_baseline_sample(Wv, Xv, grids, budget_rows=768):
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline_sample(Wv, Xv, grids, budget_rows=768, single_rows=48):
+    """The oracle on this host: all cores (OpenMP over blocks) on ``budget_rows`` rows per format,
+    and one thread on ``single_rows`` rows, each with the full imatrix pass (single-threaded in the
+    oracle) once."""
     import oracle
     oracle.build()
     ids = np.zeros((T_ACT, 1), np.int32)
-    t0 = time.perf_counter()
-    s2, cn, _ = oracle.imatrix_accumulate(Xv, ids, 1)
-    w = oracle.imatrix_weights(s2, cn)[0]
-    for f in FORMATS:
-        p, _ = oracle.encode(f, Wv[:budget_rows], grids[f], importance=w)
-        ch = np.full((budget_rows * C // 256, oracle.format_info(f)["groups"]), 7, np.uint8)
-        oracle.encode(f, Wv[:budget_rows], grids[f], importance=w, choices=ch)
-        oracle.decode(f, p, budget_rows, C, grids[f])
-    dt = time.perf_counter() - t0
+
+    def run(rows, threads):
+        t0 = time.perf_counter()
+        s2, cn, _ = oracle.imatrix_accumulate(Xv, ids, 1)
+        w = oracle.imatrix_weights(s2, cn)[0]
+        for f in FORMATS:
+            p, _ = oracle.encode(f, Wv[:rows], grids[f], importance=w, threads=threads)
+            ch = np.full((rows * C // 256, oracle.format_info(f)["groups"]), 7, np.uint8)
+            oracle.encode(f, Wv[:rows], grids[f], importance=w, choices=ch, threads=threads)
+            oracle.decode(f, p, rows, C, grids[f])
+        return time.perf_counter() - t0
+
+    dt = run(budget_rows, 0)
+    dt1 = run(single_rows, 1)
     return {"value": round(5 * budget_rows * C / dt / 1e6, 4), "unit": "M elem/s", "cores": os.cpu_count(),
-            "kind": "oracle",
+            "kind": "oracle", "cpu_model": cpu_model(),
             "sample": f"one step on {budget_rows} of {R} rows per format (searched + fixed encode, decode) plus the "
-                      f"full {T_ACT}x{C} imatrix pass; {dt:.1f} s"}
+                      f"full {T_ACT}x{C} imatrix pass; {dt:.1f} s",
+            "single_thread": {"value": round(5 * single_rows * C / dt1 / 1e6, 4), "unit": "M elem/s", "cores": 1,
+                              "sample": f"one step on {single_rows} rows per format plus the imatrix pass, one "
+                                        f"thread; {dt1:.1f} s"}}
 
 
 # ----------------------------------------------------------------------------------------------
@@ -323,15 +353,21 @@ def run_ours(args):
                  "encode_fixed_Melem_s": round(R * C / (x_ms * 1e-3) / 1e6, 1),
                  "decode_GB_s": round(dec_bytes / (d_ms * 1e-3) / 1e9, 1),
                  "encode_ms": round(e_ms, 4), "fixed_ms": round(x_ms, 4), "decode_ms": round(d_ms, 4)}
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     im_ms = float(np.mean(per["imatrix"]))
     im_bytes = T_ACT * C * 2 + T_ACT * 4 + 2 * C * 4
     hbm, hbm_src = measured_peaks()
     moe = measure_imatrix_moe(args, dev, flush, hbm)
     dec_large = measure_decode_large(args, dev, flush, hbm)
     lhs = measure_local_hessian(args, dev, flush)
+    moe_enc = measure_moe_expert_encode(args, dev, flush)
+    wb = measure_write_back(args, dev, flush, W, G, wbuf["w"][0])
+    large = measure_large_layers(args, dev, flush)
     for f in FORMATS:
-        pf[f]["decode_frac_hbm"] = round(pf[f]["decode_GB_s"] / hbm, 4)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        # the step's 46 MB fp32 output stays in L2: this is an L2-resident rate, not an HBM one
+        pf[f]["decode_note"] = "output L2-resident (46 MB < L2); the HBM-bound decode is decode_large"
+        pf[f]["encode_searched_frac_fp32"] = _encode_figures(f, R * C, pf[f]["encode_ms"], sms)["frac_fp32"]
+        pf[f]["encode_searched_frac_cuda_core_work"] = _encode_figures(f, R * C, pf[f]["encode_ms"], sms)["frac_cuda_core_work"]
     dom = max(FORMATS, key=lambda f: pf[f]["encode_ms"])
     dom_ms = pf[dom]["encode_ms"]
     achieved = R * C * flops_per_element(dom) / (dom_ms * 1e-3) / 1e12
@@ -362,14 +398,16 @@ def run_ours(args):
             "per_format": pf,
             "imatrix": {"ms": round(im_ms, 4), "GB_s": round(im_bytes / (im_ms * 1e-3) / 1e9, 1),
                         "frac_hbm": round(im_bytes / (im_ms * 1e-3) / 1e9 / hbm, 4)},
-            "imatrix_moe": moe, "decode_large": dec_large, "local_hessian": lhs, "hbm_peak_GB_s": hbm, "hbm_peak_source": hbm_src}
+            "imatrix_moe": moe, "decode_large": dec_large, "local_hessian": lhs, "moe_expert_encode": moe_enc,
+            "large_layer_encode": large, "write_back": wb, "hbm_peak_GB_s": hbm, "hbm_peak_source": hbm_src}
     print(json.dumps(line))
 
 
 def run_only(args, dev, fns, flush, stream):
     """One part of the step on its own (the profiling runs): --warmup untimed eager calls, then
     --steps calls each timed with CUDA events after an L2 flush.  Parts: imatrix, weights,
-    encode:<fmt>, fixed:<fmt>, decode:<fmt>, imatrix_moe, decode_large, local_hessian."""
+    encode:<fmt>, fixed:<fmt>, decode:<fmt>, imatrix_moe, decode_large, local_hessian,
+    moe_expert_encode, large_layer_encode."""
     import torch
     if args.only in ("imatrix_moe", "decode_large"):
         hbm, _ = measured_peaks()
@@ -379,8 +417,13 @@ def run_only(args, dev, fns, flush, stream):
     if args.only == "local_hessian":
         print(json.dumps({"only": args.only, **measure_local_hessian(args, dev, flush)}))
         return
+    if args.only in ("moe_expert_encode", "large_layer_encode"):
+        fn = measure_moe_expert_encode if args.only == "moe_expert_encode" else measure_large_layers
+        print(json.dumps({"only": args.only, **fn(args, dev, flush)}))
+        return
     if args.only not in fns:
-        raise SystemExit(f"--only: unknown part {args.only!r}; one of {sorted(fns) + ['imatrix_moe', 'decode_large', 'local_hessian']}")
+        extra = ['imatrix_moe', 'decode_large', 'local_hessian', 'moe_expert_encode', 'large_layer_encode']
+        raise SystemExit(f"--only: unknown part {args.only!r}; one of {sorted(fns) + extra}")
     fns["imatrix"]()
     fns["weights"]()
     fn = fns[args.only]
@@ -542,11 +585,139 @@ def measure_imatrix_moe(args, dev, flush, hbm):
             "tokens_per_expert_min_median_max": [int(counts.min()), int(np.median(counts)), int(counts.max())]}
 
 
+def _time_call(fn, args, flush, stream, fill):
+    """Median CUDA-event time (ms) of ``fn`` over max(3, steps) calls, L2 flushed before each."""
+    import torch
+    fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(max(3, args.steps)):
+        flush.fill_(fill)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return float(np.median(ts))
+
+
+def _encode_figures(fmt, nelem, ms, sms):
+    tf = nelem * flops_per_element(fmt) / (ms * 1e-3) / 1e12
+    tf_cc = nelem * cuda_core_flops_per_element(fmt) / (ms * 1e-3) / 1e12
+    peak = fp32_peak_tflops(sms, 2032.0)
+    return {"ms": round(ms, 4), "Melem_s": round(nelem / (ms * 1e-3) / 1e6, 1),
+            "frac_fp32": round(tf / peak, 4), "frac_cuda_core_work": round(tf_cc / peak, 4)}
+
+
+def measure_moe_expert_encode(args, dev, flush):
+    """MoE expert encode: 128 experts x a fused gate/up weight [1536, 2048] bf16 (Student-t nu=4 x
+    0.02) in one call per format (rows_per_expert 1536), each expert weighted by its own imatrix
+    slice from 4096 routed tokens (top-8 of a Zipf(1.2) router with 8 idle experts, whose weight
+    is 1), searched choices."""
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api, synth
+    xs, _ = synth.as_dtype(synth.activations(T_ACT, EXP_C, seed=3), "bf16")
+    ids = torch.from_numpy(synth.router(T_ACT, EXP_E, 8, seed=3)).to(dev)
+    X = torch.from_numpy(np.ascontiguousarray(xs).view(np.int16)).view(torch.bfloat16).to(dev)
+    s2, cn = api.imatrix_accumulate(X, ids, EXP_E)
+    w = api.imatrix_weights(s2, cn)
+    del X
+    store, _ = synth.as_dtype(synth.weight_t4(EXP_E * EXP_R, EXP_C, seed=3), "bf16")
+    W = torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    nelem = EXP_E * EXP_R * EXP_C
+    out = {"workload": f"{EXP_E} experts x [{EXP_R}, {EXP_C}] bf16, per-expert importance, searched"}
+    for f in ("IQ2_XXS", "IQ1_M"):
+        g = torch.from_numpy(synth.grid(f)).to(dev)
+        ws = api.encode_workspace(f, EXP_E * EXP_R, EXP_C, dev)
+        pay = api.encode(f, W, g, importance=w, rows_per_expert=EXP_R, workspace=ws)
+        ms = _time_call(lambda: api.encode(f, W, g, importance=w, rows_per_expert=EXP_R, payload=pay, workspace=ws),
+                        args, flush, stream, 6)
+        out[f] = _encode_figures(f, nelem, ms, sms)
+    return out
+
+
+def measure_large_layers(args, dev, flush):
+    """Large-layer encode: [17408, 5120] and [5120, 17408] bf16 weights (Student-t nu=4 x 0.02) in
+    all five formats, searched, with the every-choice error table written next to the payload;
+    importance from 4096 log-normal-scaled activations."""
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api, synth
+    stream = torch.cuda.current_stream(dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    out = {}
+    for (r, c) in LARGE_SHAPES:
+        xs, _ = synth.as_dtype(synth.activations(T_ACT, c, seed=4), "bf16")
+        X = torch.from_numpy(np.ascontiguousarray(xs).view(np.int16)).view(torch.bfloat16).to(dev)
+        s2, cn = api.imatrix_accumulate(X, torch.zeros(T_ACT, 1, dtype=torch.int32, device=dev), 1)
+        w = api.imatrix_weights(s2, cn)[0]
+        del X
+        store, _ = synth.as_dtype(synth.weight_t4(r, c, seed=4), "bf16")
+        W = torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(dev)
+        key = f"{r}x{c}"
+        out[key] = {}
+        for f in FORMATS:
+            g = torch.from_numpy(synth.grid(f)).to(dev)
+            ws = api.encode_workspace(f, r, c, dev)
+            pay, tbl = api.encode(f, W, g, importance=w, every_choice=True, workspace=ws)
+            ms = _time_call(lambda: api.encode(f, W, g, importance=w, payload=pay, table=tbl, every_choice=True,
+                                               workspace=ws), args, flush, stream, 7)
+            out[key][f] = _encode_figures(f, r * c, ms, sms)
+            out[key][f]["table_MB"] = round(tbl.numel() * 4 / 1e6, 1)
+            del pay, tbl, ws
+        del W
+        torch.cuda.empty_cache()
+    return out
+
+
+def measure_write_back(args, dev, flush, W0, G, w):
+    """Encode with write-back of the decoded weight (one call, fused) against a separate encode and
+    decode, on the step's 5632 x 2048 bf16 weight with its importance (searched choices).  W is
+    restored from a copy before each timed call, outside the timed region."""
+    import torch
+
+    from ggml_iq_codebook_accumulate_b300 import api
+    stream = torch.cuda.current_stream(dev)
+    Wt = torch.empty_like(W0)
+    out = {}
+    for f in FORMATS:
+        ws = api.encode_workspace(f, R, C, dev)
+        pay = api.encode(f, W0, G[f], importance=w, workspace=ws)
+        dec = torch.empty_like(W0)
+
+        def fused():
+            api.encode_write_back(f, Wt, G[f], importance=w, payload=pay, workspace=ws)
+
+        def separate():
+            api.encode(f, Wt, G[f], importance=w, payload=pay, workspace=ws)
+            api.decode(f, pay, R, C, G[f], out=dec)
+
+        res = {}
+        for name, fn in (("fused_ms", fused), ("encode_then_decode_ms", separate)):
+            ts = []
+            for _ in range(max(3, args.steps) + 1):
+                Wt.copy_(W0)
+                flush.fill_(8)
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                fn()
+                b.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a.elapsed_time(b))
+            res[name] = round(float(np.median(ts[1:])), 4)
+        out[f] = res
+    return out
+
+
 def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
     """The same step through the public API with host inputs: pinned host -> device copies of the
-    weight and activations, and device -> host copies of the five searched payloads, timed.  Each
-    payload's copy runs on a second stream while the next format is encoded; the step ends when
-    both streams are done."""
+    weight and activations, and device -> host copies of the five searched payloads and their
+    every-choice error tables, timed.  Each format's copies run on a second stream while the next
+    format is encoded; the step ends when both streams are done."""
     import torch
 
     from ggml_iq_codebook_accumulate_b300 import api
@@ -554,6 +725,8 @@ def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
     Xh = torch.from_numpy(np.ascontiguousarray(Xst).view(np.int16)).view(torch.bfloat16).pin_memory()
     B = R * C // 256
     outs = {f: torch.empty(B, info[f]["block_bytes"], dtype=torch.uint8).pin_memory() for f in FORMATS}
+    touts = {f: torch.empty(B, info[f]["choice_groups"], info[f]["num_choices"], dtype=torch.float32).pin_memory()
+             for f in FORMATS}
     W = torch.empty(R, C, dtype=torch.bfloat16, device=dev)
     X = torch.empty(T_ACT, C, dtype=torch.bfloat16, device=dev)
     ch7 = {f: torch.full((B, info[f]["choice_groups"]), 7, dtype=torch.uint8, device=dev) for f in FORMATS}
@@ -571,7 +744,9 @@ def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
             copier.wait_stream(compute)               # the payload is complete
             with torch.cuda.stream(copier):
                 outs[f].copy_(p, non_blocking=True)
+                touts[f].copy_(t, non_blocking=True)
             p.record_stream(copier)                   # not reused before its copy is done
+            t.record_stream(copier)
             api.encode(f, W, G[f], importance=w[0], choices=ch7[f])
             api.decode(f, p, R, C, G[f])
         compute.synchronize()
@@ -585,7 +760,7 @@ def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
         step()
     dt = (time.perf_counter() - t0) / n
     h2d = Wh.numel() * 2 + Xh.numel() * 2
-    d2h = sum(o.numel() for o in outs.values())
+    d2h = sum(o.numel() for o in outs.values()) + sum(t.numel() * 4 for t in touts.values())
     return {"value": round(5 * R * C / dt / 1e6, 2), "unit": "M elem/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3)}
 

@@ -65,11 +65,57 @@ struct EncArgs {
   float *table;
   int32_t *status;
   int uniform_choice;
+  void *wb;  // write-back: W (same dtype) overwritten with the decoded payload, or null
 };
 
 // the fixed choice of group g of block b
 template <int G> __device__ __forceinline__ int fixed_choice(const EncArgs &a, int64_t b, int g) {
   return a.choices ? (int)a.choices[b * G + g] : a.uniform_choice;
+}
+
+// Write-back of one vector (lane `lane` of block b): its 8 decoded values by the value rule
+// (IQ2 q = d (2s+1)/8 g, negated where sign bit i is set; IQ1 q = d (2s+1) (g + delta)), stored in
+// W's dtype (fp32 exact: every decoded value is an exact fp32 product; bf16 rounded to nearest
+// even).  g8: the entry's 8 codebook values.  Zero scale or a rejected block: d = 0 gives zeros.
+__device__ __forceinline__ void store8(float *o, const float *q) {
+  reinterpret_cast<float4 *>(o)[0] = make_float4(q[0], q[1], q[2], q[3]);
+  reinterpret_cast<float4 *>(o)[1] = make_float4(q[4], q[5], q[6], q[7]);
+}
+__device__ __forceinline__ void store8(__nv_bfloat16 *o, const float *q) {
+  uint32_t u[4];
+#pragma unroll
+  for (int k = 0; k < 4; k++) {
+    const __nv_bfloat162 h2 = __floats2bfloat162_rn(q[2 * k], q[2 * k + 1]);
+    u[k] = *reinterpret_cast<const uint32_t *>(&h2);
+  }
+  *reinterpret_cast<uint4 *>(o) = make_uint4(u[0], u[1], u[2], u[3]);
+}
+template <int F, typename TIn>
+__device__ __forceinline__ void write_back_vec(const EncArgs &a, int64_t b, int lane, const float *g8, float d, int s,
+                                               int sgn, int dbit) {
+  float q[8];
+  if (!Fmt<F>::IQ1) {
+    const float dl = __fmul_rn(__fmul_rn(d, (float)(2 * s + 1)), 0.125f);
+#pragma unroll
+    for (int i = 0; i < 8; i++) {
+      const float v = __fmul_rn(dl, g8[i]);
+      q[i] = ((sgn >> i) & 1) ? -v : v;
+    }
+  } else {
+    const float dl = __fmul_rn(d, (float)(2 * s + 1));
+    const float delta = dbit ? -0.125f : 0.125f;
+#pragma unroll
+    for (int i = 0; i < 8; i++) q[i] = __fmul_rn(dl, __fadd_rn(g8[i], delta));
+  }
+  const int64_t bpr = a.cols / 256;
+  TIn *W = reinterpret_cast<TIn *>(a.wb);
+  store8(W + (b / bpr) * a.cols + (b % bpr) * 256 + lane * 8, q);
+}
+template <typename TIn>
+__device__ __forceinline__ void write_back_zero(const EncArgs &a, int64_t b, int lane) {
+  const float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const int64_t bpr = a.cols / 256;
+  store8(reinterpret_cast<TIn *>(a.wb) + (b / bpr) * a.cols + (b % bpr) * 256 + lane * 8, q);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -302,11 +348,13 @@ __device__ __forceinline__ float group_sum(float val, int g0) {
 // product of a [128 x 8] per-vector operand and the [8 x N] codebook:
 //     An = -2 (w t) . g        B = w . h (h = g^2 or |g|)        Cg = w . g (IQ1)
 // evaluated by tcgen05.mma (kind::tf32, fp32 accumulators in tensor memory), 64 codebook entries
-// per chunk.  The codebook values are small integers, exact in tf32; each fp32 per-vector operand
-// is split into two tf32 parts (hi, lo = x - hi, each rounded to tf32) accumulated into the same
-// tensor-memory column: every product of a part is exact, the split leaves at most 2^-22 of each
-// operand, and the sums carry the accumulation rounding (together measured on B300 at most 6.3
-// units of 2^-24 of sum |a*b|, inside the same rounding margin as an fp32 FMA chain).
+// per chunk.  The codebook values g (integers of at most 7 bits) are exact in tf32; h = g^2 of
+// an IQ2 grid can need 14 bits, so it is split into exact tf32 parts hi + lo when any entry needs
+// it (two more MMAs for B).  Each fp32 per-vector operand is split into two tf32 parts (hi, lo =
+// x - hi, each rounded to tf32) accumulated into the same tensor-memory column: every product of
+// a part is exact, the split leaves at most 2^-22 of each operand, and the sums carry the
+// accumulation rounding (together measured on B300 at most 6.3 units of 2^-24 of sum |a*b|,
+// inside the same rounding margin as an fp32 FMA chain).
 // A control warp issues the MMAs into a double-buffered tensor-memory region and commits each
 // chunk to an mbarrier; 8 consumer warps (2 per tensor-memory lane quarter = block) load their 32
 // columns per chunk with tcgen05.ld and do the per-choice scoring with packed f32x2 FMAs and
@@ -376,8 +424,10 @@ template <int F> struct TcCfg {
   static constexpr int NQ = Fmt<F>::IQ1 ? 3 : 2;       // An, (Cg), B columns per entry
   static constexpr int NCH = Fmt<F>::N / kChunk;        // chunks per sweep
   static constexpr int ALLOC = 2 * NQ * kChunk <= 256 ? 256 : 512;  // tensor-memory columns
+  // IQ2: h = g^2 may need more significant bits than tf32 holds; its low part goes here
+  static constexpr size_t HLO = Fmt<F>::IQ1 ? 0 : (size_t)Fmt<F>::N * 32;
   // shared memory besides the per-vector operands (tc_na below, 4 KB each)
-  static constexpr size_t SMEM = (size_t)Fmt<F>::N * 64 + 2 * 128 * 16 * 4 + 2 * 128 * 4 * 4 + 4 * 24 * 4;
+  static constexpr size_t SMEM = (size_t)Fmt<F>::N * 64 + HLO + 2 * 128 * 16 * 4 + 2 * 128 * 4 * 4 + 4 * 24 * 4;
   // every-choice payloads: per (warp half, vector, choice) the minimum, the near bound (fp32) and
   // key | count << 16
   static constexpr size_t EVERY = 2 * 128 * 16 * 4 * 3;
@@ -407,8 +457,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   constexpr uint32_t IDESC = umma_idesc<kChunk>();
   extern __shared__ __align__(1024) uint8_t smem[];
   float *cb = reinterpret_cast<float *>(smem);              // codebook g [N x 8], then h [N x 8]
+  float *hlo = cb + (size_t)N * 16;                         // IQ2: low tf32 part of h [N x 8]
   constexpr int NA = tc_na<F, MODE>();
-  float *aop = cb + (size_t)N * 16;                         // [NA][128 x 8] per-vector operands
+  float *aop = hlo + TcCfg<F>::HLO / 4;                     // [NA][128 x 8] per-vector operands
   float *xchg = aop + NA * 1024;                            // [2][128][16] per-choice minima
   float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
   uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
@@ -444,6 +495,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   const bool ok = grid_bad || load_codebook(reinterpret_cast<float4 *>(cb), ws.tab, N * 64, &cb_bar);
   if (grid_bad && blockIdx.x == 0 && threadIdx.x == 0 && a.status) atomicOr(a.status, IQ_STATUS_BAD_GRID);
   __syncthreads();
+  // IQ2 codebooks: h = g^2 has up to 14 significant bits (values up to 127), tf32 holds 11.  Each
+  // h becomes hi = rna_tf32(h) in place plus lo = h - hi (an integer of at most 4 significant
+  // bits), both exact in tf32; when some h needs the low part, B = w . hi + w . lo takes two more
+  // MMAs per chunk, so the codebook operand stays exact for every accepted grid.
+  bool hsplit = false;
+  if constexpr (!Fmt<F>::IQ1) {
+    bool inexact = false;
+    if (ok && !grid_bad) {
+      float *hs = cb + (size_t)N * 8;
+      for (int i = threadIdx.x; i < N * 8; i += blockDim.x) {
+        const float h = hs[i], hh = tf32_rna(h);
+        inexact |= hh != h;
+        hs[i] = hh;
+        hlo[i] = __fsub_rn(h, hh);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    hsplit = __syncthreads_or(inexact) != 0;
+  }
 
   constexpr bool kOpSync = F == IQ1_S && MODE == MODE_SEARCH;  // operands written between the sweeps
   const int g0 = lane & ~(VPG - 1);
@@ -486,6 +556,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
             for (int i = lane; i < BB; i += 32) a.payload[((size_t)c * a.nblocks + b) * BB + i] = 0;
         } else if (MODE != MODE_TABLE) {
           for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = 0;
+          if (a.wb) write_back_zero<TIn>(a, b, lane);
         }
         if (a.table && MODE != MODE_FIXED) {
           float cs = 0.0f;
@@ -531,7 +602,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       // ---- MMA issue: sweep 1 (unless fixed choices) and sweep 2 (unless table only) ---------
       if (lane == 0) {
         const int nsweeps = (MODE != MODE_FIXED) + (MODE != MODE_TABLE);
-        const uint32_t sa = smem_u32(aop), sg = smem_u32(cb), sh = sg + N * 32;
+        const uint32_t sa = smem_u32(aop), sg = smem_u32(cb), sh = sg + N * 32, shl = smem_u32(hlo);
         for (int sw = 0; sw < nsweeps; sw++) {
           for (int ch = 0; ch < NCH; ch++, issued++) {
             const uint32_t buf = issued & 1;
@@ -567,6 +638,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
               }
               umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // B = w . h
               umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+              if (!Fmt<F>::IQ1 && hsplit) {                                             //   + w . h lo
+                const uint64_t bl = umma_desc(shl + ch * kChunk * 32);
+                umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bl, IDESC, 1);
+                umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bl, IDESC, 1);
+              }
             }
             umma_commit(&full_bar[buf]);
           }
@@ -977,6 +1053,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           const int slot = atomicAdd(&ws.hdr[1], 1);
           ws.fb[slot] = make_uint2((uint32_t)b, flags);
         }
+        // write-back: a block left to the exact rescoring is written by it, after its final
+        // decisions (it reads the block's weight first)
+        if (a.wb && !flags) {
+          float g8[8];
+#pragma unroll
+          for (int i = 0; i < 8; i++) g8[i] = cb[kmaj(idx, i)];
+          write_back_vec<F, TIn>(a, b, lane, g8, d, F == IQ1_S ? (c1 & 7) : c1, v.sgn,
+                                 F == IQ1_S ? (c1 >> 3) : F == IQ1_M ? key / N : 0);
+        }
       }
     }
   }
@@ -1054,6 +1139,30 @@ __device__ __forceinline__ void cand_of_choice(int c, int &s, int &db0, int &db1
   if (F == IQ1_S) { s = c & 7; db0 = db1 = c >> 3; }
   else if (F == IQ1_M) { s = c; db0 = 0; db1 = 1; }
   else { s = c; db0 = db1 = 0; }
+}
+
+// Write-back of a rescored block from its final payload bytes (one warp; lane = vector), with the
+// codebook values from the prepared table.
+template <int F, typename TIn>
+__device__ __forceinline__ void write_back_bytes(const EncArgs &a, const float4 *tab, int64_t b, int lane,
+                                                 const uint8_t *pbytes, float d) {
+  constexpr int VPG = Fmt<F>::VPG;
+  const int cg = lane / VPG;
+  const int s = (int)get_bits(pbytes, f_scale<F>(cg));
+  const Bits lo = f_idx_lo<F>(lane);
+  const int idx = (int)(get_bits(pbytes, lo) | (get_bits(pbytes, f_idx_hi<F>(lane)) << lo.width));
+  int sgn = 0, dbit = 0;
+  if (!Fmt<F>::IQ1) {
+    sgn = (int)get_bits(pbytes, f_sign<F>(lane));
+    if (Fmt<F>::PAR) sgn |= parity7(sgn) << 7;
+  } else {
+    dbit = F == IQ1_S ? (int)get_bits(pbytes, f_dbit_grp<F>(cg)) : (int)get_bits(pbytes, f_dbit_vec<F>(lane));
+  }
+  const float *tf = reinterpret_cast<const float *>(tab);
+  float g8[8];
+#pragma unroll
+  for (int i = 0; i < 8; i++) g8[i] = tf[kmaj(idx, i)];
+  write_back_vec<F, TIn>(a, b, lane, g8, d, s, sgn, dbit);
 }
 
 // Exact rescoring of the flagged items, in one of two layouts chosen by their number.
@@ -1258,6 +1367,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
       __syncthreads();
     }
     for (int i = threadIdx.x; i < BB; i += blockDim.x) payb[i] = pbytes[i];
+    if (a.wb && wid == 0) write_back_bytes<F, TIn>(a, tab, b, lane, pbytes, d);
     __syncthreads();  // the payload bytes are reused by the next item
   }
 }
@@ -1423,6 +1533,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       __syncwarp();
     }
     for (int i = lane; i < BB; i += 32) payb[i] = pbytes[i];
+    if (a.wb) write_back_bytes<F, TIn>(a, tab, b, lane, pbytes, d);
     __syncwarp();
    }
   }
@@ -1576,7 +1687,7 @@ extern "C" int iq_encode(iq_format f, const void *W, iq_dtype dt, int64_t rows, 
   size_t need = 0;
   iq_encode_workspace_size(f, rows, cols, &need);
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
-  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, choices, payload, group_errors, status, 0};
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, choices, payload, group_errors, status, 0, nullptr};
   cudaStream_t st = (cudaStream_t)stream;
   if (choices)
     return dt == IQ_BF16 ? dispatch_encode<MODE_FIXED, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
@@ -1587,15 +1698,27 @@ extern "C" int iq_encode(iq_format f, const void *W, iq_dtype dt, int64_t rows, 
 
 // Encode and write the decoded weight back ("Add imatrix calibration for the GGML formats ...",
 // What imatrix does: the encoder encodes each weight with its statistic, writes the decoded weight
-// back and pins the payload): iq_encode, then the decoder from the payload into W in W's dtype.
+// back and pins the payload), fused: the encoder writes each block's decoded values over W in its
+// epilogue, and the exact rescoring writes the blocks it re-decides after their final decisions,
+// so W is read once and the payload is not read back.
 extern "C" int iq_encode_write_back(iq_format f, void *W, iq_dtype dt, int64_t rows, int64_t cols,
                                     const float *importance, int64_t rows_per_expert, const float *grid,
                                     const uint16_t *d16, const uint8_t *choices, uint8_t *payload, int32_t *status,
                                     void *workspace, size_t workspace_bytes, void *stream) {
-  const int rc = iq_encode(f, W, dt, rows, cols, importance, rows_per_expert, grid, d16, choices, payload, nullptr,
-                           status, workspace, workspace_bytes, stream);
+  int rc = check_common(f, W, dt, rows, cols, importance, rows_per_expert, grid);
   if (rc) return rc;
-  return iq_decode(f, payload, rows, cols, grid, W, dt, stream);
+  const int64_t nb = rows * (cols / 256);
+  if (nb > 0 && !payload) return IQ_ERR_ARG;
+  size_t need = 0;
+  iq_encode_workspace_size(f, rows, cols, &need);
+  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, choices, payload, nullptr, status, 0, W};
+  cudaStream_t st = (cudaStream_t)stream;
+  if (choices)
+    return dt == IQ_BF16 ? dispatch_encode<MODE_FIXED, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
+                         : dispatch_encode<MODE_FIXED, float>(f, a, workspace, workspace_bytes, st);
+  return dt == IQ_BF16 ? dispatch_encode<MODE_SEARCH, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
+                       : dispatch_encode<MODE_SEARCH, float>(f, a, workspace, workspace_bytes, st);
 }
 
 extern "C" int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
@@ -1610,7 +1733,7 @@ extern "C" int iq_group_errors(iq_format f, const void *W, iq_dtype dt, int64_t 
   size_t need = 0;
   iq_encode_workspace_size(f, rows, cols, &need);
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
-  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, nullptr, group_errors, status, 0};
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, nullptr, group_errors, status, 0, nullptr};
   cudaStream_t st = (cudaStream_t)stream;
   return dt == IQ_BF16 ? dispatch_encode<MODE_TABLE, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
                        : dispatch_encode<MODE_TABLE, float>(f, a, workspace, workspace_bytes, st);
@@ -1635,7 +1758,7 @@ extern "C" int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, i
   iq_encode_workspace_size(f, rows * info.num_choices, cols, &need);  // a flag list entry per (block, choice)
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
-  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, payloads, nullptr, status, 0};
+  EncArgs a{W, rows, cols, nb, importance, rows_per_expert, grid, d16, nullptr, payloads, nullptr, status, 0, nullptr};
   return dt == IQ_BF16 ? dispatch_encode<MODE_EVERY, __nv_bfloat16>(f, a, workspace, workspace_bytes, st)
                        : dispatch_encode<MODE_EVERY, float>(f, a, workspace, workspace_bytes, st);
 }

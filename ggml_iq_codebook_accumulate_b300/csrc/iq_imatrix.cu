@@ -7,8 +7,9 @@
 //
 // Definition computed (bit for bit): for each chunk of rows_per_chunk tokens and each expert e the
 // chunk routes tokens to, partial[e][j] starts at +0 and, over those tokens in ascending order,
-// becomes fl(partial + x*x) -- the exact square added with one rounding; then in_sum2[e][j] =
-// fl(in_sum2[e][j] + partial[e][j]), chunk by chunk.
+// becomes fl(partial + fl(x*x)) -- the square rounded to fp32, then added with one more rounding
+// (for bf16 activations the square is exact, so this is the exact square added with one
+// rounding); then in_sum2[e][j] = fl(in_sum2[e][j] + partial[e][j]), chunk by chunk.
 //
 // Kernels per call:
 //  route       one CTA per (chunk, 128-row sub-tile): builds the sub-tile's expert bitmap in shared
@@ -238,9 +239,10 @@ __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   return v;
 }
 
-// acc[0..CPL) += x^2 for the CPL values of this lane (u: the lane's 8 bytes of one row), each exact
-// square added with one rounding.  For bf16 the mixed-precision FMA takes the two halves of a
-// 32-bit register directly (one instruction per value).
+// acc[0..CPL) += x^2 for the CPL values of this lane (u: the lane's 8 bytes of one row).  A bf16
+// value's square is exact in fp32, so the mixed-precision FMA (which takes the two halves of a
+// 32-bit register directly) rounds once, as fl(acc + fl(x*x)) does; fp32 values are squared with
+// one rounding and added with another.
 __device__ __forceinline__ void sq_acc(float *acc, uint2 u, __nv_bfloat16) {
   asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %4;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n"
       " mov.b32 {l, h}, %5;\n fma.rn.f32.bf16 %2, l, l, %2;\n fma.rn.f32.bf16 %3, h, h, %3;\n}\n"
@@ -249,8 +251,8 @@ __device__ __forceinline__ void sq_acc(float *acc, uint2 u, __nv_bfloat16) {
 }
 __device__ __forceinline__ void sq_acc(float *acc, uint2 u, float) {
   const float x0 = __uint_as_float(u.x), x1 = __uint_as_float(u.y);
-  acc[0] = __fmaf_rn(x0, x0, acc[0]);
-  acc[1] = __fmaf_rn(x1, x1, acc[1]);
+  acc[0] = __fadd_rn(acc[0], __fmul_rn(x0, x0));
+  acc[1] = __fadd_rn(acc[1], __fmul_rn(x1, x1));
 }
 // The 4 rows of a group: their offsets (4 x uint16) in one load, then the rows' values.
 struct Group { uint2 v0, v1, v2, v3; };

@@ -46,15 +46,20 @@ def as_dtype(x: np.ndarray, dtype: str):
     raise ValueError(dtype)
 
 
-def grid(fmt: str, seed: int | None = None) -> np.ndarray:
-    """Synthetic codebook [entries, 8] fp32 for ``fmt`` (seed defaults to 1000 + format index)."""
+def grid(fmt: str, seed: int | None = None, values=None) -> np.ndarray:
+    """Synthetic codebook [entries, 8] fp32 for ``fmt`` (seed defaults to 1000 + format index):
+    distinct 8-vectors over ``values`` (default: the format's value set), drawn without
+    replacement."""
     n = GRID_ENTRIES[fmt]
     if seed is None:
         seed = 1000 + FORMATS.index(fmt)
+    if values is None:
+        values = IQ1_VALUES if fmt.startswith("IQ1") else IQ2_VALUES
+    vals = np.array(values, np.float32)
+    m = len(vals)
     rng = np.random.default_rng(seed)
-    codes = rng.choice(3 ** 8, size=n, replace=False)
-    digits = np.stack([(codes // 3 ** i) % 3 for i in range(8)], axis=1)
-    vals = np.array(IQ1_VALUES if fmt.startswith("IQ1") else IQ2_VALUES, np.float32)
+    codes = rng.choice(m ** 8, size=n, replace=False)
+    digits = np.stack([(codes // m ** i) % m for i in range(8)], axis=1)
     return vals[digits].astype(np.float32)
 
 

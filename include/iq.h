@@ -102,8 +102,9 @@ IQ_API int iq_format_info(iq_format f, iq_format_info_t *out);
 /* ---- imatrix ([imatrix] "What imatrix does", Bounded memory; [coverage] Facts) ----------------
  * For each chunk of `rows_per_chunk` consecutive tokens (1,024 on the pages) and each expert e the
  * chunk routes tokens to: partial[e][j] starts at +0 and, over the chunk's tokens whose top-k ids
- * contain e in ascending token order, becomes fl(partial + x[t][j]*x[t][j]) -- the exact square
- * added with ONE rounding (a fused multiply-add); then in_sum2[e][j] = fl(in_sum2[e][j] +
+ * contain e in ascending token order, becomes fl(partial + fl(x[t][j]*x[t][j])) -- the square
+ * rounded to fp32 (exact for bf16 activations), then added with one more rounding (no fused
+ * multiply-add for fp32 activations); then in_sum2[e][j] = fl(in_sum2[e][j] +
  * partial[e][j]) (chunk order) and counts[e] += tokens routed to e.  A token's ids are a set (a
  * repeated id counts once and sets IQ_STATUS_DUP_EXPERT_ID; an id outside [0, num_experts) is
  * skipped and sets IQ_STATUS_BAD_EXPERT_ID).  After the call, a non-finite in_sum2 value of an

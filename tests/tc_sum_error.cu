@@ -6,6 +6,9 @@
 //   plain sums     a . b over 8 terms (2 MMAs), a signed or positive, b one of the codebook
 //                  operand kinds: g^2 of {8, 25, 43}, {8, 25, 43}, ternary, |ternary|
 //   deferred sums  w . h + sig (w/4) . g over 8 + 8 terms (4 MMAs), w >= 0, g ternary, h = |g|
+//   split sums     a . h with h = g^2 of integers g up to 127 (up to 14 significant bits) split
+//                  into exact tf32 parts hi + lo: a hi . h hi + a lo . h hi + a hi . h lo +
+//                  a lo . h lo (4 MMAs)
 // Each result is compared with the exact value in fp64; the program prints the worst
 // |D - exact| / sum |terms| in units u = 2^-24 per operand kind.  All waits are bounded.
 #include <cstdio>
@@ -46,7 +49,7 @@ __device__ __forceinline__ uint64_t sdesc(const void *base, uint32_t lbo, uint32
 }
 
 __global__ void __launch_bounds__(128, 1) probe(const float *A, const float *B, const float *B2, float *D, int nsplit,
-                                                int *err, uint32_t lbo, uint32_t sbo, float sig) {
+                                                int *err, uint32_t lbo, uint32_t sbo, float sig, int hsplit) {
   __shared__ __align__(1024) float sA[4][M * K];   // w hi, w lo, sig w/4 hi, sig w/4 lo
   __shared__ __align__(1024) float sB[2][N * K];    // h, g
   __shared__ uint64_t mbar;
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(128, 1) probe(const float *A, const float *B, 
   if (tid == 0) {
     for (int s = 0; s < nsplit; s++) {
       const uint64_t bdesc = sdesc(sB[s < 2 ? 0 : 1], lbo, sbo);
-      const uint64_t adesc = sdesc(sA[s], lbo, sbo);
+      const uint64_t adesc = sdesc(sA[hsplit ? (s & 1) : s], lbo, sbo);
       const uint32_t acc = s > 0;
       asm volatile("{ .reg .pred p; setp.ne.u32 p, %4, 0; tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p; }"
                    ::"r"(tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc) : "memory");
@@ -130,12 +133,12 @@ int main() {
   float *dA, *dH, *dG, *dD; int *derr;
   cudaMalloc(&dA, A.size() * 4); cudaMalloc(&dH, H.size() * 4); cudaMalloc(&dG, Gv.size() * 4);
   cudaMalloc(&dD, D.size() * 4); cudaMalloc(&derr, 4);
-  auto launch = [&](int nsplit, float sig) -> bool {
+  auto launch = [&](int nsplit, float sig, int hsplit = 0) -> bool {
     cudaMemcpy(dA, A.data(), A.size() * 4, cudaMemcpyHostToDevice);
     cudaMemcpy(dH, H.data(), H.size() * 4, cudaMemcpyHostToDevice);
     cudaMemcpy(dG, Gv.data(), Gv.size() * 4, cudaMemcpyHostToDevice);
     cudaMemset(derr, 0, 4); cudaMemset(dD, 0, D.size() * 4);
-    probe<<<1, 128>>>(dA, dH, dG, dD, nsplit, derr, 128, 256, sig);
+    probe<<<1, 128>>>(dA, dH, dG, dD, nsplit, derr, 128, 256, sig, hsplit);
     cudaError_t e = cudaDeviceSynchronize();
     int herr = 0; cudaMemcpy(&herr, derr, 4, cudaMemcpyDeviceToHost);
     if (e != cudaSuccess || herr) { printf("error %s timeout=%d\n", cudaGetErrorString(e), herr); return false; }
@@ -196,5 +199,40 @@ int main() {
   }
   printf("deferred plus %.3f\n", dfr[0]);
   printf("deferred minus %.3f\n", dfr[1]);
+  // split sums: h = g^2 for integers g in [1, 127] (a third of them 47, 101 or 127), as hi + lo
+  std::uniform_int_distribution<int> gd(1, 127), pick(0, 5);
+  const int wide[3] = {47, 101, 127};
+  auto tf32_host = [](float x) {  // round to nearest (ties away), 10 explicit mantissa bits
+    uint32_t b; std::memcpy(&b, &x, 4); b = (b + 0x1000u) & ~0x1fffu; std::memcpy(&x, &b, 4); return x;
+  };
+  double spl = 0;
+  std::vector<double> Hx(N * K);
+  for (int trial = 0; trial < 160; trial++) {
+    const int ak = trial % 4;
+    for (int m = 0; m < M; m++)
+      for (int k = 0; k < K; k++) {
+        float a;
+        if (ak == 0) a = nd(rng) * std::exp(nd(rng));
+        else if (ak == 1) a = std::exp(3.0f * nd(rng));
+        else if (ak == 2) { const float b = std::exp(nd(rng)); a = (k & 1) ? -A[m * K + k - 1] * (1.0f + 1e-3f * nd(rng)) : b; }
+        else a = 1.0f + std::fabs(nd(rng)) * 0.3f;
+        A[m * K + k] = a;
+      }
+    for (int i = 0; i < N * K; i++) {
+      const int p = pick(rng);
+      const int g = p < 2 ? wide[p] : p == 2 ? 127 : gd(rng);
+      const float h = (float)(g * g), hi = tf32_host(h);
+      H[i] = hi; Gv[i] = h - hi; Hx[i] = (double)g * g;
+    }
+    if (!launch(4, 1.0f, 1)) return 1;
+    for (int m = 0; m < M; m++)
+      for (int n = 0; n < N; n++) {
+        double e = 0, s = 0;
+        for (int k = 0; k < K; k++) { const double t = (double)A[m * K + k] * Hx[n * K + k]; e += t; s += std::fabs(t); }
+        ex[m * N + n] = e; ab[m * N + n] = s;
+      }
+    spl = std::max(spl, worst_of(D, ex, ab));
+  }
+  printf("split g2wide %.3f\n", spl);
   return 0;
 }

@@ -28,6 +28,7 @@ def test_reference_arm_prints_one_contract_line():
     assert d["higher_is_better"] is True and d["scaling"] == "weak" and d["data"] == "synthetic"
     assert d["steps"] == 1 and d["warmup"] == 0 and d["n_gpus"] == 1
     assert "workload" in d["config"]
+    assert "CUDA" not in json.dumps(d["config"]) and "L2" not in json.dumps(d["config"])   # a CPU run
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["unit"] == d["unit"] and cb["cores"] >= 1
     assert "8 of 5632 rows" in cb["sample"]

@@ -7,6 +7,7 @@ import torch
 import oracle
 from oracle import imatrix_tools as it
 from ggml_iq_codebook_accumulate_b300 import api, synth
+from parity import check_payload
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -47,25 +48,43 @@ def test_neutral_entries_and_coverage():
     assert tuple(api.imatrix_coverage(cn).cpu().tolist()) == (40, 1500 * 4 + 7, 1, ref_cov[3])
 
 
-@pytest.mark.parametrize("fmt", ["IQ2_XXS", "IQ2_S", "IQ1_M"])
+@pytest.mark.parametrize("fmt", synth.FORMATS)
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_encode_write_back(fmt, dtype):
-    """W is overwritten with the decoded payload: exact in fp32, rounded to nearest even in bf16."""
+    """The fused write-back: the payload is the oracle's encode of the original W (byte-identical),
+    and W is overwritten with its decode (exact in fp32, rounded to nearest even in bf16), for
+    searched and for fixed choices; a zero block and a block with a non-finite value decode to
+    zeros."""
     R, C = 24, 768
-    store, wv = synth.as_dtype(synth.weight_t4(R, C, seed=44), dtype)
-    if dtype == "bf16":
-        W = torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(DEV)
-    else:
-        W = torch.from_numpy(np.ascontiguousarray(store)).to(DEV)
+    x = synth.weight_t4(R, C, seed=44)
+    x[3, 256:512] = 0.0                                     # zero-scale block
+    x[5, 7] = np.nan                                        # rejected block (non-finite value)
+    store, wv = synth.as_dtype(x, dtype)
     grid = synth.grid(fmt)
     g = torch.from_numpy(grid).to(DEV)
-    imp = torch.rand(C, device=DEV) + 0.5
-    ref_pay = api.encode(fmt, W, g, importance=imp)
-    pay = api.encode_write_back(fmt, W, g, importance=imp)
-    assert torch.equal(pay, ref_pay)
-    q = oracle.decode(fmt, pay.cpu().numpy(), R, C, grid)
-    if dtype == "f32":
-        assert np.array_equal(W.cpu().numpy().view(np.uint32), q.view(np.uint32))
-    else:
-        ref = torch.from_numpy(q).to(torch.bfloat16)           # round to nearest even (CPU conversion)
-        assert torch.equal(W.cpu().view(torch.int16), ref.view(torch.int16))
+    imp_np = (np.random.default_rng(45).random(C) + 0.5).astype(np.float32)
+    imp = torch.from_numpy(imp_np).to(DEV)
+    info = oracle.format_info(fmt)
+    ch = np.random.default_rng(46).integers(0, info["num_choices"], (R * C // 256, info["groups"])).astype(np.uint8)
+    for choices in (None, ch):
+        if dtype == "bf16":
+            W = torch.from_numpy(np.ascontiguousarray(store).view(np.int16)).view(torch.bfloat16).to(DEV)
+        else:
+            W = torch.from_numpy(np.ascontiguousarray(store)).to(DEV)
+        st = torch.zeros(1, dtype=torch.int32, device=DEV)
+        pay = api.encode_write_back(fmt, W, g, importance=imp, status=st,
+                                    choices=None if choices is None else torch.from_numpy(choices).to(DEV))
+        p_orc, st_orc, det = oracle.encode(fmt, wv, grid, importance=imp_np, choices=choices, details=True)
+        assert int(st.item()) == st_orc == oracle.ST_BAD_INPUT
+        ph = pay.cpu().numpy()
+        if choices is None:
+            assert check_payload(fmt, wv, grid, ph, p_orc, det, importance=imp_np) == 0
+        else:
+            assert np.array_equal(ph, p_orc)
+        q = oracle.decode(fmt, ph, R, C, grid)
+        assert not q[3, 256:512].any() and not q[5, :256].any()
+        if dtype == "f32":
+            assert np.array_equal(W.cpu().numpy().view(np.uint32), q.view(np.uint32))
+        else:
+            ref = torch.from_numpy(q).to(torch.bfloat16)           # round to nearest even (CPU conversion)
+            assert torch.equal(W.cpu().view(torch.int16), ref.view(torch.int16))

@@ -121,14 +121,20 @@ def _signs(fmt, x, w):
     return m
 
 
-@pytest.mark.parametrize("fmt", FORMATS)
-def test_search_brute_force_whole_groups(orc, fmt):
+WIDE_IQ2_VALUES = (8.0, 25.0, 43.0, 47.0, 101.0, 127.0)   # squares up to 14 significant bits
+
+
+@pytest.mark.parametrize("fmt,values", [(f, None) for f in FORMATS] +
+                         [(f, WIDE_IQ2_VALUES) for f in ("IQ2_XXS", "IQ2_XS", "IQ2_S")])
+def test_search_brute_force_whole_groups(orc, fmt, values):
     """Tiny codebooks (first 3 entries): enumerate every (choice, entry per vector[, delta per
     vector]) assignment of a choice group, score each by decode + fp64 error, and check that the
-    oracle's group error is the minimum and its payload decodes to a minimising assignment."""
+    oracle's group error is the minimum and its payload decodes to a minimising assignment.  The
+    IQ2 formats also run on a grid over a wider value set (up to 127, the largest the formats'
+    integer codebooks accept)."""
     info = orc.format_info(fmt)
     n_e = 3
-    grid = synth.grid(fmt)
+    grid = synth.grid(fmt, values=values, seed=None if values is None else 77)
     rng = np.random.default_rng(FORMATS.index(fmt))
     W = synth.weight_t4(2, 256, seed=30 + FORMATS.index(fmt))
     imp = np.exp(rng.standard_normal(256)).astype(np.float32)
