@@ -111,11 +111,14 @@ __device__ __forceinline__ void write_back_vec(const EncArgs &a, int64_t b, int 
   TIn *W = reinterpret_cast<TIn *>(a.wb);
   store8(W + (b / bpr) * a.cols + (b % bpr) * 256 + lane * 8, q);
 }
-template <typename TIn>
+// Write-back of a rejected or zero-scale block: the decode of its all-zero payload (scale 0, entry
+// 0, choice 0, no signs, delta bit 0), whose values are zeros carrying the sign of entry 0's
+// values (+- 0 for IQ1, where g + delta can be negative).
+template <int F, typename TIn>
 __device__ __forceinline__ void write_back_zero(const EncArgs &a, int64_t b, int lane) {
-  const float q[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  const int64_t bpr = a.cols / 256;
-  store8(reinterpret_cast<TIn *>(a.wb) + (b / bpr) * a.cols + (b % bpr) * 256 + lane * 8, q);
+  float g8[8];
+  load8(a.grid, g8);
+  write_back_vec<F, TIn>(a, b, lane, g8, 0.0f, 0, 0, 0);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -310,9 +313,11 @@ __device__ __forceinline__ void load_block_vec(const EncArgs &a, int64_t b, int 
   }
 }
 
-// Validates the block and returns its scale bits; 0 means "write an all-zero payload".
+// Validates the block and returns its scale bits; 0 means "write an all-zero payload".  d16in: the
+// given scale bits of the block (read ahead), or -1 to compute the anchor; cin: lane g < G holds the
+// fixed choice of group g (read ahead; fixed-choice mode).
 template <int F, int MODE>
-__device__ __forceinline__ uint32_t block_scale(const EncArgs &a, int64_t b, int lane, const Vec &v, int &bad_bits) {
+__device__ __forceinline__ uint32_t block_scale(const Vec &v, int lane, int d16in, int cin, int &bad_bits) {
   constexpr int G = Fmt<F>::G, C = Fmt<F>::C;
   bad_bits = 0;
   bool fin = finite8(v.x);
@@ -322,12 +327,11 @@ __device__ __forceinline__ uint32_t block_scale(const EncArgs &a, int64_t b, int
   if (!__all_sync(0xffffffffu, fin)) bad_bits |= IQ_STATUS_BAD_INPUT;
   else if (!__all_sync(0xffffffffu, wok)) bad_bits |= IQ_STATUS_BAD_IMPORTANCE;
   if (bad_bits) return 0;
-  uint32_t d16 = a.d16 ? (uint32_t)a.d16[b] : (uint32_t)half_bits_rn(anchor_scale<F>(v.x));
+  uint32_t d16 = d16in >= 0 ? (uint32_t)d16in : (uint32_t)half_bits_rn(anchor_scale<F>(v.x));
   if ((d16 & 0x7c00u) == 0x7c00u || ((d16 & 0x8000u) && (d16 & 0x7fffu))) { bad_bits |= IQ_STATUS_BAD_SCALE; return 0; }
   d16 &= 0x7fffu;
   if (MODE == MODE_FIXED) {
-    const int c = lane < G ? fixed_choice<G>(a, b, lane) : 0;
-    if (__any_sync(0xffffffffu, c >= C)) { bad_bits |= IQ_STATUS_BAD_CHOICE; return 0; }
+    if (__any_sync(0xffffffffu, lane < G && cin >= C)) { bad_bits |= IQ_STATUS_BAD_CHOICE; return 0; }
   }
   return d16;
 }
@@ -417,8 +421,12 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
 }
 
 constexpr int kTcConsumers = 8;                      // 2 consumer warps per block of the quad
-constexpr int kTcThreads = (kTcConsumers + 1) * 32;  // + the control warp
+constexpr int kCtrlWarp = kTcConsumers;              // issues the MMAs
+constexpr int kPrepWarp = kTcConsumers + 1;          // first of the warps preparing the next quad
+constexpr int kPrepWarps = 2;                        // each prepares 2 of the quad's 4 blocks
+constexpr int kTcThreads = (kTcConsumers + 1 + kPrepWarps) * 32;
 constexpr int kChunk = 64;                           // codebook entries per MMA chunk
+constexpr size_t kMaxDynSmem = 227 * 1024;
 
 template <int F> struct TcCfg {
   static constexpr int NQ = Fmt<F>::IQ1 ? 3 : 2;       // An, (Cg), B columns per entry
@@ -431,6 +439,8 @@ template <int F> struct TcCfg {
   // every-choice payloads: per (warp half, vector, choice) the minimum, the near bound (fp32) and
   // key | count << 16
   static constexpr size_t EVERY = 2 * 128 * 16 * 4 * 3;
+  // per-quad state from the prep warp: per vector (Cs, nT2, Ws, sign mask), per block d16 | active
+  static constexpr size_t STATE = 128 * 16 + 4 * 4;
 };
 
 // Per-vector [128 x 8] tf32 operands: nw2 hi, nw2 lo, w hi, w lo; for the second sweep of the
@@ -449,6 +459,15 @@ template <int F, int MODE> __host__ __device__ constexpr int tc_na() {
 template <int F, int MODE> __host__ __device__ constexpr bool tc_deferred(int sweep) {
   return Fmt<F>::IQ1 && (MODE == MODE_FIXED || (MODE == MODE_SEARCH && sweep == 1));
 }
+// Dynamic shared memory with nb buffers of the per-quad operands and state; two buffers (the
+// prep warp fills quad q + 1 while the consumers sweep quad q) wherever they fit.
+template <int F, int MODE> __host__ __device__ constexpr size_t tc_smem(int nb) {
+  return TcCfg<F>::SMEM + (MODE == MODE_EVERY ? TcCfg<F>::EVERY : 0) +
+         (size_t)nb * ((size_t)tc_na<F, MODE>() * 4096 + TcCfg<F>::STATE);
+}
+template <int F, int MODE> __host__ __device__ constexpr int tc_nbuf() {
+  return tc_smem<F, MODE>(2) <= kMaxDynSmem ? 2 : 1;
+}
 
 template <int F, int MODE, typename TIn>
 __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, EncWs ws, int64_t nquads) {
@@ -459,19 +478,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   float *cb = reinterpret_cast<float *>(smem);              // codebook g [N x 8], then h [N x 8]
   float *hlo = cb + (size_t)N * 16;                         // IQ2: low tf32 part of h [N x 8]
   constexpr int NA = tc_na<F, MODE>();
-  float *aop = hlo + TcCfg<F>::HLO / 4;                     // [NA][128 x 8] per-vector operands
-  float *xchg = aop + NA * 1024;                            // [2][128][16] per-choice minima
+  constexpr int NB = tc_nbuf<F, MODE>();
+  float *aop0 = hlo + TcCfg<F>::HLO / 4;                    // [NB][NA][128 x 8] per-vector operands
+  float *xchg = aop0 + NB * NA * 1024;                      // [2][128][16] per-choice minima
   float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
   uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
   float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][128][16] (every mode)
   uint32_t *evk = reinterpret_cast<uint32_t *>(evm + 2 * 128 * 16); // [2][128][16] (every mode)
   float *evt = reinterpret_cast<float *>(evk + 2 * 128 * 16);       // [2][128][16] (every mode)
-  __shared__ uint64_t cb_bar, full_bar[2], empty_bar[2], op_bar;
+  float4 *vst = reinterpret_cast<float4 *>(MODE == MODE_EVERY ? evt + 2 * 128 * 16 : evm);  // [NB][128]
+  uint32_t *bst = reinterpret_cast<uint32_t *>(vst + NB * 128);     // [NB][4]
+  __shared__ uint64_t cb_bar, full_bar[2], empty_bar[2], op_bar, op_full[2], op_empty[2];
   __shared__ uint32_t tmem_base;
   __shared__ int abort_flag;
+  __shared__ int hsplit;  // IQ2: some h = g^2 needs its low tf32 part (read by the MMA issuer)
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const bool control = warp == kTcConsumers;
+  const bool control = warp == kCtrlWarp;
   const int quarter = warp & 3, sub = warp >> 2;
   if (threadIdx.x == 0) {
     mbar_init(&full_bar[0], 1);
@@ -479,6 +502,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
     mbar_init(&empty_bar[0], kTcConsumers);
     mbar_init(&empty_bar[1], kTcConsumers);
     mbar_init(&op_bar, 128);  // searched IQ1_S: the 4 blocks' shifted operands (every writer), per quad
+    mbar_init(&op_full[0], kPrepWarps);   // the prep warps have written a quad's operands and state
+    mbar_init(&op_full[1], kPrepWarps);
+    mbar_init(&op_empty[0], kTcConsumers);   // the consumers are done with a quad's buffer
+    mbar_init(&op_empty[1], kTcConsumers);
     abort_flag = 0;
     mbar_fence_init();
   }
@@ -499,7 +526,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   // h becomes hi = rna_tf32(h) in place plus lo = h - hi (an integer of at most 4 significant
   // bits), both exact in tf32; when some h needs the low part, B = w . hi + w . lo takes two more
   // MMAs per chunk, so the codebook operand stays exact for every accepted grid.
-  bool hsplit = false;
   if constexpr (!Fmt<F>::IQ1) {
     bool inexact = false;
     if (ok && !grid_bad) {
@@ -512,8 +538,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    hsplit = __syncthreads_or(inexact) != 0;
+    const int any = __syncthreads_or(inexact);
+    if (threadIdx.x == 0) hsplit = any;
   }
+  __syncthreads();  // hsplit is published
 
   constexpr bool kOpSync = F == IQ1_S && MODE == MODE_SEARCH;  // operands written between the sweeps
   const int g0 = lane & ~(VPG - 1);
@@ -526,139 +554,194 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   int st_acc = 0;
 
   bool okl = ok;                                            // this thread's waits all completed
-  for (int64_t qd = blockIdx.x; qd < nquads; qd += gridDim.x) {
-    // a timeout is published only before the CTA-wide barrier, so all threads read one value after it
-    if (!okl) {
-      abort_flag = 1;
-      if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
-    }
-    const int64_t b = qd * 4 + quarter;
-    bool active = false;
-    uint32_t d16 = 0;
-    Vec v;
-    float Cgrp = 0.0f;
-    if (!control) {
-      int bad = 0;
-      const bool has = b < a.nblocks && !grid_bad;
-      if (has) {
-        load_block_vec<TIn>(a, b, lane, v);
-        d16 = block_scale<F, MODE>(a, b, lane, v, bad);
-      }
-      if (sub == 0) st_acc |= bad;
-      active = has && d16 != 0;
-      if (active) {
-        vec_setup<F>(v);
-        Cgrp = group_sum<VPG>(v.Cs, g0);
-      } else if (sub == 0 && b < a.nblocks) {
-        // a rejected or zero-scale block: all-zero payload; every choice decodes to zeros
-        if (MODE == MODE_EVERY) {
-          for (int c = 0; c < C; c++)
-            for (int i = lane; i < BB; i += 32) a.payload[((size_t)c * a.nblocks + b) * BB + i] = 0;
-        } else if (MODE != MODE_TABLE) {
-          for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = 0;
-          if (a.wb) write_back_zero<TIn>(a, b, lane);
-        }
-        if (a.table && MODE != MODE_FIXED) {
-          float cs = 0.0f;
-          if (has) {
+  // A timeout in any role sets abort_flag (and the status bit); every role checks it once per quad,
+  // and every wait is bounded, so all roles leave the quad loop and meet at the final barrier.
+  auto give_up = [&]() {
+    *(volatile int *)&abort_flag = 1;
+    if (a.status && lane == 0) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+  };
+  uint32_t it = 0;                                          // this CTA's quad counter
+  if (warp >= kPrepWarp) {
+    // ---- prep: loads, scale, sign rule and tf32 operands of the quad, one quad ahead; prep warp
+    // pw takes blocks 2 pw and 2 pw + 1 of each quad ----------------------------------------
+    const int blk0 = 2 * (warp - kPrepWarp);
+    for (int64_t qd = blockIdx.x; qd < nquads; qd += gridDim.x, it++) {
+      const uint32_t qb = it % NB;
+      if (it >= NB && okl && !mbar_wait_bounded(&op_empty[qb], ((it / NB) - 1) & 1)) okl = false;
+      okl = __all_sync(0xffffffffu, okl);
+      if (!okl) { give_up(); break; }
+      if (*(volatile int *)&abort_flag) break;
+      float X[2][8], Wt[2][8];
+      int d16p[2], chp[2];   // given scales, and (lane < G) the fixed choice of group `lane`
 #pragma unroll
-            for (int i = 0; i < 8; i++) cs = __fmaf_rn(__fmul_rn(v.w[i], v.x[i]), v.x[i], cs);
-          }
-          const float e0 = group_sum<VPG>(cs, g0);
-          const float val = (bad || grid_bad) ? __int_as_float(0x7fc00000) : e0;
-          if (lane == g0)
-            for (int c = 0; c < C; c++) a.table[(b * G + cg) * C + c] = val;
+      for (int bi = 0; bi < 2; bi++) {   // every load first
+        const int64_t b = qd * 4 + blk0 + bi;
+        d16p[bi] = -1;
+        chp[bi] = 0;
+        if (b < a.nblocks && !grid_bad) {
+          Vec t;
+          load_block_vec<TIn>(a, b, lane, t);
+#pragma unroll
+          for (int i = 0; i < 8; i++) { X[bi][i] = t.x[i]; Wt[bi][i] = t.w[i]; }
+          if (a.d16) d16p[bi] = (int)a.d16[b];
+          if (MODE == MODE_FIXED && lane < G) chp[bi] = fixed_choice<G>(a, b, lane);
         }
       }
-      if (sub == 0) {
+      float *aop = aop0 + qb * NA * 1024;
+#pragma unroll
+      for (int bi = 0; bi < 2; bi++) {
+        const int blk = blk0 + bi;
+        const int64_t b = qd * 4 + blk;
+        const int prow = 32 * blk + lane;
+        Vec v;
+#pragma unroll
+        for (int i = 0; i < 8; i++) { v.x[i] = X[bi][i]; v.w[i] = Wt[bi][i]; }
+        int bad = 0;
+        uint32_t d16 = 0;
+        const bool has = b < a.nblocks && !grid_bad;
+        if (has) d16 = block_scale<F, MODE>(v, lane, d16p[bi], chp[bi], bad);
+        const int cfix = MODE == MODE_FIXED ? __shfl_sync(0xffffffffu, chp[bi], cg) : 0;  // this vector's group
+        st_acc |= bad;
+        const bool active = has && d16 != 0;
+        if (active) {
+          vec_setup<F>(v);
+        } else if (b < a.nblocks) {
+          // a rejected or zero-scale block: all-zero payload; every choice decodes to zeros
+          if (MODE == MODE_EVERY) {
+            for (int c = 0; c < C; c++)
+              for (int i = lane; i < BB; i += 32) a.payload[((size_t)c * a.nblocks + b) * BB + i] = 0;
+          } else if (MODE != MODE_TABLE) {
+            for (int i = lane; i < BB; i += 32) a.payload[b * BB + i] = 0;
+            if (a.wb) write_back_zero<F, TIn>(a, b, lane);
+          }
+          if (a.table && MODE != MODE_FIXED) {
+            float cs = 0.0f;
+            if (has) {
+#pragma unroll
+              for (int i = 0; i < 8; i++) cs = __fmaf_rn(__fmul_rn(v.w[i], v.x[i]), v.x[i], cs);
+            }
+            const float e0 = group_sum<VPG>(cs, g0);
+            const float val = (bad || grid_bad) ? __int_as_float(0x7fc00000) : e0;
+            if (lane == g0)
+              for (int c = 0; c < C; c++) a.table[(b * G + cg) * C + c] = val;
+          }
+        }
         // IQ1_S with fixed choices: the sign of the group's shift (choice c = scale + 8 * shift bit)
-        const float sig = MODE == MODE_FIXED && NA == 6 && active && (fixed_choice<G>(a, b, cg) >> 3) ? -0.25f : 0.25f;
+        const float sig = MODE == MODE_FIXED && NA == 6 && active && (cfix >> 3) ? -0.25f : 0.25f;
 #pragma unroll
         for (int k = 0; k < 8; k++) {
           const float nw = active ? v.nw2[k] : 0.0f, ww = active ? v.w[k] : 0.0f;
           const float nh = tf32_rna(nw), wh = tf32_rna(ww);
-          aop[0 * 1024 + kmaj(row, k)] = nh;
-          aop[1 * 1024 + kmaj(row, k)] = tf32_rna(__fsub_rn(nw, nh));
+          aop[0 * 1024 + kmaj(prow, k)] = nh;
+          aop[1 * 1024 + kmaj(prow, k)] = tf32_rna(__fsub_rn(nw, nh));
           const float wl = tf32_rna(__fsub_rn(ww, wh));
-          aop[2 * 1024 + kmaj(row, k)] = wh;
-          aop[3 * 1024 + kmaj(row, k)] = wl;
+          aop[2 * 1024 + kmaj(prow, k)] = wh;
+          aop[3 * 1024 + kmaj(prow, k)] = wl;
           if (NA == 8) {  // exact power-of-two scalings of the tf32 parts
-            aop[4 * 1024 + kmaj(row, k)] = 0.25f * wh;
-            aop[5 * 1024 + kmaj(row, k)] = 0.25f * wl;
-            aop[6 * 1024 + kmaj(row, k)] = -0.25f * wh;
-            aop[7 * 1024 + kmaj(row, k)] = -0.25f * wl;
+            aop[4 * 1024 + kmaj(prow, k)] = 0.25f * wh;
+            aop[5 * 1024 + kmaj(prow, k)] = 0.25f * wl;
+            aop[6 * 1024 + kmaj(prow, k)] = -0.25f * wh;
+            aop[7 * 1024 + kmaj(prow, k)] = -0.25f * wl;
           } else if (NA == 6 && MODE == MODE_FIXED) {
-            aop[4 * 1024 + kmaj(row, k)] = sig * wh;
-            aop[5 * 1024 + kmaj(row, k)] = sig * wl;
+            aop[4 * 1024 + kmaj(prow, k)] = sig * wh;
+            aop[5 * 1024 + kmaj(prow, k)] = sig * wl;
           }
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        // .w: the sign mask (bits 0..7) and, with fixed choices, the group's choice (bits 8..15)
+        vst[qb * 128 + prow] = active ? make_float4(v.Cs, v.nT2, v.Ws, __int_as_float(v.sgn | cfix << 8))
+                                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (lane == 0) bst[qb * 4 + blk] = d16 | (active ? 1u << 16 : 0u);
       }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // operands seen by the MMAs
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&op_full[qb]);
     }
-    named_bar(1, kTcThreads);  // the quad's operands are in shared memory; the previous quad is done
-    if (*(volatile int *)&abort_flag) break;
-
-    if (control) {
-      // ---- MMA issue: sweep 1 (unless fixed choices) and sweep 2 (unless table only) ---------
+  } else if (control) {
+    // IQ2: whether B takes the low parts of h too (read once: the flag is fixed for the call)
+    const bool hsreg = !Fmt<F>::IQ1 && *(volatile int *)&hsplit;
+    // ---- MMA issue: sweep 1 (unless fixed choices) and sweep 2 (unless table only) ---------
+    for (int64_t qd = blockIdx.x; qd < nquads; qd += gridDim.x, it++) {
+      const uint32_t qb = it % NB;
       if (lane == 0) {
-        const int nsweeps = (MODE != MODE_FIXED) + (MODE != MODE_TABLE);
-        const uint32_t sa = smem_u32(aop), sg = smem_u32(cb), sh = sg + N * 32, shl = smem_u32(hlo);
-        for (int sw = 0; sw < nsweeps; sw++) {
-          for (int ch = 0; ch < NCH; ch++, issued++) {
-            const uint32_t buf = issued & 1;
-            // searched IQ1_S: the second sweep's shifted operands are written after the first sweep
-            if (kOpSync && sw == 1 && ch == 0 && okl && !mbar_wait_bounded(&op_bar, nquad & 1)) okl = false;
-            if (!okl || (issued >= 2 && !mbar_wait_bounded(&empty_bar[buf], ((issued >> 1) - 1) & 1))) {
-              okl = false;  // stop issuing; consumers' waits on the missing chunks time out
-              break;
-            }
-            tc_fence_after();
-            const uint32_t d = tmem + buf * NQ * kChunk;
-            const uint64_t bg = umma_desc(sg + ch * kChunk * 32), bh = umma_desc(sh + ch * kChunk * 32);
-            umma_tf32(d, umma_desc(sa + 0 * 4096), bg, IDESC, 0);          // An = nw2 . g
-            umma_tf32(d, umma_desc(sa + 1 * 4096), bg, IDESC, 1);
-            if (tc_deferred<F, MODE>(sw) && F == IQ1_S) {
-              umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);      // Bd' = w . h
-              umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
-              umma_tf32(d + kChunk, umma_desc(sa + 4 * 4096), bg, IDESC, 1);      //      + (sigma w/4) . g
-              umma_tf32(d + kChunk, umma_desc(sa + 5 * 4096), bg, IDESC, 1);
-            } else if (tc_deferred<F, MODE>(sw)) {
-              umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);      // Bp' = w . h
-              umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
-              umma_tf32(d + kChunk, umma_desc(sa + 4 * 4096), bg, IDESC, 1);      //      + (w/4) . g
-              umma_tf32(d + kChunk, umma_desc(sa + 5 * 4096), bg, IDESC, 1);
-              umma_tf32(d + 2 * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // Bm' = w . h
-              umma_tf32(d + 2 * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
-              umma_tf32(d + 2 * kChunk, umma_desc(sa + 6 * 4096), bg, IDESC, 1);  //      - (w/4) . g
-              umma_tf32(d + 2 * kChunk, umma_desc(sa + 7 * 4096), bg, IDESC, 1);
-            } else {
-              if (NQ == 3) {
-                umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bg, IDESC, 0);  // Cg = w . g
-                umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bg, IDESC, 1);
+        if (okl && !mbar_wait_bounded(&op_full[qb], (it / NB) & 1)) okl = false;
+        if (okl && !*(volatile int *)&abort_flag) {
+            const int nsweeps = (MODE != MODE_FIXED) + (MODE != MODE_TABLE);
+            const uint32_t sa = smem_u32(aop0 + qb * NA * 1024), sg = smem_u32(cb), sh = sg + N * 32, shl = smem_u32(hlo);
+            for (int sw = 0; sw < nsweeps; sw++) {
+              for (int ch = 0; ch < NCH; ch++, issued++) {
+                const uint32_t buf = issued & 1;
+                // searched IQ1_S: the second sweep's shifted operands are written after the first sweep
+                if (kOpSync && sw == 1 && ch == 0 && okl && !mbar_wait_bounded(&op_bar, nquad & 1)) okl = false;
+                if (!okl || (issued >= 2 && !mbar_wait_bounded(&empty_bar[buf], ((issued >> 1) - 1) & 1))) {
+                  okl = false;  // stop issuing; consumers' waits on the missing chunks time out
+                  break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * NQ * kChunk;
+                const uint64_t bg = umma_desc(sg + ch * kChunk * 32), bh = umma_desc(sh + ch * kChunk * 32);
+                umma_tf32(d, umma_desc(sa + 0 * 4096), bg, IDESC, 0);          // An = nw2 . g
+                umma_tf32(d, umma_desc(sa + 1 * 4096), bg, IDESC, 1);
+                if (tc_deferred<F, MODE>(sw) && F == IQ1_S) {
+                  umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);      // Bd' = w . h
+                  umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+                  umma_tf32(d + kChunk, umma_desc(sa + 4 * 4096), bg, IDESC, 1);      //      + (sigma w/4) . g
+                  umma_tf32(d + kChunk, umma_desc(sa + 5 * 4096), bg, IDESC, 1);
+                } else if (tc_deferred<F, MODE>(sw)) {
+                  umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);      // Bp' = w . h
+                  umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+                  umma_tf32(d + kChunk, umma_desc(sa + 4 * 4096), bg, IDESC, 1);      //      + (w/4) . g
+                  umma_tf32(d + kChunk, umma_desc(sa + 5 * 4096), bg, IDESC, 1);
+                  umma_tf32(d + 2 * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // Bm' = w . h
+                  umma_tf32(d + 2 * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+                  umma_tf32(d + 2 * kChunk, umma_desc(sa + 6 * 4096), bg, IDESC, 1);  //      - (w/4) . g
+                  umma_tf32(d + 2 * kChunk, umma_desc(sa + 7 * 4096), bg, IDESC, 1);
+                } else {
+                  if (NQ == 3) {
+                    umma_tf32(d + kChunk, umma_desc(sa + 2 * 4096), bg, IDESC, 0);  // Cg = w . g
+                    umma_tf32(d + kChunk, umma_desc(sa + 3 * 4096), bg, IDESC, 1);
+                  }
+                  umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // B = w . h
+                  umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
+                  if (hsreg) {                                                              //   + w . h lo
+                    const uint64_t bl = umma_desc(shl + ch * kChunk * 32);
+                    umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bl, IDESC, 1);
+                    umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bl, IDESC, 1);
+                  }
+                }
+                umma_commit(&full_bar[buf]);
               }
-              umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bh, IDESC, 0);  // B = w . h
-              umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bh, IDESC, 1);
-              if (!Fmt<F>::IQ1 && hsplit) {                                             //   + w . h lo
-                const uint64_t bl = umma_desc(shl + ch * kChunk * 32);
-                umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 2 * 4096), bl, IDESC, 1);
-                umma_tf32(d + (NQ - 1) * kChunk, umma_desc(sa + 3 * 4096), bl, IDESC, 1);
-              }
+              if (!okl) break;
             }
-            umma_commit(&full_bar[buf]);
-          }
-          if (!okl) break;
         }
         nquad++;
       }
       okl = __shfl_sync(0xffffffffu, okl, 0);
-      continue;
+      if (!okl) { give_up(); break; }
+      if (*(volatile int *)&abort_flag) break;
     }
+  } else {
+  for (int64_t qd = blockIdx.x; qd < nquads; qd += gridDim.x, it++) {
+    const uint32_t qb = it % NB;
+    if (okl && !mbar_wait_bounded(&op_full[qb], (it / NB) & 1)) okl = false;
+    okl = __all_sync(0xffffffffu, okl);
+    if (!okl) { give_up(); break; }
+    if (*(volatile int *)&abort_flag) break;
+    const int64_t b = qd * 4 + quarter;
+    const uint32_t bs = bst[qb * 4 + quarter];
+    const uint32_t d16 = bs & 0xffffu;
+    const bool active = (bs >> 16) & 1u;
+    const float4 vs = vst[qb * 128 + row];
+    const float vCs = vs.x, vnT2 = vs.y, vWs = vs.z;
+    const int vsgn = __float_as_int(vs.w) & 0xff;
+    const int vfix = __float_as_int(vs.w) >> 8;   // fixed-choice mode: the group's choice
+    const float Cgrp = group_sum<VPG>(vCs, g0);
+    float *aop = aop0 + qb * NA * 1024;
 
     // ---- consumers ---------------------------------------------------------------------------
     const float d = half_bits_to_float((uint16_t)d16);
     const IQ1Const kc = iq1_consts();
-    const uint64_t nT2p = pk2(v.nT2, v.nT2), Wsp = pk2(v.Ws, v.Ws);
-    const float w64 = 0.015625f * v.Ws, t8 = 0.125f * v.nT2;  // exact power-of-two scalings
+    const uint64_t nT2p = pk2(vnT2, vnT2), Wsp = pk2(vWs, vWs);
+    const float w64 = 0.015625f * vWs, t8 = 0.125f * vnT2;  // exact power-of-two scalings
     const int ebase0 = 32 * sub;  // this warp's first entry in each chunk
     // IQ1_S second sweep (fixed or searched choices): deferred layout [An | Bd' | -]
     constexpr bool kDefS = F == IQ1_S && (MODE == MODE_FIXED || MODE == MODE_SEARCH);
@@ -739,7 +822,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         for (int c = 0; c < C; c++) {
           const float al = alpha_choice<F>(d, c);
           const float e1 = __fmul_rn(al, m[c]);
-          const float De = 1.01f * kMargin * fmaxf(4.0f * v.Cs + 2.0f * e1, 0.0f);
+          const float De = 1.01f * kMargin * fmaxf(4.0f * vCs + 2.0f * e1, 0.0f);
           evt[(sub * 128 + row) * 16 + c] =
               active ? m[c] + 1.01f * (De / al) + 9.5367431640625e-07f * fabsf(m[c]) : -INFINITY;
           evm[(sub * 128 + row) * 16 + c] = m[c];
@@ -758,7 +841,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         gflag = __fsub_rn(D2, D1) <= kMargin * (4.0f * Cgrp + D1 + D2);
       }
     } else if (active) {
-      c1 = fixed_choice<G>(a, b, cg);
+      c1 = vfix;
     }
     if constexpr (kOpSync) {
       // the second sweep's shifted operand sigma w/4 (hi, lo) of each vector, sigma the sign of its
@@ -766,11 +849,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       if (sub == 0) {
         const float sig = (c1 >> 3) ? -0.25f : 0.25f;
 #pragma unroll
-        for (int k = 0; k < 8; k++) {
-          const float ww = active ? v.w[k] : 0.0f;
-          const float wh = tf32_rna(ww), wl = tf32_rna(__fsub_rn(ww, wh));
-          aop[4 * 1024 + kmaj(row, k)] = sig * wh;
-          aop[5 * 1024 + kmaj(row, k)] = sig * wl;
+        for (int k = 0; k < 8; k++) {   // the tf32 parts of w (zero for an inactive block), scaled
+          aop[4 * 1024 + kmaj(row, k)] = sig * aop[2 * 1024 + kmaj(row, k)];
+          aop[5 * 1024 + kmaj(row, k)] = sig * aop[3 * 1024 + kmaj(row, k)];
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         mbar_arrive(&op_bar);
@@ -890,7 +971,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           const Bits lo = f_idx_lo<F>(lane);
           put_bits(pb, lo, (uint32_t)idx);
           if (F == IQ2_S || Fmt<F>::IQ1) put_bits(pb, f_idx_hi<F>(lane), (uint32_t)idx >> lo.width);
-          if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)v.sgn);
+          if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)vsgn);
           if (F == IQ1_M) {
             put_bits(pb, f_dbit_vec<F>(lane), (uint32_t)(k / N));
             if (lane < 4) put_bits(pb, f_d16_nib<F>(lane), (d16 >> (4 * lane)) & 15u);
@@ -937,7 +1018,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         constexpr float kW = Fmt<F>::IQ1 ? 2.02f : 1.01f;
         constexpr float kR = Fmt<F>::IQ1 ? 1.9073486328125e-06f : 9.5367431640625e-07f;
         const float e1 = __fmul_rn(alpha, smin);
-        const float De = 1.01f * kMargin * fmaxf(4.0f * v.Cs + 2.0f * e1, 0.0f);
+        const float De = 1.01f * kMargin * fmaxf(4.0f * vCs + 2.0f * e1, 0.0f);
         T = smin + kW * (De / alpha) + kR * fabsf(smin);
       }
       // Two trackers per shift, over the even and the odd pairs of each half chunk (two shorter
@@ -1024,7 +1105,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         // searched mode: no second candidate near the best means no flag; no best found at all
         // (cannot happen while both sweeps agree) hands the vector to the exact rescoring
         const bool vflag = !(s1 < INFINITY) ||
-                           (s2 < INFINITY && __fsub_rn(e2, e1) <= kMargin * (4.0f * v.Cs + e1 + e2));
+                           (s2 < INFINITY && __fsub_rn(e2, e1) <= kMargin * (4.0f * vCs + e1 + e2));
         // pack
         uint32_t *pb = packbuf + quarter * 24;
         if (lane < 24) pb[lane] = 0u;
@@ -1033,7 +1114,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         const Bits lo = f_idx_lo<F>(lane);
         put_bits(pb, lo, (uint32_t)idx);
         if (F == IQ2_S || Fmt<F>::IQ1) put_bits(pb, f_idx_hi<F>(lane), (uint32_t)idx >> lo.width);
-        if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)v.sgn);
+        if (!Fmt<F>::IQ1) put_bits(pb, f_sign<F>(lane), (uint32_t)vsgn);
         if (F == IQ1_M) {
           put_bits(pb, f_dbit_vec<F>(lane), (uint32_t)(key / N));
           if (lane < 4) put_bits(pb, f_d16_nib<F>(lane), (d16 >> (4 * lane)) & 15u);
@@ -1059,11 +1140,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           float g8[8];
 #pragma unroll
           for (int i = 0; i < 8; i++) g8[i] = cb[kmaj(idx, i)];
-          write_back_vec<F, TIn>(a, b, lane, g8, d, F == IQ1_S ? (c1 & 7) : c1, v.sgn,
+          write_back_vec<F, TIn>(a, b, lane, g8, d, F == IQ1_S ? (c1 & 7) : c1, vsgn,
                                  F == IQ1_S ? (c1 >> 3) : F == IQ1_M ? key / N : 0);
         }
       }
     }
+    // this warp is done with the quad's state and operands (its MMAs have completed): the prep
+    // warp may refill the buffer
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&op_empty[qb]);
+  }
   }
   if (!okl && a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
   if (st_acc && a.status && lane == 0) atomicOr(a.status, st_acc);
@@ -1227,6 +1313,9 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
       }
       // (a) fp32 minima of vector kv over slice js for every choice (or the fixed one), as the
       // sweep computes them
+      // (with the group's choice fixed only the flagged vectors are re-decided: the entries of the
+      // others are independent decisions the sweep already made exactly)
+      const bool kvflag = !kFixedLike || ((mask >> (g * VPG + kv)) & 1u);
       {
         const Vec u = shfl_vec(v, g * VPG + kv);
         float lm[C], alc[C];
@@ -1237,7 +1326,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
           cand_of_choice<F>(c, s, db0, db1);
           alc[c] = alpha_of<F>(d, s);
         }
-        for (int e = js * SL + lane; e < (js + 1) * SL; e += 32) {
+        for (int e = js * SL + lane; kvflag && e < (js + 1) * SL; e += 32) {
           Entry en;
           load_entry<F>(tab, e, en);
           // the entry's sums once, then every choice's score as cand_score forms it
@@ -1287,12 +1376,14 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         }
         for (int c = 0; c < C; c++)
           if (D[c] != INFINITY && __fsub_rn(D[c], D1) <= kMargin * (4.0f * Cg + D1 + D[c])) near |= 1u << c;
+        if (kFixedLike) near = 1u << cfix;
       }
       // (c) exact minimum per (near choice, vector) over the candidates the bound cannot exclude:
       // units (near choice, vector, slice) dealt to the warps
       const int nunits = __popc(near) * VPG * NSL;
       for (int unit = wid; unit < nunits; unit += kRsWarps) {
         const int ci = unit / (VPG * NSL), k = (unit / NSL) % VPG, j = unit % NSL;
+        if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
         uint32_t rest = near;
         for (int q = 0; q < ci; q++) rest &= rest - 1u;
         const int c = __ffs(rest) - 1;
@@ -1350,11 +1441,13 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
           for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, sm.ex[k][c]);
           if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
         }
+        if (kFixedLike) cstar = cfix;
         if (cstar >= 0) {
           set_bits_bytes(pbytes, f_scale<F>(g), (uint32_t)(F == IQ1_S ? (cstar & 7) : cstar));
           if (F == IQ1_S) set_bits_bytes(pbytes, f_dbit_grp<F>(g), (uint32_t)(cstar >> 3));
           for (int k = 0; k < VPG; k++) {
             const int vv = g * VPG + k;
+            if (kFixedLike && !((mask >> vv) & 1u)) continue;
             const int key = sm.exkey[k][cstar];
             const int idx = F == IQ1_M ? key % N : key;
             const Bits lo = f_idx_lo<F>(vv);
@@ -1415,11 +1508,14 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       const uint32_t gm = ((1u << VPG) - 1u) << (g * VPG);
       if (!(mask & gm)) continue;
       float Cg = 0.0f;
-      // (a) fp32 per-vector minima for every choice (or the fixed one), as the sweep computes them
+      // (a) fp32 per-vector minima for every choice (or the fixed one), as the sweep computes them.
+      // With the group's choice fixed, the vectors' entries are independent decisions: only the
+      // flagged vectors are re-decided, the others keep the sweep's exact pick.
       int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : MODE == MODE_EVERY ? cpass : -1;
       for (int k = 0; k < VPG; k++) {
         const Vec u = shfl_vec(v, g * VPG + k);
         Cg = k == 0 ? u.Cs : __fadd_rn(Cg, u.Cs);
+        if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
         float lm[C], alc[C];
 #pragma unroll
         for (int c = 0; c < C; c++) {
@@ -1472,6 +1568,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       uint32_t near = 0;
       for (int c = 0; c < C; c++)
         if (D[c] != INFINITY && __fsub_rn(D[c], D1) <= kMargin * (4.0f * Cg + D1 + D[c])) near |= 1u << c;
+      if (kFixedLike) near = 1u << cfix;
       // (c) exact minimum per (vector, near choice) over the candidates the bound cannot exclude
       for (int c = 0; c < C; c++) {
         if (!((near >> c) & 1)) continue;
@@ -1479,6 +1576,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
         cand_of_choice<F>(c, s, db0, db1);
         const float al = alpha_of<F>(d, s);
         for (int k = 0; k < VPG; k++) {
+          if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
           const Vec u = shfl_vec(v, g * VPG + k);
           const float mh = sm.mh[k][c];
           const float emin = __fmul_rn(al, mh);
@@ -1516,12 +1614,14 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
         for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, sm.ex[k][c]);
         if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
       }
+      if (kFixedLike) cstar = cfix;
       // (e) rewrite the group's fields (keep the sweep's decision if nothing was comparable)
       if (lane == 0 && cstar >= 0) {
         set_bits_bytes(pbytes, f_scale<F>(g), (uint32_t)(F == IQ1_S ? (cstar & 7) : cstar));
         if (F == IQ1_S) set_bits_bytes(pbytes, f_dbit_grp<F>(g), (uint32_t)(cstar >> 3));
         for (int k = 0; k < VPG; k++) {
           const int vv = g * VPG + k;
+          if (kFixedLike && !((mask >> vv) & 1u)) continue;
           const int key = sm.exkey[k][cstar];
           const int idx = F == IQ1_M ? key % N : key;
           const Bits lo = f_idx_lo<F>(vv);
@@ -1592,7 +1692,7 @@ static int run_encode(const EncArgs &a, void *workspace, size_t ws_bytes, cudaSt
   EncWs ws = enc_ws(workspace, N);
   if (cudaMemsetAsync(ws.hdr, 0, 256, st) != cudaSuccess) return IQ_ERR_CUDA;
   prep_codebook<F><<<(N + 255) / 256, 256, 0, st>>>(a.grid, ws);
-  const size_t smem = TcCfg<F>::SMEM + (size_t)tc_na<F, MODE>() * 4096 + (MODE == MODE_EVERY ? TcCfg<F>::EVERY : 0);
+  const size_t smem = tc_smem<F, MODE>(tc_nbuf<F, MODE>());
   auto kern = encode_tc_kernel<F, MODE, TIn>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;

@@ -14,19 +14,20 @@
 // Kernels per call:
 //  route       one CTA per (chunk, 128-row sub-tile): builds the sub-tile's expert bitmap in shared
 //              memory (a token's ids are a set) and writes the sub-tile's segment: for every expert
-//              the offset of its rows and the rows themselves (as 16-bit byte offsets into a staged
+//              the offset of its rows and the rows themselves (as 32-bit byte offsets into a staged
 //              tile, ascending, each run padded to a multiple of 4 with the offset of a zero row);
-//              per-chunk counts are added atomically, and the last CTA to finish ranks the experts
-//              by their count over the whole call (the order consumer warps are dealt from, the same
-//              for every chunk so that each expert's in_sum2 row has one owner);
+//              per-chunk counts are added atomically, and the last CTA to finish plans the work:
+//              experts ranked by their count over the whole call, heavy ones cut into 2 or 4 column
+//              parts, and the resulting units dealt to the consumer warps so that their loads match
+//              (the same plan for every chunk, so each (expert, column) sum has one owner);
 //  accumulate  one CTA per column tile (128 bf16 / 64 fp32 columns, 256 bytes of a row) and,
 //              when there are too few tiles to fill the GPU, per chunk as well.  A producer warp
-//              streams the tile's rows through a 3-stage shared-memory ring: each stage is one 2-D
-//              TMA tensor copy of 128 rows plus one bulk copy of the sub-tile's segment, both
-//              completing on the stage's mbarrier (waits bounded by the global timer).  Each
-//              consumer warp owns up to 8 experts (dealt from the count order so heavy and light
-//              experts mix), walks their rows 4 at a time from shared memory only and keeps one
-//              register accumulator per (expert, column of its lane);
+//              streams the tile's rows through a ring of up to 4 shared-memory stages: each stage is
+//              one 2-D TMA tensor copy of 128 rows plus one bulk copy of the sub-tile's segment,
+//              both completing on the stage's mbarrier (waits bounded by the global timer).  Each
+//              consumer warp walks its units' rows 4 at a time from shared memory (a unit's lane
+//              reads 8, 4 or 2 bytes of a row) and keeps one register accumulator per (unit,
+//              column of its lane);
 //  combine     (per-chunk mode only) adds the chunk partials to in_sum2 in chunk order.
 // No atomics touch in_sum2, so the sums are the sequential definition above.
 #include <cudaTypedefs.h>
@@ -39,26 +40,32 @@
 namespace iqk {
 
 constexpr int kSub = 128;           // rows per stage
-constexpr int kStages = 3;          // shared-memory ring depth
+constexpr int kMaxStages = 4;       // shared-memory ring depth (fewer when segments are large)
 constexpr int kRowBytes = 256;      // bytes of one row of a column tile
-constexpr int kSlots = 8;           // experts per consumer warp
+constexpr int kSlots = 9;           // work units per consumer warp (the plan needs at most 9)
+constexpr int kMaxRounds = 40;      // dealing rounds per scheduler: at most (kBatch + 9) / 4 units
 constexpr int kMaxConsumers = 16;   // consumer warps per CTA
-constexpr int kBatch = kSlots * kMaxConsumers;  // experts per pass over x
+constexpr int kBatch = 128;         // experts per pass over x
 constexpr int kMinSeqCtas = 112;    // below this many (tile, batch) CTAs, chunks also run in parallel
-constexpr int kMaxTopK = 64;        // bounds the rows a segment holds (kSub * top_k bytes)
+constexpr int kMaxTopK = 64;        // bounds the rows a segment holds
+constexpr size_t kSmemBudget = 200 * 1024;
+
+// cost of one (row, unit) pair in half instructions by column split (1, 2 or 4 parts of a row);
+// a unit with more parts covers fewer columns per lane for the same per-row overhead
+__host__ __device__ inline int unit_cost(int lk) { return lk == 0 ? 13 : lk == 1 ? 9 : 7; }
 
 template <typename T> struct Col;
-template <> struct Col<__nv_bfloat16> { static constexpr int CPL = 4, TILE = 128; };
-template <> struct Col<float> { static constexpr int CPL = 2, TILE = 64; };
+template <> struct Col<__nv_bfloat16> { static constexpr int TILE = 128, MAXLK = 2; };  // up to 4 parts
+template <> struct Col<float> { static constexpr int TILE = 64, MAXLK = 1; };           // up to 2 parts
 
 __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 __host__ __device__ inline int align16(int n) { return (n + 15) & ~15; }
 
 // A segment (one per chunk and 128-row sub-tile): int32 offsets[E + 1] (padded to 16 bytes), then
-// the rows of expert 0, expert 1, ... as uint16 byte offsets (row * 256) into the staged tile, each
+// the rows of expert 0, expert 1, ... as uint32 byte offsets (row * 256) into the staged tile, each
 // run ascending and padded to a multiple of 4 entries with the zero row's offset (kSub * 256).
-constexpr uint16_t kZeroOff = (uint16_t)(kSub * kRowBytes);
+constexpr uint32_t kZeroOff = (uint32_t)(kSub * kRowBytes);
 struct SegLayout {
   int offb;   // bytes of the offset table
   int bytes;  // segment bytes (multiple of 16)
@@ -66,14 +73,19 @@ struct SegLayout {
 __host__ __device__ inline SegLayout seg_layout(int E, int top_k) {
   SegLayout l;
   l.offb = align16((E + 1) * 4);
-  l.bytes = l.offb + align16(2 * (kSub * (top_k < E ? top_k : E) + 3 * E));
+  l.bytes = l.offb + align16(4 * (kSub * (top_k < E ? top_k : E) + 3 * E));
   return l;
 }
+
+// A work unit of the accumulation: expert e over part j of the 2^lk parts of a tile row (so a
+// heavy expert is spread over several consumer warps, each walking its rows for fewer columns).
+// plan[batch][warp][slot] = e | j << 16 | lk << 20, or -1 (no unit).
+__host__ __device__ inline int unit_desc(int e, int j, int lk) { return e | (j << 16) | (lk << 20); }
 
 struct RouteWs {
   int32_t *touched;    // [E]   experts this call routed at least one token to; [E] = CTAs done
   int32_t *ccount;     // [nchunks][E] tokens per (chunk, expert)
-  int32_t *order;      // [E] experts by descending count over the call (ties: lower id)
+  int32_t *plan;       // [nbatch][kMaxConsumers][kSlots] work units of each consumer warp
   uint8_t *seg;        // [nchunks][nsub] segments of seg_bytes
   float *partial;      // [nchunks][E][cols] (per-chunk mode only)
   size_t zero_bytes;   // bytes from the start to clear before the call (touched + ccount)
@@ -81,7 +93,7 @@ struct RouteWs {
 
 struct Plan {
   int64_t nchunks, ntiles, nbatch;
-  int nsub;
+  int nsub, nw, maxlk;
   SegLayout seg;
   bool split;
 };
@@ -92,8 +104,10 @@ static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_
   p.nsub = (int)((rpc + kSub - 1) / kSub);
   p.seg = seg_layout(E, top_k);
   const int tile = dt == IQ_BF16 ? Col<__nv_bfloat16>::TILE : Col<float>::TILE;
+  p.maxlk = dt == IQ_BF16 ? Col<__nv_bfloat16>::MAXLK : Col<float>::MAXLK;
   p.ntiles = (cols + tile - 1) / tile;
   p.nbatch = (E + kBatch - 1) / kBatch;
+  p.nw = kMaxConsumers;   // the plan deals over all four schedulers' warps
   p.split = p.nchunks > 1 && p.ntiles * p.nbatch < kMinSeqCtas;
   return p;
 }
@@ -104,24 +118,140 @@ static RouteWs route_ws(void *ws, const Plan &p, int E, int64_t cols) {
   r.touched = (int32_t *)q; q += align256((size_t)(E + 1) * 4);
   r.ccount = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
   r.zero_bytes = (size_t)(q - (uint8_t *)ws);
-  r.order = (int32_t *)q; q += align256((size_t)E * 4);
+  r.plan = (int32_t *)q; q += align256((size_t)p.nbatch * kMaxConsumers * kSlots * 4);
   r.seg = q; q += align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   r.partial = p.split ? (float *)q : nullptr;
   return r;
 }
 static size_t route_ws_bytes(const Plan &p, int E, int64_t cols) {
-  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * 4) + align256((size_t)E * 4) +
-             align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
+  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * 4) +
+             align256((size_t)p.nbatch * kMaxConsumers * kSlots * 4) + align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   if (p.split) n += align256((size_t)p.nchunks * E * cols * 4);
   return n;
 }
 
 // ---------------------------------------------------------------------------------------------
+// The last route CTA: the work plan of every expert batch.  The consumer warps share the SM's four
+// warp schedulers (warp w issues on scheduler w % 4), so the plan balances the schedulers' loads
+// first, then the warps of each scheduler.  Experts are ranked by their count over the call (ties:
+// lower id) and taken in batches of kBatch by rank.  In a batch, an expert with more than a quarter
+// of the batch's work (possible only when the batch has few experts) is cut into 2 or 4 column
+// parts; every part or whole expert is a unit.  The units, by cost (ties: lower index), are dealt
+// in rounds of four: in a round the scheduler with the k-th least load takes the round's k-th
+// unit; then each scheduler deals its units (in the order it took them) to its four warps the same
+// way, one unit per warp and round, so a unit's slot is its round.
+__device__ void build_plan(const int *cnt, int E, int maxlk, int32_t *plan, int *ord, long long *ucost, int *udesc,
+                           int *usort, int *kpart, int *slist, int *sh) {
+  __shared__ long long total;
+  const int t = threadIdx.x, lane = t & 31;
+  for (int e = t; e < E; e += blockDim.x) {   // rank by count (descending), ties by id
+    const int c = cnt[e];
+    int rank = 0;
+    for (int o = 0; o < E; o++) {
+      const int co = cnt[o];
+      rank += (co > c) || (co == c && o < e);
+    }
+    ord[rank] = e;
+  }
+  __syncthreads();
+  const int nbatch = (E + kBatch - 1) / kBatch;
+  for (int b = 0; b < nbatch; b++) {
+    const int ne = min(kBatch, E - b * kBatch);
+    if (t < 32) {
+      long long tot = 0;
+      for (int i = lane; i < ne; i += 32) tot += cnt[ord[b * kBatch + i]];
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+      if (lane == 0) total = tot * unit_cost(0);
+    }
+    __syncthreads();
+    // split factor: 2^lk parts while one part costs more than a quarter of the batch (one
+    // scheduler's share); each part walks all the expert's rows
+    for (int i = t; i < ne; i += blockDim.x) {
+      const long long c = cnt[ord[b * kBatch + i]];
+      int lk = 0;
+      while (lk < maxlk && 4LL * c * unit_cost(lk) > total) lk++;
+      kpart[i] = c > 0 ? lk : -1;
+    }
+    __syncthreads();
+    if (t < 32) {   // unit list in rank order (exclusive scan of the parts per expert)
+      int base = 0;
+      for (int i0 = 0; i0 < ne; i0 += 32) {
+        const int i = i0 + lane;
+        const int lk = i < ne ? kpart[i] : -1;
+        const int n = lk < 0 ? 0 : 1 << lk;
+        int incl = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (n) {
+          const int e = ord[b * kBatch + i];
+          for (int j = 0; j < n; j++) {
+            ucost[base + incl - n + j] = (long long)cnt[e] * unit_cost(lk);
+            udesc[base + incl - n + j] = unit_desc(e, j, lk);
+          }
+        }
+        base += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) sh[0] = base;
+    }
+    __syncthreads();
+    const int nu = sh[0];
+    for (int u = t; u < nu; u += blockDim.x) {   // sort by cost (descending), ties by index
+      const long long c = ucost[u];
+      int rank = 0;
+      for (int v = 0; v < nu; v++) rank += (ucost[v] > c) || (ucost[v] == c && v < u);
+      usort[rank] = u;
+    }
+    __syncthreads();
+    if (t < 32) {
+      // (1) schedulers: lane sb < 4 holds scheduler sb's load; round r takes sorted units 4r..4r+3
+      const int nr = (nu + 3) / 4;
+      long long ld = 0;
+      for (int r = 0; r < nr; r++) {
+        int rk = 0;
+#pragma unroll
+        for (int o = 0; o < 4; o++) {
+          const long long lo = __shfl_sync(0xffffffffu, ld, o);
+          rk += (lo < ld) || (lo == ld && o < lane);
+        }
+        const int u = 4 * r + rk;
+        if (lane < 4) {
+          const int uu = u < nu ? usort[u] : -1;
+          slist[lane * kMaxRounds + r] = uu;
+          if (uu >= 0) ld += ucost[uu];
+        }
+      }
+      // (2) each scheduler's warps: lane = 4 wi + sb; round k takes the scheduler's units 4k..4k+3
+      const int sb = lane & 3, wi = (lane >> 2) & 3;
+      long long wl = 0;
+      for (int k = 0; k < kSlots; k++) {
+        int rk = 0;
+#pragma unroll
+        for (int o = 0; o < 4; o++) {
+          const long long lo = __shfl_sync(0xffffffffu, wl, 4 * o + sb);
+          rk += (lo < wl) || (lo == wl && o < wi);
+        }
+        const int j = 4 * k + rk;   // index in the scheduler's list
+        int d = -1;
+        if (lane < 16 && j < nr) {
+          const int uu = slist[sb * kMaxRounds + j];
+          if (uu >= 0) { d = udesc[uu]; wl += ucost[uu]; }
+        }
+        if (lane < 16) plan[((size_t)b * kMaxConsumers + wi * 4 + sb) * kSlots + k] = d;
+      }
+    }
+    __syncthreads();
+  }
+}
+
 // One CTA per (sub-tile s, chunk k): rows [128 s, 128 s + 128) of chunk k.
 __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__ ids, int64_t tokens, int top_k,
                                                      int E, int64_t rpc, int nsub, SegLayout sl, RouteWs ws,
                                                      unsigned long long *__restrict__ counts,
-                                                     int32_t *__restrict__ status) {
+                                                     int32_t *__restrict__ status, int maxlk) {
   __shared__ uint32_t bm[1024][kSub / 32];   // expert x row bitmap of the sub-tile
   __shared__ int cnt[1024 + 1], off[1024 + 1];
   __shared__ int last;
@@ -171,7 +301,7 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
   __syncthreads();
   uint8_t *seg = ws.seg + ((size_t)k * nsub + s) * sl.bytes;
   int32_t *soff = reinterpret_cast<int32_t *>(seg);
-  uint16_t *srow = reinterpret_cast<uint16_t *>(seg + sl.offb);
+  uint32_t *srow = reinterpret_cast<uint32_t *>(seg + sl.offb);
   for (int e = threadIdx.x; e <= E; e += blockDim.x) soff[e] = off[e];
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int p = off[e];
@@ -181,7 +311,7 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
       while (word) {
         const int bit = __ffs(word) - 1;
         word &= word - 1;
-        srow[p++] = (uint16_t)((w * 32 + bit) * kRowBytes);
+        srow[p++] = (uint32_t)((w * 32 + bit) * kRowBytes);
       }
     }
     while (p & 3) srow[p++] = kZeroOff;
@@ -192,7 +322,7 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
       ws.touched[e] = 1;
     }
   }
-  // the last CTA to finish ranks the experts by their count over the whole call
+  // the last CTA to finish builds the work plan from the counts over the whole call
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) last = atomicAdd(&ws.touched[E], 1) == (int)(gridDim.x * gridDim.y) - 1;
@@ -205,21 +335,21 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
     cnt[e] = c;
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int c = cnt[e];
-    int rank = 0;
-    for (int o = 0; o < E; o++) {
-      const int co = cnt[o];
-      rank += (co > c) || (co == c && o < e);
-    }
-    ws.order[rank] = e;
-  }
+  // scratch for the plan, reusing the bitmap's shared memory (16 KB)
+  int *ord = reinterpret_cast<int *>(&bm[0][0]);              // [1024]
+  long long *ucost = reinterpret_cast<long long *>(ord + 1024); // [4 * kMaxRounds] units
+  int *udesc = reinterpret_cast<int *>(ucost + 4 * kMaxRounds);
+  int *usort = udesc + 4 * kMaxRounds;
+  int *kpart = usort + 4 * kMaxRounds;                         // [kBatch]
+  int *slist = kpart + kBatch;                                 // [4][kMaxRounds]
+  int *sh = slist + 4 * kMaxRounds;                            // [2]
+  build_plan(cnt, E, maxlk, ws.plan, ord, ucost, udesc, usort, kpart, slist, sh);
 }
 
 // ---------------------------------------------------------------------------------------------
 struct AccArgs {
   int64_t tokens, cols, rpc, nchunks;
-  int E, nconsumers, nsub, stage_bytes;
+  int E, nconsumers, nsub, stage_bytes, nstages;
   SegLayout sl;
   RouteWs ws;
   float *in_sum2;
@@ -233,52 +363,128 @@ __device__ __forceinline__ int lds_s32(uint32_t a) {
   asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
   return v;
 }
-__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
-  uint2 v;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
   return v;
 }
 
-// acc[0..CPL) += x^2 for the CPL values of this lane (u: the lane's 8 bytes of one row).  A bf16
-// value's square is exact in fp32, so the mixed-precision FMA (which takes the two halves of a
-// 32-bit register directly) rounds once, as fl(acc + fl(x*x)) does; fp32 values are squared with
-// one rounding and added with another.
-__device__ __forceinline__ void sq_acc(float *acc, uint2 u, __nv_bfloat16) {
-  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %4;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n"
-      " mov.b32 {l, h}, %5;\n fma.rn.f32.bf16 %2, l, l, %2;\n fma.rn.f32.bf16 %3, h, h, %3;\n}\n"
-      : "+f"(acc[0]), "+f"(acc[1]), "+f"(acc[2]), "+f"(acc[3])
-      : "r"(u.x), "r"(u.y));
+// One row's share of a lane: LB bytes (8, 4 or 2).
+template <int LB> struct Lane;
+template <> struct Lane<8> { uint2 v; };
+template <> struct Lane<4> { uint32_t v; };
+template <> struct Lane<2> { uint32_t v; };
+template <int LB> __device__ __forceinline__ Lane<LB> lds_lane(uint32_t a);
+template <> __device__ __forceinline__ Lane<8> lds_lane<8>(uint32_t a) {
+  Lane<8> r;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.v.x), "=r"(r.v.y) : "r"(a));
+  return r;
 }
-__device__ __forceinline__ void sq_acc(float *acc, uint2 u, float) {
-  const float x0 = __uint_as_float(u.x), x1 = __uint_as_float(u.y);
-  acc[0] = __fadd_rn(acc[0], __fmul_rn(x0, x0));
-  acc[1] = __fadd_rn(acc[1], __fmul_rn(x1, x1));
+template <> __device__ __forceinline__ Lane<4> lds_lane<4>(uint32_t a) {
+  Lane<4> r;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r.v) : "r"(a));
+  return r;
 }
-// The 4 rows of a group: their offsets (4 x uint16) in one load, then the rows' values.
-struct Group { uint2 v0, v1, v2, v3; };
-__device__ __forceinline__ Group load_group(uint32_t srow_j, uint32_t tile) {
-  const uint2 o = lds_v2(srow_j);
-  Group g;
-  g.v0 = lds_v2(tile + (o.x & 0xffffu));
-  g.v1 = lds_v2(tile + (o.x >> 16));
-  g.v2 = lds_v2(tile + (o.y & 0xffffu));
-  g.v3 = lds_v2(tile + (o.y >> 16));
-  return g;
+template <> __device__ __forceinline__ Lane<2> lds_lane<2>(uint32_t a) {
+  Lane<2> r;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(r.v) : "r"(a));
+  return r;
+}
+
+// acc += x^2 for the lane's values of one row.  bf16: the square of a bf16 value is exact in fp32,
+// so the mixed-precision FMA (one rounding) equals fl(acc + fl(x*x)); fp32: the square rounded,
+// then added with one more rounding.
+__device__ __forceinline__ void fma_bf16(float &acc, uint32_t h16) {
+  asm("{\n .reg .b16 l;\n cvt.u16.u32 l, %1;\n fma.rn.f32.bf16 %0, l, l, %0;\n}\n" : "+f"(acc) : "r"(h16));
+}
+__device__ __forceinline__ void fma_bf16x2(float &a0, float &a1, uint32_t u) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n}\n"
+      : "+f"(a0), "+f"(a1) : "r"(u));
+}
+__device__ __forceinline__ void sq_add(float &acc, float x) { acc = __fadd_rn(acc, __fmul_rn(x, x)); }
+
+template <typename T, int LB> __device__ __forceinline__ void acc_row(float *acc, const Lane<LB> &r);
+template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 8>(float *acc, const Lane<8> &r) {
+  fma_bf16x2(acc[0], acc[1], r.v.x);
+  fma_bf16x2(acc[2], acc[3], r.v.y);
+}
+template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 4>(float *acc, const Lane<4> &r) {
+  fma_bf16x2(acc[0], acc[1], r.v);
+}
+template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 2>(float *acc, const Lane<2> &r) {
+  fma_bf16(acc[0], r.v);
+}
+template <> __device__ __forceinline__ void acc_row<float, 8>(float *acc, const Lane<8> &r) {
+  sq_add(acc[0], __uint_as_float(r.v.x));
+  sq_add(acc[1], __uint_as_float(r.v.y));
+}
+template <> __device__ __forceinline__ void acc_row<float, 4>(float *acc, const Lane<4> &r) {
+  sq_add(acc[0], __uint_as_float(r.v));
+}
+template <> __device__ __forceinline__ void acc_row<float, 2>(float *acc, const Lane<2> &r) {}
+
+// The rows [0, n) of one unit in this stage (n a multiple of 4; padding rows point at the zero row),
+// in ascending order.  srow: shared address of the unit's first row offset; base: the lane's first
+// byte in the staged tile.  Software pipelined: the next group's offsets and rows are loaded before
+// this group's additions.
+template <typename T, int LB>
+__device__ __forceinline__ void run_unit(float *acc, uint32_t srow, int n, uint32_t base) {
+  // offsets run one group ahead of the rows, the rows one group ahead of the additions
+  const uint4 o = lds_v4(srow);
+  uint4 on = lds_v4(srow + 4 * min(4, n - 4));
+  Lane<LB> r0 = lds_lane<LB>(base + o.x), r1 = lds_lane<LB>(base + o.y), r2 = lds_lane<LB>(base + o.z),
+           r3 = lds_lane<LB>(base + o.w);
+#pragma unroll 1
+  for (int j = 4; j < n; j += 4) {
+    const uint4 onn = lds_v4(srow + 4 * min(j + 4, n - 4));
+    const Lane<LB> n0 = lds_lane<LB>(base + on.x), n1 = lds_lane<LB>(base + on.y), n2 = lds_lane<LB>(base + on.z),
+                   n3 = lds_lane<LB>(base + on.w);
+    acc_row<T, LB>(acc, r0); acc_row<T, LB>(acc, r1); acc_row<T, LB>(acc, r2); acc_row<T, LB>(acc, r3);
+    r0 = n0; r1 = n1; r2 = n2; r3 = n3;
+    on = onn;
+  }
+  acc_row<T, LB>(acc, r0); acc_row<T, LB>(acc, r1); acc_row<T, LB>(acc, r2); acc_row<T, LB>(acc, r3);
+}
+
+// The lane's nv current sums at src (nv = 4, 2 or 1 consecutive floats).
+__device__ __forceinline__ void load_unit(const float *src, float *v, int nv) {
+  if (nv == 4) {
+    const float4 t = *reinterpret_cast<const float4 *>(src);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+  } else if (nv == 2) {
+    const float2 t = *reinterpret_cast<const float2 *>(src);
+    v[0] = t.x; v[1] = t.y;
+  } else {
+    v[0] = src[0];
+  }
+}
+// dst = old + acc (add: in_sum2 += the lane's sums, one rounding each), or dst = acc (the chunk
+// partial, for the ordered combine)
+__device__ __forceinline__ void store_unit(float *dst, const float *acc, const float *old, int nv, bool add) {
+  float o[4];
+#pragma unroll
+  for (int c = 0; c < 4; c++) o[c] = add ? __fadd_rn(old[c], acc[c]) : acc[c];
+  if (nv == 4) *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+  else if (nv == 2) *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
+  else dst[0] = o[0];
 }
 
 template <typename T>
-__global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_kernel(
+__global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulate_kernel(
     const __grid_constant__ CUtensorMap tmap, AccArgs a) {
-  constexpr int CPL = Col<T>::CPL, TILE = Col<T>::TILE;
+  constexpr int TILE = Col<T>::TILE;
+  constexpr int ESZ = (int)sizeof(T);
   constexpr uint32_t kTileBytes = kSub * kRowBytes;
   constexpr uint32_t kSegOff = kTileBytes + kRowBytes;   // after the tile and its zero row
   const uint32_t kStageBytes = (uint32_t)a.stage_bytes;  // tile + zero row + segment, multiple of 128
+  const int NS = a.nstages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   // stage buffers start on a 128-byte boundary (one spare 128 bytes is allocated for this)
   uint8_t *smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
   const uint32_t smem_s = smem_u32(smem);
-  __shared__ uint64_t full_bar[kStages], empty_bar[kStages];
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
   __shared__ int abort_flag;
+  __shared__ int ud[kMaxConsumers][kSlots];  // the consumer warps' work units (from the plan)
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int NW = a.nconsumers;
@@ -289,14 +495,16 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
   const int64_t kbeg = split ? blockIdx.y : 0, kend = split ? blockIdx.y + 1 : a.nchunks;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; s++) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], NW); }
+    for (int s = 0; s < NS; s++) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], NW); }
     abort_flag = 0;
     mbar_fence_init();
   }
   // row kSub of every stage is a zero row: a group of row indices is padded with it (adding +0 to
   // a sum of squares leaves it unchanged)
-  for (int i = threadIdx.x; i < kStages * kRowBytes / 4; i += blockDim.x)
+  for (int i = threadIdx.x; i < NS * kRowBytes / 4; i += blockDim.x)
     reinterpret_cast<uint32_t *>(smem + (size_t)(i / (kRowBytes / 4)) * kStageBytes + kTileBytes)[i % (kRowBytes / 4)] = 0u;
+  for (int i = threadIdx.x; i < kMaxConsumers * kSlots; i += blockDim.x)
+    ud[i / kSlots][i % kSlots] = a.ws.plan[(size_t)blockIdx.z * kMaxConsumers * kSlots + i];
   __syncthreads();
 
   if (warp == NW) {
@@ -308,8 +516,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
         const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
         const int nsub = (int)((rows + kSub - 1) / kSub);
         for (int sub = 0; sub < nsub && ok; sub++, q++) {
-          const int st = (int)(q % kStages);
-          if (q >= kStages) ok = mbar_wait_bounded(&empty_bar[st], (uint32_t)((q / kStages - 1) & 1));
+          const int st = (int)(q % NS);
+          if (q >= NS) ok = mbar_wait_bounded(&empty_bar[st], (uint32_t)((q / NS - 1) & 1));
           if (!ok || *(volatile int *)&abort_flag) { ok = false; break; }
           uint8_t *dst = smem + (size_t)st * kStageBytes;
           mbar_expect_tx(&full_bar[st], kTileBytes + (uint32_t)a.sl.bytes);
@@ -323,81 +531,71 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
         if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
       }
       // every issued copy must land before the CTA's shared memory is released
-      for (int64_t u = q - kStages < 0 ? 0 : q - kStages; u < q; u++)
-        mbar_wait_bounded(&full_bar[u % kStages], (uint32_t)((u / kStages) & 1));
+      for (int64_t u = q - NS < 0 ? 0 : q - NS; u < q; u++)
+        mbar_wait_bounded(&full_bar[u % NS], (uint32_t)((u / NS) & 1));
     }
   } else if (warp < NW) {
-    // ---- consumers ----------------------------------------------------------------------------
-    const int64_t mycol = col0 + lane * CPL;
-    const bool col_ok = mycol < a.cols;
+    // ---- consumers: each warp walks its units (plan) over every stage --------------------------
     int64_t q = 0;
     bool ok = true;
     for (int64_t k = kbeg; k < kend && ok; k++) {
       const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
       const int nsub = (int)((rows + kSub - 1) / kSub);
-      int e_[kSlots], cnt_[kSlots];
-      float acc[kSlots][CPL];
+      float acc[kSlots][4];
+      uint32_t hit = 0;   // slots whose expert has rows in this chunk
 #pragma unroll
-      for (int s = 0; s < kSlots; s++) {
-        const int je = s * NW + ((s & 1) ? NW - 1 - warp : warp);
-        e_[s] = je < ne ? a.ws.order[eb + je] : -1;
+      for (int s = 0; s < kSlots; s++)
 #pragma unroll
-        for (int c = 0; c < CPL; c++) acc[s][c] = 0.0f;
-      }
-#pragma unroll
-      for (int s = 0; s < kSlots; s++) cnt_[s] = e_[s] >= 0 ? a.ws.ccount[(size_t)k * a.E + e_[s]] : 0;
+        for (int c = 0; c < 4; c++) acc[s][c] = 0.0f;
       for (int sub = 0; sub < nsub; sub++, q++) {
-        const int st = (int)(q % kStages);
-        if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((q / kStages) & 1)) || *(volatile int *)&abort_flag) {
+        const int st = (int)(q % NS);
+        if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((q / NS) & 1)) || *(volatile int *)&abort_flag) {
           ok = false;
           break;
         }
         const uint32_t stage = smem_s + (uint32_t)st * kStageBytes;
-        const uint32_t tile = stage + lane * (uint32_t)(CPL * sizeof(T));
         const uint32_t soff = stage + kSegOff, srow = soff + (uint32_t)a.sl.offb;
 #pragma unroll
         for (int s = 0; s < kSlots; s++) {
-          if (cnt_[s] == 0) continue;
-          const int beg = lds_s32(soff + 4 * e_[s]), end = lds_s32(soff + 4 * (e_[s] + 1));
-          // 4 rows at a time (runs are padded to a multiple of 4 with the zero row), software
-          // pipelined: the next group's loads are issued before this group's 4 ordered additions
-          if (beg < end) {
-            Group g = load_group(srow + 2 * beg, tile);
-#pragma unroll 1
-            for (int j = beg + 4; j < end; j += 4) {
-              const Group n = load_group(srow + 2 * j, tile);
-              sq_acc(acc[s], g.v0, T()); sq_acc(acc[s], g.v1, T());
-              sq_acc(acc[s], g.v2, T()); sq_acc(acc[s], g.v3, T());
-              g = n;
-            }
-            sq_acc(acc[s], g.v0, T()); sq_acc(acc[s], g.v1, T());
-            sq_acc(acc[s], g.v2, T()); sq_acc(acc[s], g.v3, T());
-          }
+          const int d = ud[warp][s];
+          if (d < 0) continue;
+          const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
+          const int beg = lds_s32(soff + 4 * e), end = lds_s32(soff + 4 * (e + 1));
+          if (beg >= end) continue;
+          hit |= 1u << s;
+          const uint32_t base = stage + (uint32_t)(j * (kRowBytes >> lk));
+          if (lk == 0) run_unit<T, 8>(acc[s], srow + 4 * beg, end - beg, base + lane * 8);
+          else if (lk == 1) run_unit<T, 4>(acc[s], srow + 4 * beg, end - beg, base + lane * 4);
+          else run_unit<T, 2>(acc[s], srow + 4 * beg, end - beg, base + lane * 2);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);
       }
       if (!ok) break;
-      // chunk done: add the partials to in_sum2 (or store them for the ordered combine)
+      // chunk done: add the partials to in_sum2 (or store them for the ordered combine), for the
+      // experts the chunk routed rows to (every part of an expert sees the same rows).  The
+      // current sums of half the slots at a time are loaded first, so their latencies overlap.
+      auto unit_dst = [&](int s) -> float * {
+        const int d = ud[warp][s];
+        if (d < 0 || !((hit >> s) & 1u)) return nullptr;
+        const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
+        const int64_t c = col0 + (j * (kRowBytes >> lk) + lane * (8 >> lk)) / ESZ;
+        if (c >= a.cols) return nullptr;
+        return split ? a.ws.partial + ((size_t)k * a.E + e) * a.cols + c : a.in_sum2 + (size_t)e * a.cols + c;
+      };
+      constexpr int kHalf = (kSlots + 1) / 2;
 #pragma unroll
-      for (int s = 0; s < kSlots; s++) {
-        if (cnt_[s] == 0 || !col_ok) continue;
-        const float *v = acc[s];
-        if (split) {
-          float *dst = a.ws.partial + ((size_t)k * a.E + e_[s]) * a.cols + mycol;
-          if (CPL == 4) *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-          else *reinterpret_cast<float2 *>(dst) = make_float2(v[0], v[1]);
-        } else {
-          float *dst = a.in_sum2 + (size_t)e_[s] * a.cols + mycol;
-          if (CPL == 4) {
-            float4 o = *reinterpret_cast<float4 *>(dst);
-            o.x = __fadd_rn(o.x, v[0]); o.y = __fadd_rn(o.y, v[1]); o.z = __fadd_rn(o.z, v[2]); o.w = __fadd_rn(o.w, v[3]);
-            *reinterpret_cast<float4 *>(dst) = o;
-          } else {
-            float2 o = *reinterpret_cast<float2 *>(dst);
-            o.x = __fadd_rn(o.x, v[0]); o.y = __fadd_rn(o.y, v[1]);
-            *reinterpret_cast<float2 *>(dst) = o;
-          }
+      for (int h = 0; h < kSlots; h += kHalf) {
+        float old[kHalf][4];
+#pragma unroll
+        for (int s = h; s < h + kHalf && s < kSlots; s++) {
+          const float *p = unit_dst(s);
+          if (p && !split) load_unit(p, old[s - h], (8 >> (ud[warp][s] >> 20)) / ESZ);
+        }
+#pragma unroll
+        for (int s = h; s < h + kHalf && s < kSlots; s++) {
+          float *p = unit_dst(s);
+          if (p) store_unit(p, acc[s], old[s - h], (8 >> (ud[warp][s] >> 20)) / ESZ, !split);
         }
       }
     }
@@ -410,6 +608,7 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1)) imatrix_accumulate_k
   // non-finite check of the touched experts' final sums in this tile (sequential mode; the
   // combine kernel checks in per-chunk mode)
   if (!split && a.status && warp < NW) {
+    constexpr int CPL = 8 / ESZ;
     const int64_t mycol = col0 + lane * CPL;
     int bad = 0;
     for (int je = warp; je < ne; je += NW) {
@@ -470,7 +669,7 @@ static bool make_tmap(CUtensorMap *m, const void *x, iq_dtype dt, int64_t tokens
 
 template <typename T>
 static int launch_accumulate(const CUtensorMap &tm, const AccArgs &a, const Plan &p, cudaStream_t st) {
-  const size_t smem = (size_t)kStages * a.stage_bytes + 128;
+  const size_t smem = (size_t)a.nstages * a.stage_bytes + 128;
   auto kern = imatrix_accumulate_kernel<T>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
@@ -517,14 +716,17 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
   RouteWs ws = route_ws(workspace, p, num_experts, cols);
   if (cudaMemsetAsync(workspace, 0, ws.zero_bytes, st) != cudaSuccess) return IQ_ERR_CUDA;
   imatrix_route<<<dim3((unsigned)p.nsub, (unsigned)p.nchunks), 256, 0, st>>>(
-      expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.nsub, p.seg, ws, (unsigned long long *)counts, status);
+      expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.nsub, p.seg, ws, (unsigned long long *)counts, status,
+      p.maxlk);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   AccArgs a;
   a.tokens = tokens; a.cols = cols; a.rpc = rows_per_chunk; a.nchunks = p.nchunks;
   a.E = num_experts; a.nsub = p.nsub; a.sl = p.seg;
   a.stage_bytes = (kSub * kRowBytes + kRowBytes + p.seg.bytes + 127) & ~127;
-  const int ne = num_experts < kBatch ? num_experts : kBatch;
-  a.nconsumers = (ne + kSlots - 1) / kSlots;
+  a.nstages = (int)(kSmemBudget / (size_t)a.stage_bytes);
+  if (a.nstages > kMaxStages) a.nstages = kMaxStages;
+  if (a.nstages < 2) a.nstages = 2;
+  a.nconsumers = p.nw;
   a.ws = ws; a.in_sum2 = in_sum2; a.status = status;
   const int rc = dt == IQ_BF16 ? launch_accumulate<__nv_bfloat16>(tm, a, p, st) : launch_accumulate<float>(tm, a, p, st);
   if (rc != IQ_OK) return rc;

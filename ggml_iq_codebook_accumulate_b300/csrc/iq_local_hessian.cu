@@ -18,8 +18,12 @@
 // column i of the block in the U products.  The damped group-diagonal blocks of H', the tile's x,
 // dw of the current choices, U and the Q_g(c) table live in shared memory; the off-diagonal panels
 // of H' are read from global memory in coalesced rows (every tile of a column block reads the same
-// 256 KB, which stays in L2).  The dequantized values of every choice come from the decoder, written
-// once into the workspace.  All arithmetic is fp32.
+// 256 KB, which stays in L2).  The dequantized values of every choice are decoded on the fly from
+// the payloads: per tile, each (row, choice) block's bytes are read once and unpacked in shared
+// memory into the groups' local scales d (2s+1)[/8] and the vectors' (entry, signs or shift), and
+// the codebook sits in shared memory, so a value costs a few shared-memory reads and one or two
+// rounded products (the decoder's own arithmetic, so every value is the exact decoded one).  All
+// arithmetic is fp32.
 #include <cmath>
 
 #include "iq_common.cuh"
@@ -30,25 +34,78 @@ constexpr int kLhRows = 16;      // rows per tile
 constexpr int kLhThreads = 256;  // one thread per column of the block
 
 template <int F> struct LhCfg {
-  static constexpr int G = Fmt<F>::G, NC = Fmt<F>::C, GS = 256 / G;
+  static constexpr int G = Fmt<F>::G, NC = Fmt<F>::C, GS = 256 / G, N = Fmt<F>::N;
   static constexpr int GPW = 32 / GS;  // groups a warp handles side by side (1 or 2)
   // Hgg [256][GS], Qe [kLhRows][G][NC], Xs / DWt / U [256][kLhRows], Dl [GS][kLhRows],
-  // Ds [8 warps][32 lanes][NC], cur [kLhRows][G]
+  // Ds [8 warps][32 lanes][NC], cur [kLhRows][G], codebook [N][8], local scales [kLhRows][NC][G],
+  // vector codes [kLhRows][NC][32]
   static constexpr size_t SMEM = 4 * ((size_t)256 * GS + (size_t)kLhRows * G * NC + 3 * 256 * kLhRows +
-                                      GS * kLhRows + 8 * 32 * NC + kLhRows * G) + 64;
+                                      GS * kLhRows + 8 * 32 * NC + kLhRows * G + (size_t)N * 8 +
+                                      (size_t)kLhRows * NC * G + (size_t)kLhRows * NC * 32) + 64;
+  static_assert((size_t)kLhRows * NC * Fmt<F>::BB <= 2 * 256 * kLhRows * 4, "payload bytes fit the staging area");
 };
+
+// Unpacks one (row, choice) block from its payload bytes: the local scale of every group (IQ2
+// d (2s+1) / 8, IQ1 d (2s+1), rounded as the decoder rounds them) and per vector its entry, its
+// 8-bit sign mask (IQ2; bit 7 from even parity for IQ2_XXS / IQ2_XS) and its shift bit (IQ1).
+template <int F>
+__device__ __forceinline__ void lh_unpack(const uint8_t *pb, float *alph, uint32_t *code) {
+  constexpr int G = Fmt<F>::G, VPG = Fmt<F>::VPG;
+  uint32_t d16;
+  if (F == IQ1_M) {
+    d16 = 0;
+#pragma unroll
+    for (int k = 0; k < 4; k++) d16 |= get_bits(pb, f_d16_nib<F>(k)) << (4 * k);
+  } else {
+    d16 = get_bits(pb, f_d16<F>());
+  }
+  const float d = half_bits_to_float((uint16_t)d16);
+  for (int g = 0; g < G; g++) {
+    const int s = (int)get_bits(pb, f_scale<F>(g));
+    alph[g] = Fmt<F>::IQ1 ? __fmul_rn(d, (float)(2 * s + 1)) : __fmul_rn(__fmul_rn(d, (float)(2 * s + 1)), 0.125f);
+  }
+  for (int v = 0; v < 32; v++) {
+    const Bits lo = f_idx_lo<F>(v);
+    const uint32_t idx = get_bits(pb, lo) | (get_bits(pb, f_idx_hi<F>(v)) << lo.width);
+    uint32_t extra = 0;
+    if (!Fmt<F>::IQ1) {
+      uint32_t sg = get_bits(pb, f_sign<F>(v));
+      if (Fmt<F>::PAR) sg |= (uint32_t)parity7((int)sg) << 7;
+      extra = sg << 16;
+    } else {
+      const uint32_t db = F == IQ1_S ? get_bits(pb, f_dbit_grp<F>(v / VPG)) : get_bits(pb, f_dbit_vec<F>(v));
+      extra = db << 24;
+    }
+    code[v] = idx | extra;
+  }
+}
+
+// The decoded value of element i (0..255) of a block from its unpacked scales and codes.
+template <int F>
+__device__ __forceinline__ float lh_value(const float *alph, const uint32_t *code, const float *cbs, int i) {
+  constexpr int GS = 256 / Fmt<F>::G;
+  const uint32_t cd = code[i >> 3];
+  const float gv = cbs[(cd & 0xffffu) * 8 + (i & 7)];
+  const float al = alph[i / GS];
+  if (!Fmt<F>::IQ1) {
+    const float v = __fmul_rn(al, gv);
+    return ((cd >> (16 + (i & 7))) & 1u) ? -v : v;
+  }
+  return __fmul_rn(al, __fadd_rn(gv, (cd >> 24) ? -0.125f : 0.125f));
+}
 
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 template <int F, typename TIn>
-__global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__restrict__ W, int64_t rows, int64_t cols,
-                                                               const float *__restrict__ Q,
+__global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__restrict__ W, int64_t rows, int64_t cols,
+                                                               const uint8_t *__restrict__ payloads,
+                                                               const float *__restrict__ grid,
                                                                const float *__restrict__ H, float perc_damp,
                                                                uint8_t *__restrict__ choices,
                                                                int32_t *__restrict__ status) {
   using Cfg = LhCfg<F>;
-  constexpr int G = Cfg::G, NC = Cfg::NC, GS = Cfg::GS, GPW = Cfg::GPW, R = kLhRows;
+  constexpr int G = Cfg::G, NC = Cfg::NC, GS = Cfg::GS, GPW = Cfg::GPW, R = kLhRows, N = Cfg::N, BB = Fmt<F>::BB;
   extern __shared__ __align__(16) float sm[];
   float *Hgg = sm;                      // Hgg[(g*GS + b)*GS + a] = H'[g*GS + b][g*GS + a]
   float *Qe = Hgg + 256 * GS;           // [R][G][NC]
@@ -58,6 +115,12 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
   float *Dl = U + 256 * R;              // [GS][R] change of dw_g after a move
   float *Ds = Dl + GS * R;              // [8][32][NC] each warp's dw of every choice, for broadcast
   int *cur = reinterpret_cast<int *>(Ds + 8 * 32 * NC);  // [R][G]
+  float *cbs = reinterpret_cast<float *>(cur + R * G);   // [N][8] codebook
+  float *alph = cbs + N * 8;                              // [R][NC][G] local scales
+  uint32_t *code = reinterpret_cast<uint32_t *>(alph + R * NC * G);  // [R][NC][32] vector codes
+  uint8_t *pstage = reinterpret_cast<uint8_t *>(DWt);     // the tile's payload bytes (DWt and U, before use)
+  // decoded value of element i of (row r, choice c) of the tile
+  auto qv = [&](int r, int c, int i) { return lh_value<F>(alph + (r * NC + c) * G, code + (r * NC + c) * 32, cbs, i); };
   __shared__ float red[kLhThreads / 32];
   __shared__ int moved;
 
@@ -66,6 +129,7 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
   const int64_t j = blockIdx.x;
   const float *Hj = H + (size_t)j * 256 * 256;
   const int64_t ntiles = (rows + R - 1) / R;
+  for (int i = tid; i < N * 8; i += kLhThreads) cbs[i] = grid[i];
 
   // damping: lambda = perc_damp * mean(diag(H_bb))
   float dsum = Hj[(size_t)tid * 257];
@@ -95,6 +159,13 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
     // ---- x of the tile ---------------------------------------------------------------------
     for (int r = 0; r < R; r++)
       Xs[tid * R + r] = r < nr ? to_f(W[(size_t)(r0 + r) * cols + j * 256 + tid]) : 0.0f;
+    // ---- every (row, choice) block of the tile: bytes staged, then unpacked --------------------
+    for (int t = tid; t < R * NC * BB; t += kLhThreads) {
+      const int rc = t / BB, bi = t % BB, r = rc / NC, c = rc % NC;
+      pstage[t] = r < nr ? payloads[((size_t)c * rows * nb + (size_t)(r0 + r) * nb + j) * BB + bi] : (uint8_t)0;
+    }
+    __syncthreads();
+    if (tid < R * NC) lh_unpack<F>(pstage + tid * BB, alph + tid * G, code + tid * 32);
     __syncthreads();
     // ---- step 2: Q_g(c) for every (row, group, choice) -------------------------------------
     for (int u = warp; u < R * (G / GPW); u += kLhThreads / 32) {
@@ -108,7 +179,7 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
         float *ds = Ds + warp * 32 * NC;  // lane's row: the NC values of its element
 #pragma unroll
         for (int c = 0; c < NC; c++) {
-          dw[c] = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
+          dw[c] = __fsub_rn(x, qv(r, c, i));
           y[c] = 0.0f;
         }
 #pragma unroll
@@ -152,9 +223,7 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
     {  // dw of the current choices
       const int g = tid / GS;
       for (int r = 0; r < R; r++)
-        DWt[tid * R + r] = r < nr ? __fsub_rn(Xs[tid * R + r],
-                                              Q[((size_t)cur[r * G + g] * rows + r0 + r) * cols + j * 256 + tid])
-                                  : 0.0f;
+        DWt[tid * R + r] = r < nr ? __fsub_rn(Xs[tid * R + r], qv(r, cur[r * G + g], tid)) : 0.0f;
     }
     __syncthreads();
     // ---- U = H'_offdiag dw: thread tid owns column tid (in registers; the visited group's slice is
@@ -206,7 +275,7 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
 #pragma unroll
             for (int st = 0; st < NS; st++) {
               const int c = st * GPW + lane / GS;
-              const float dwc = __fsub_rn(x, Q[((size_t)c * rows + r0 + r) * cols + j * 256 + i]);
+              const float dwc = __fsub_rn(x, qv(r, c, i));
               t[st] = __fmul_rn(__fsub_rn(dwc, dcur), uu);
             }
 #pragma unroll
@@ -230,7 +299,7 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
           if (r < nr && bestc != cc) {
             if (lane < GS) {
               const float x = Xs[i * R + r];
-              const float dwn = __fsub_rn(x, Q[((size_t)bestc * rows + r0 + r) * cols + j * 256 + i]);
+              const float dwn = __fsub_rn(x, qv(r, bestc, i));
               Dl[a * R + r] = __fsub_rn(dwn, DWt[i * R + r]);
               DWt[i * R + r] = dwn;
             }
@@ -269,15 +338,15 @@ __global__ void __launch_bounds__(kLhThreads) lh_search_kernel(const TIn *__rest
 }
 
 template <int F, typename TIn>
-static int run_lh(const void *W, int64_t rows, int64_t cols, const float *Q, const float *H, float perc_damp,
-                  uint8_t *choices, int32_t *status, cudaStream_t st) {
+static int run_lh(const void *W, int64_t rows, int64_t cols, const uint8_t *payloads, const float *grid,
+                  const float *H, float perc_damp, uint8_t *choices, int32_t *status, cudaStream_t st) {
   const size_t smem = LhCfg<F>::SMEM;
   auto kern = lh_search_kernel<F, TIn>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
   const int64_t ntiles = (rows + kLhRows - 1) / kLhRows;
-  const dim3 grid((unsigned)(cols / 256), (unsigned)(ntiles < 65535 ? ntiles : 65535));
-  kern<<<grid, kLhThreads, smem, st>>>((const TIn *)W, rows, cols, Q, H, perc_damp, choices, status);
+  const dim3 grid_dim((unsigned)(cols / 256), (unsigned)(ntiles < 65535 ? ntiles : 65535));
+  kern<<<grid_dim, kLhThreads, smem, st>>>((const TIn *)W, rows, cols, payloads, grid, H, perc_damp, choices, status);
   return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
 }
 
@@ -289,7 +358,7 @@ static int lh_num_choices(iq_format f) { return f == IQ1_M ? 8 : 16; }
 
 extern "C" int iq_local_hessian_workspace_size(iq_format f, int64_t rows, int64_t cols, size_t *bytes) {
   if ((unsigned)f > IQ1_M || rows < 0 || cols <= 0 || cols % 256 || !bytes) return IQ_ERR_ARG;
-  *bytes = (size_t)lh_num_choices(f) * (size_t)rows * (size_t)cols * sizeof(float);
+  *bytes = 0;  // the search decodes the payloads itself and needs no scratch
   return IQ_OK;
 }
 
@@ -305,23 +374,15 @@ extern "C" int iq_local_hessian_choices(iq_format f, const void *W, iq_dtype dt,
   if (nb == 0) return IQ_OK;
   if (!W || !grid || !payloads || !hessian || !choices) return IQ_ERR_ARG;
   if (((uintptr_t)W & 15) || ((uintptr_t)grid & 15) || ((uintptr_t)hessian & 15)) return IQ_ERR_ARG;
-  size_t need = 0;
-  iq_local_hessian_workspace_size(f, rows, cols, &need);
-  if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
+  (void)workspace;
+  (void)workspace_bytes;
   cudaStream_t st = (cudaStream_t)stream;
-  const int NC = lh_num_choices(f);
-  const size_t bb = (size_t)fmt_block_bytes(f);
-  float *Q = (float *)workspace;
-  for (int c = 0; c < NC; c++) {
-    const int rc = iq_decode(f, payloads + (size_t)c * nb * bb, rows, cols, grid, Q + (size_t)c * rows * cols, IQ_F32,
-                             stream);
-    if (rc) return rc;
-  }
   switch (f) {
 #define LH_CASE(FMT)                                                                                      \
   case FMT:                                                                                               \
-    return dt == IQ_BF16 ? run_lh<FMT, __nv_bfloat16>(W, rows, cols, Q, hessian, perc_damp, choices, status, st) \
-                         : run_lh<FMT, float>(W, rows, cols, Q, hessian, perc_damp, choices, status, st);
+    return dt == IQ_BF16                                                                                 \
+               ? run_lh<FMT, __nv_bfloat16>(W, rows, cols, payloads, grid, hessian, perc_damp, choices, status, st) \
+               : run_lh<FMT, float>(W, rows, cols, payloads, grid, hessian, perc_damp, choices, status, st);
     LH_CASE(IQ2_XXS)
     LH_CASE(IQ2_XS)
     LH_CASE(IQ2_S)

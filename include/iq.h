@@ -234,8 +234,8 @@ IQ_API int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, int64
  *   perc_damp  finite, >= 0
  *   choices    device uint8 [B, choice_groups] output
  *   status     IQ_STATUS_BAD_INPUT when a block's damping term is not finite
- *   workspace  device scratch of iq_local_hessian_workspace_size bytes (num_choices * rows * cols
- *              fp32: every choice's decoded weight), 256-byte aligned */
+ *   workspace  unused (iq_local_hessian_workspace_size reports 0 bytes; may be NULL): the search
+ *              decodes the payloads itself, block by block in shared memory */
 IQ_API int iq_local_hessian_workspace_size(iq_format f, int64_t rows, int64_t cols, size_t *bytes);
 IQ_API int iq_local_hessian_choices(iq_format f, const void *W, iq_dtype dt, int64_t rows, int64_t cols,
                                     const float *grid, const uint8_t *payloads, const float *hessian,
