@@ -39,76 +39,91 @@
 
 namespace iqk {
 
-constexpr int kSub = 128;           // rows per stage
-constexpr int kMaxStages = 4;       // shared-memory ring depth (fewer when segments are large)
-constexpr int kRowBytes = 256;      // bytes of one row of a column tile
-constexpr int kSlots = 9;           // work units per consumer warp (the plan needs at most 9)
-constexpr int kMaxRounds = 40;      // dealing rounds per scheduler: at most (kBatch + 9) / 4 units
-constexpr int kMaxConsumers = 16;   // consumer warps per CTA
-constexpr int kBatch = 128;         // experts per pass over x
-constexpr int kMinSeqCtas = 112;    // below this many (tile, batch) CTAs, chunks also run in parallel
+constexpr int kRowBytes = 512;      // bytes of one row of a column tile (256 bf16 / 128 fp32 columns)
+constexpr int kMaxSub = 128;        // rows per stage (64 when the segments are large)
+constexpr int kMaxStages = 4;       // shared-memory ring depth (fewer when stages are large)
+constexpr int kSlots = 6;           // work units per consumer warp
+constexpr int kMaxConsumers = 12;   // consumer warps per CTA: 3 per warp scheduler
+constexpr int kPartUnits = kMaxConsumers * kSlots;  // units one CTA (part) can hold
+constexpr int kMaxParts = 16;       // CTAs that share a column tile, each with its own experts
+constexpr int kMinSeqCtas = 112;    // below this many (tile, part) CTAs, chunks also run in parallel
 constexpr int kMaxTopK = 64;        // bounds the rows a segment holds
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudget = 220 * 1024;
 
 // cost of one (row, unit) pair in half instructions by column split (1, 2 or 4 parts of a row);
 // a unit with more parts covers fewer columns per lane for the same per-row overhead
-__host__ __device__ inline int unit_cost(int lk) { return lk == 0 ? 13 : lk == 1 ? 9 : 7; }
+__host__ __device__ inline int unit_cost(int lk) { return lk == 0 ? 21 : lk == 1 ? 13 : 9; }
 
 template <typename T> struct Col;
-template <> struct Col<__nv_bfloat16> { static constexpr int TILE = 128, MAXLK = 2; };  // up to 4 parts
-template <> struct Col<float> { static constexpr int TILE = 64, MAXLK = 1; };           // up to 2 parts
+template <> struct Col<__nv_bfloat16> { static constexpr int TILE = 256; };
+template <> struct Col<float> { static constexpr int TILE = 128; };
 
 __host__ __device__ inline size_t align256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 __host__ __device__ inline int align16(int n) { return (n + 15) & ~15; }
 
-// A segment (one per chunk and 128-row sub-tile): int32 offsets[E + 1] (padded to 16 bytes), then
-// the rows of expert 0, expert 1, ... as uint32 byte offsets (row * 256) into the staged tile, each
-// run ascending and padded to a multiple of 4 entries with the zero row's offset (kSub * 256).
-constexpr uint32_t kZeroOff = (uint32_t)(kSub * kRowBytes);
+// A segment (one per chunk and sub-tile of `sub` rows): int2 (start, length) per expert (padded to
+// 16 bytes), then the rows of expert 0, expert 1, ... as uint32 byte offsets (row * 512) into the
+// staged tile, each run ascending and padded to a multiple of 4 entries (so a run starts on a
+// 16-byte boundary) with the offset of the zero row that follows the tile.
 struct SegLayout {
-  int offb;   // bytes of the offset table
+  int offb;   // bytes of the (start, length) table
   int bytes;  // segment bytes (multiple of 16)
 };
-__host__ __device__ inline SegLayout seg_layout(int E, int top_k) {
+__host__ __device__ inline SegLayout seg_layout(int E, int top_k, int sub) {
   SegLayout l;
-  l.offb = align16((E + 1) * 4);
-  l.bytes = l.offb + align16(4 * (kSub * (top_k < E ? top_k : E) + 3 * E));
+  l.offb = align16(E * 8);
+  l.bytes = l.offb + align16(4 * (sub * (top_k < E ? top_k : E) + 3 * E));
   return l;
 }
 
-// A work unit of the accumulation: expert e over part j of the 2^lk parts of a tile row (so a
-// heavy expert is spread over several consumer warps, each walking its rows for fewer columns).
-// plan[batch][warp][slot] = e | j << 16 | lk << 20, or -1 (no unit).
+// A work unit of the accumulation: expert e over part j of the 2^lk column parts of a tile row.
+// plan[part][warp][slot] = e | j << 16 | lk << 20, or -1 (no unit).
 __host__ __device__ inline int unit_desc(int e, int j, int lk) { return e | (j << 16) | (lk << 20); }
 
 struct RouteWs {
   int32_t *touched;    // [E]   experts this call routed at least one token to; [E] = CTAs done
   int32_t *ccount;     // [nchunks][E] tokens per (chunk, expert)
-  int32_t *plan;       // [nbatch][kMaxConsumers][kSlots] work units of each consumer warp
+  int32_t *ecount;     // [E]   tokens per expert over the call
+  int32_t *plan;       // [nparts][kMaxConsumers][kSlots] work units of each consumer warp
   uint8_t *seg;        // [nchunks][nsub] segments of seg_bytes
   float *partial;      // [nchunks][E][cols] (per-chunk mode only)
-  size_t zero_bytes;   // bytes from the start to clear before the call (touched + ccount)
+  size_t zero_bytes;   // bytes from the start to clear before the call (touched, ccount, ecount)
 };
 
 struct Plan {
-  int64_t nchunks, ntiles, nbatch;
-  int nsub, nw, maxlk;
+  int64_t nchunks, ntiles;
+  int nsub, sub, nparts, nstages, stage_bytes;
   SegLayout seg;
   bool split;
 };
 
-static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_k, int64_t rpc) {
+static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_k, int64_t rpc, int sms) {
   Plan p;
   p.nchunks = (tokens + rpc - 1) / rpc;
-  p.nsub = (int)((rpc + kSub - 1) / kSub);
-  p.seg = seg_layout(E, top_k);
+  // stages of 128 rows, or 64 when three stages with their segments would not fit
+  p.sub = kMaxSub;
+  for (;;) {
+    p.seg = seg_layout(E, top_k, p.sub);
+    p.stage_bytes = (p.sub * kRowBytes + kRowBytes + p.seg.bytes + 127) & ~127;
+    if (p.sub == 64 || 3 * (size_t)p.stage_bytes <= kSmemBudget) break;
+    p.sub = 64;
+  }
+  p.nstages = (int)(kSmemBudget / (size_t)p.stage_bytes);
+  if (p.nstages > kMaxStages) p.nstages = kMaxStages;
+  if (p.nstages < 2) p.nstages = 2;
+  p.nsub = (int)((rpc + p.sub - 1) / p.sub);
   const int tile = dt == IQ_BF16 ? Col<__nv_bfloat16>::TILE : Col<float>::TILE;
-  p.maxlk = dt == IQ_BF16 ? Col<__nv_bfloat16>::MAXLK : Col<float>::MAXLK;
   p.ntiles = (cols + tile - 1) / tile;
-  p.nbatch = (E + kBatch - 1) / kBatch;
-  p.nw = kMaxConsumers;   // the plan deals over all four schedulers' warps
-  p.split = p.nchunks > 1 && p.ntiles * p.nbatch < kMinSeqCtas;
+  // parts per tile: enough to hold one unit per expert (splits take only the room left), and as
+  // many as fill the SMs (at most one per expert)
+  const int need = (E + kPartUnits - 1) / kPartUnits;
+  int fill = (int)(sms / p.ntiles);
+  if (fill > E) fill = E;
+  if (fill > kMaxParts) fill = kMaxParts;
+  if (fill < 1) fill = 1;
+  p.nparts = need > fill ? need : fill;
+  p.split = p.nchunks > 1 && p.ntiles * p.nparts < kMinSeqCtas;
   return p;
 }
 
@@ -117,150 +132,122 @@ static RouteWs route_ws(void *ws, const Plan &p, int E, int64_t cols) {
   RouteWs r;
   r.touched = (int32_t *)q; q += align256((size_t)(E + 1) * 4);
   r.ccount = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
+  r.ecount = (int32_t *)q; q += align256((size_t)E * 4);
   r.zero_bytes = (size_t)(q - (uint8_t *)ws);
-  r.plan = (int32_t *)q; q += align256((size_t)p.nbatch * kMaxConsumers * kSlots * 4);
+  r.plan = (int32_t *)q; q += align256((size_t)p.nparts * kMaxConsumers * kSlots * 4);
   r.seg = q; q += align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   r.partial = p.split ? (float *)q : nullptr;
   return r;
 }
 static size_t route_ws_bytes(const Plan &p, int E, int64_t cols) {
-  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * 4) +
-             align256((size_t)p.nbatch * kMaxConsumers * kSlots * 4) + align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
+  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * 4) + align256((size_t)E * 4) +
+             align256((size_t)p.nparts * kMaxConsumers * kSlots * 4) +
+             align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   if (p.split) n += align256((size_t)p.nchunks * E * cols * 4);
   return n;
 }
 
 // ---------------------------------------------------------------------------------------------
-// The last route CTA: the work plan of every expert batch.  The consumer warps share the SM's four
-// warp schedulers (warp w issues on scheduler w % 4), so the plan balances the schedulers' loads
-// first, then the warps of each scheduler.  Experts are ranked by their count over the call (ties:
-// lower id) and taken in batches of kBatch by rank.  In a batch, an expert with more than a quarter
-// of the batch's work (possible only when the batch has few experts) is cut into 2 or 4 column
-// parts; every part or whole expert is a unit.  The units, by cost (ties: lower index), are dealt
-// in rounds of four: in a round the scheduler with the k-th least load takes the round's k-th
-// unit; then each scheduler deals its units (in the order it took them) to its four warps the same
-// way, one unit per warp and round, so a unit's slot is its round.
-__device__ void build_plan(const int *cnt, int E, int maxlk, int32_t *plan, int *ord, long long *ucost, int *udesc,
-                           int *usort, int *kpart, int *slist, int *sh) {
-  __shared__ long long total;
-  const int t = threadIdx.x, lane = t & 31;
-  for (int e = t; e < E; e += blockDim.x) {   // rank by count (descending), ties by id
-    const int c = cnt[e];
-    int rank = 0;
-    for (int o = 0; o < E; o++) {
-      const int co = cnt[o];
-      rank += (co > c) || (co == c && o < e);
+__device__ __forceinline__ int snake(int r, int n) {
+  const int q = r / n, m = r - q * n;
+  return (q & 1) ? n - 1 - m : m;
+}
+
+// The last route CTA: the work plan.  Experts are ranked by their count over the call (ties: lower
+// id) with a bitonic sort and dealt to the parts (the CTAs sharing a column tile) in snake order.
+// In a part, an expert whose rows cost more than a sixth of the part's work is cut into 2 or 4
+// column parts while the part has room (one warp's share of the part is a twelfth, and a warp's
+// own pace cannot keep up with more than about twice that); every column part or whole expert is a
+// unit.  A part's units, in rank order, are dealt in snake order to the four warp schedulers (warp w
+// issues on scheduler w % 4) and each scheduler's to its three warps, so heavy and light units mix.
+__device__ void build_plan(const int *cnt, int E, int nparts, int32_t *plan, unsigned long long *key, float *ptot) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
+  int n2 = 1;
+  while (n2 < E) n2 <<= 1;
+  for (int i = t; i < n2; i += blockDim.x)   // ascending keys: larger count first, then lower id
+    key[i] = i < E ? ((unsigned long long)(0x7fffffffu - (uint32_t)cnt[i]) << 32) | (uint32_t)i : ~0ull;
+  for (int i = t; i < kMaxParts; i += blockDim.x) ptot[i] = 0.0f;
+  __syncthreads();
+  for (int k = 2; k <= n2; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = t; i < n2; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = key[i], b = key[l];
+          if (((i & k) == 0) == (a > b)) { key[i] = b; key[l] = a; }
+        }
+      }
+      __syncthreads();
     }
-    ord[rank] = e;
+  // parts in snake order of rank; each part's work (unsplit costs)
+  for (int r = t; r < E; r += blockDim.x) {
+    const int e = (int)(key[r] & 0xffffffffu), c = cnt[e];
+    if (c > 0) atomicAdd(&ptot[snake(r, nparts)], (float)c * (float)unit_cost(0));
   }
   __syncthreads();
-  const int nbatch = (E + kBatch - 1) / kBatch;
-  for (int b = 0; b < nbatch; b++) {
-    const int ne = min(kBatch, E - b * kBatch);
-    if (t < 32) {
-      long long tot = 0;
-      for (int i = lane; i < ne; i += 32) tot += cnt[ord[b * kBatch + i]];
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
-      if (lane == 0) total = tot * unit_cost(0);
-    }
-    __syncthreads();
-    // split factor: 2^lk parts while one part costs more than a quarter of the batch (one
-    // scheduler's share); each part walks all the expert's rows
-    for (int i = t; i < ne; i += blockDim.x) {
-      const long long c = cnt[ord[b * kBatch + i]];
+  // one warp per part: its experts in rank order (ranks p, 2P - 1 - p, 2P + p, ...), split
+  // decisions, unit positions (a scan), and the units dealt to schedulers and warps
+  for (int p = warp; p < nparts; p += nwarps) {
+    for (int i = lane; i < kMaxConsumers * kSlots; i += 32) plan[(size_t)p * kMaxConsumers * kSlots + i] = -1;
+    __syncwarp();
+    const float limit = ptot[p] / 6.0f;
+    const int nexp = (E + nparts - 1) / nparts;        // bound on the part's experts (ranks < E)
+    int base = 0;
+    for (int l0 = 0; l0 < nexp; l0 += 32) {
+      const int l = l0 + lane;
+      int e = 0, c = 0;
+      const int r = l * nparts + ((l & 1) ? nparts - 1 - p : p);
+      if (l < nexp && r < E) {
+        e = (int)(key[r] & 0xffffffffu);
+        c = cnt[e];
+      }
       int lk = 0;
-      while (lk < maxlk && 4LL * c * unit_cost(lk) > total) lk++;
-      kpart[i] = c > 0 ? lk : -1;
-    }
-    __syncthreads();
-    if (t < 32) {   // unit list in rank order (exclusive scan of the parts per expert)
-      int base = 0;
-      for (int i0 = 0; i0 < ne; i0 += 32) {
-        const int i = i0 + lane;
-        const int lk = i < ne ? kpart[i] : -1;
-        const int n = lk < 0 ? 0 : 1 << lk;
-        int incl = n;
+      while (c > 0 && lk < 2 && (float)c * (float)unit_cost(lk) > limit) lk++;
+      int n = c > 0 ? 1 << lk : 0;
+      int incl = n;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int v = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += v;
-        }
-        if (n) {
-          const int e = ord[b * kBatch + i];
-          for (int j = 0; j < n; j++) {
-            ucost[base + incl - n + j] = (long long)cnt[e] * unit_cost(lk);
-            udesc[base + incl - n + j] = unit_desc(e, j, lk);
-          }
-        }
-        base += __shfl_sync(0xffffffffu, incl, 31);
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
       }
-      if (lane == 0) sh[0] = base;
-    }
-    __syncthreads();
-    const int nu = sh[0];
-    for (int u = t; u < nu; u += blockDim.x) {   // sort by cost (descending), ties by index
-      const long long c = ucost[u];
-      int rank = 0;
-      for (int v = 0; v < nu; v++) rank += (ucost[v] > c) || (ucost[v] == c && v < u);
-      usort[rank] = u;
-    }
-    __syncthreads();
-    if (t < 32) {
-      // (1) schedulers: lane sb < 4 holds scheduler sb's load; round r takes sorted units 4r..4r+3
-      const int nr = (nu + 3) / 4;
-      long long ld = 0;
-      for (int r = 0; r < nr; r++) {
-        int rk = 0;
+      // a split must leave room for one unit of every later expert of the part
+      if (n > 1 && base + incl + (nexp - 1 - l) > kPartUnits) { lk = 0; n = 1; }
+      incl = n;
 #pragma unroll
-        for (int o = 0; o < 4; o++) {
-          const long long lo = __shfl_sync(0xffffffffu, ld, o);
-          rk += (lo < ld) || (lo == ld && o < lane);
-        }
-        const int u = 4 * r + rk;
-        if (lane < 4) {
-          const int uu = u < nu ? usort[u] : -1;
-          slist[lane * kMaxRounds + r] = uu;
-          if (uu >= 0) ld += ucost[uu];
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      for (int jj = 0; jj < n; jj++) {
+        const int ui = base + incl - n + jj;           // the unit's index in the part
+        if (ui < kPartUnits) {
+          const int sb = snake(ui, 4), si = ui / 4;
+          const int wi = snake(si, 3), slot = si / 3;
+          plan[((size_t)p * kMaxConsumers + wi * 4 + sb) * kSlots + slot] = unit_desc(e, jj, lk);
         }
       }
-      // (2) each scheduler's warps: lane = 4 wi + sb; round k takes the scheduler's units 4k..4k+3
-      const int sb = lane & 3, wi = (lane >> 2) & 3;
-      long long wl = 0;
-      for (int k = 0; k < kSlots; k++) {
-        int rk = 0;
-#pragma unroll
-        for (int o = 0; o < 4; o++) {
-          const long long lo = __shfl_sync(0xffffffffu, wl, 4 * o + sb);
-          rk += (lo < wl) || (lo == wl && o < wi);
-        }
-        const int j = 4 * k + rk;   // index in the scheduler's list
-        int d = -1;
-        if (lane < 16 && j < nr) {
-          const int uu = slist[sb * kMaxRounds + j];
-          if (uu >= 0) { d = udesc[uu]; wl += ucost[uu]; }
-        }
-        if (lane < 16) plan[((size_t)b * kMaxConsumers + wi * 4 + sb) * kSlots + k] = d;
-      }
+      base += __shfl_sync(0xffffffffu, incl, 31);
     }
-    __syncthreads();
   }
 }
 
-// One CTA per (sub-tile s, chunk k): rows [128 s, 128 s + 128) of chunk k.
+// One CTA per (sub-tile s, chunk k): rows [sub * s, sub * s + sub) of chunk k.
 __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__ ids, int64_t tokens, int top_k,
-                                                     int E, int64_t rpc, int nsub, SegLayout sl, RouteWs ws,
+                                                     int E, int64_t rpc, int nsub, int sub, SegLayout sl, RouteWs ws,
                                                      unsigned long long *__restrict__ counts,
-                                                     int32_t *__restrict__ status, int maxlk) {
-  __shared__ uint32_t bm[1024][kSub / 32];   // expert x row bitmap of the sub-tile
+                                                     int32_t *__restrict__ status, int nparts) {
+  __shared__ uint32_t bm[1024][kMaxSub / 32];   // expert x row bitmap of the sub-tile
   __shared__ int cnt[1024 + 1], off[1024 + 1];
+  __shared__ unsigned long long key[1024];
+  __shared__ float ptot[kMaxParts];
   __shared__ int last;
+  const int words = sub / 32;
   const int s = blockIdx.x;
   const int64_t k = blockIdx.y;
-  const int64_t r0 = k * rpc + (int64_t)s * kSub;
+  const int64_t r0 = k * rpc + (int64_t)s * sub;
   const int64_t rend = min(tokens, (k + 1) * rpc);
-  const int rows = (int)max((int64_t)0, min((int64_t)kSub, rend - r0));
-  for (int i = threadIdx.x; i < E * (kSub / 32); i += blockDim.x) bm[i / (kSub / 32)][i % (kSub / 32)] = 0u;
+  const int rows = (int)max((int64_t)0, min((int64_t)sub, rend - r0));
+  for (int i = threadIdx.x; i < E * words; i += blockDim.x) bm[i / words][i % words] = 0u;
   __syncthreads();
   int st = 0;
   for (int i = threadIdx.x; i < rows * top_k; i += blockDim.x) {
@@ -277,8 +264,7 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
     int c = 0;
-#pragma unroll
-    for (int w = 0; w < kSub / 32; w++) c += __popc(bm[e][w]);
+    for (int w = 0; w < words; w++) c += __popc(bm[e][w]);
     cnt[e] = c;
   }
   __syncthreads();
@@ -296,28 +282,34 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
       if (base + lane < E) off[base + lane] = run + incl - v;
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) off[E] = run;
   }
   __syncthreads();
   uint8_t *seg = ws.seg + ((size_t)k * nsub + s) * sl.bytes;
-  int32_t *soff = reinterpret_cast<int32_t *>(seg);
+  int2 *sse = reinterpret_cast<int2 *>(seg);
   uint32_t *srow = reinterpret_cast<uint32_t *>(seg + sl.offb);
-  for (int e = threadIdx.x; e <= E; e += blockDim.x) soff[e] = off[e];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+  const uint32_t zero_off = (uint32_t)(sub * kRowBytes);
+  // runs: one thread per (expert, bitmap word) writes the word's rows at the word's position in
+  // the expert's run; the last word's thread pads the run to a multiple of 4
+  for (int i = threadIdx.x; i < E * words; i += blockDim.x) {
+    const int e = i / words, w = i % words;
     int p = off[e];
-#pragma unroll
-    for (int w = 0; w < kSub / 32; w++) {
-      uint32_t word = bm[e][w];
-      while (word) {
-        const int bit = __ffs(word) - 1;
-        word &= word - 1;
-        srow[p++] = (uint32_t)((w * 32 + bit) * kRowBytes);
-      }
+    for (int v = 0; v < w; v++) p += __popc(bm[e][v]);
+    uint32_t word = bm[e][w];
+    while (word) {
+      const int bit = __ffs(word) - 1;
+      word &= word - 1;
+      srow[p++] = (uint32_t)((w * 32 + bit) * kRowBytes);
     }
-    while (p & 3) srow[p++] = kZeroOff;
+    if (w == words - 1) {
+      sse[e] = make_int2(off[e], cnt[e]);
+      while (p & 3) srow[p++] = zero_off;
+    }
+  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
     const int c = cnt[e];
     if (c) {
       atomicAdd(&ws.ccount[(size_t)k * E + e], c);
+      atomicAdd(&ws.ecount[e], c);
       atomicAdd(&counts[e], (unsigned long long)c);
       ws.touched[e] = 1;
     }
@@ -329,27 +321,15 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
   __syncthreads();
   if (!last) return;
   __threadfence();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int c = 0;
-    for (int64_t kk = 0; kk < (int64_t)gridDim.y; kk++) c += *(volatile int32_t *)&ws.ccount[(size_t)kk * E + e];
-    cnt[e] = c;
-  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = *(volatile int32_t *)&ws.ecount[e];
   __syncthreads();
-  // scratch for the plan, reusing the bitmap's shared memory (16 KB)
-  int *ord = reinterpret_cast<int *>(&bm[0][0]);              // [1024]
-  long long *ucost = reinterpret_cast<long long *>(ord + 1024); // [4 * kMaxRounds] units
-  int *udesc = reinterpret_cast<int *>(ucost + 4 * kMaxRounds);
-  int *usort = udesc + 4 * kMaxRounds;
-  int *kpart = usort + 4 * kMaxRounds;                         // [kBatch]
-  int *slist = kpart + kBatch;                                 // [4][kMaxRounds]
-  int *sh = slist + 4 * kMaxRounds;                            // [2]
-  build_plan(cnt, E, maxlk, ws.plan, ord, ucost, udesc, usort, kpart, slist, sh);
+  build_plan(cnt, E, nparts, ws.plan, key, ptot);
 }
 
 // ---------------------------------------------------------------------------------------------
 struct AccArgs {
   int64_t tokens, cols, rpc, nchunks;
-  int E, nconsumers, nsub, stage_bytes, nstages;
+  int E, nsub, sub, stage_bytes, nstages;
   SegLayout sl;
   RouteWs ws;
   float *in_sum2;
@@ -358,9 +338,14 @@ struct AccArgs {
 
 // Shared-memory loads through 32-bit shared-window addresses (explicitly the shared state space;
 // volatile so they stay after the stage's mbarrier wait).
-__device__ __forceinline__ int lds_s32(uint32_t a) {
-  int v;
-  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(v) : "r"(a));
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ int2 lds_i2(uint32_t a) {
+  int2 v;
+  asm volatile("ld.shared.v2.s32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
 __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
@@ -369,12 +354,17 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
   return v;
 }
 
-// One row's share of a lane: LB bytes (8, 4 or 2).
+// One row's share of a lane: LB bytes (16, 8 or 4).
 template <int LB> struct Lane;
+template <> struct Lane<16> { uint4 v; };
 template <> struct Lane<8> { uint2 v; };
 template <> struct Lane<4> { uint32_t v; };
-template <> struct Lane<2> { uint32_t v; };
 template <int LB> __device__ __forceinline__ Lane<LB> lds_lane(uint32_t a);
+template <> __device__ __forceinline__ Lane<16> lds_lane<16>(uint32_t a) {
+  Lane<16> r;
+  r.v = lds_v4(a);
+  return r;
+}
 template <> __device__ __forceinline__ Lane<8> lds_lane<8>(uint32_t a) {
   Lane<8> r;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.v.x), "=r"(r.v.y) : "r"(a));
@@ -382,75 +372,76 @@ template <> __device__ __forceinline__ Lane<8> lds_lane<8>(uint32_t a) {
 }
 template <> __device__ __forceinline__ Lane<4> lds_lane<4>(uint32_t a) {
   Lane<4> r;
-  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(r.v) : "r"(a));
-  return r;
-}
-template <> __device__ __forceinline__ Lane<2> lds_lane<2>(uint32_t a) {
-  Lane<2> r;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(r.v) : "r"(a));
+  r.v = lds_u32(a);
   return r;
 }
 
 // acc += x^2 for the lane's values of one row.  bf16: the square of a bf16 value is exact in fp32,
 // so the mixed-precision FMA (one rounding) equals fl(acc + fl(x*x)); fp32: the square rounded,
 // then added with one more rounding.
-__device__ __forceinline__ void fma_bf16(float &acc, uint32_t h16) {
-  asm("{\n .reg .b16 l;\n cvt.u16.u32 l, %1;\n fma.rn.f32.bf16 %0, l, l, %0;\n}\n" : "+f"(acc) : "r"(h16));
-}
 __device__ __forceinline__ void fma_bf16x2(float &a0, float &a1, uint32_t u) {
   asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n}\n"
       : "+f"(a0), "+f"(a1) : "r"(u));
 }
-__device__ __forceinline__ void sq_add(float &acc, float x) { acc = __fadd_rn(acc, __fmul_rn(x, x)); }
-
+__device__ __forceinline__ void sq_add(float &acc, uint32_t u) {
+  const float x = __uint_as_float(u);
+  acc = __fadd_rn(acc, __fmul_rn(x, x));
+}
 template <typename T, int LB> __device__ __forceinline__ void acc_row(float *acc, const Lane<LB> &r);
+template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 16>(float *acc, const Lane<16> &r) {
+  fma_bf16x2(acc[0], acc[1], r.v.x); fma_bf16x2(acc[2], acc[3], r.v.y);
+  fma_bf16x2(acc[4], acc[5], r.v.z); fma_bf16x2(acc[6], acc[7], r.v.w);
+}
 template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 8>(float *acc, const Lane<8> &r) {
-  fma_bf16x2(acc[0], acc[1], r.v.x);
-  fma_bf16x2(acc[2], acc[3], r.v.y);
+  fma_bf16x2(acc[0], acc[1], r.v.x); fma_bf16x2(acc[2], acc[3], r.v.y);
 }
 template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 4>(float *acc, const Lane<4> &r) {
   fma_bf16x2(acc[0], acc[1], r.v);
 }
-template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 2>(float *acc, const Lane<2> &r) {
-  fma_bf16(acc[0], r.v);
+template <> __device__ __forceinline__ void acc_row<float, 16>(float *acc, const Lane<16> &r) {
+  sq_add(acc[0], r.v.x); sq_add(acc[1], r.v.y); sq_add(acc[2], r.v.z); sq_add(acc[3], r.v.w);
 }
 template <> __device__ __forceinline__ void acc_row<float, 8>(float *acc, const Lane<8> &r) {
-  sq_add(acc[0], __uint_as_float(r.v.x));
-  sq_add(acc[1], __uint_as_float(r.v.y));
+  sq_add(acc[0], r.v.x); sq_add(acc[1], r.v.y);
 }
-template <> __device__ __forceinline__ void acc_row<float, 4>(float *acc, const Lane<4> &r) {
-  sq_add(acc[0], __uint_as_float(r.v));
-}
-template <> __device__ __forceinline__ void acc_row<float, 2>(float *acc, const Lane<2> &r) {}
+template <> __device__ __forceinline__ void acc_row<float, 4>(float *acc, const Lane<4> &r) { sq_add(acc[0], r.v); }
 
-// The rows [0, n) of one unit in this stage (n a multiple of 4; padding rows point at the zero row),
-// in ascending order.  srow: shared address of the unit's first row offset; base: the lane's first
-// byte in the staged tile.  Software pipelined: the next group's offsets and rows are loaded before
-// this group's additions.
+// The n rows of one unit in this stage, in ascending order.  srow: shared address of the unit's
+// first row offset (16-byte aligned); base: the lane's first byte in the staged tile.  Whole groups
+// of 4 rows are software pipelined (offsets one group ahead of the rows, rows one group ahead of
+// the additions); the last n % 4 rows follow one by one.
 template <typename T, int LB>
 __device__ __forceinline__ void run_unit(float *acc, uint32_t srow, int n, uint32_t base) {
-  // offsets run one group ahead of the rows, the rows one group ahead of the additions
-  const uint4 o = lds_v4(srow);
-  uint4 on = lds_v4(srow + 4 * min(4, n - 4));
-  Lane<LB> r0 = lds_lane<LB>(base + o.x), r1 = lds_lane<LB>(base + o.y), r2 = lds_lane<LB>(base + o.z),
-           r3 = lds_lane<LB>(base + o.w);
+  const int n4 = n & ~3;
+  if (n4) {
+    const uint4 o = lds_v4(srow);
+    uint4 on = lds_v4(srow + 4 * min(4, n4 - 4));
+    Lane<LB> r0 = lds_lane<LB>(base + o.x), r1 = lds_lane<LB>(base + o.y), r2 = lds_lane<LB>(base + o.z),
+             r3 = lds_lane<LB>(base + o.w);
 #pragma unroll 1
-  for (int j = 4; j < n; j += 4) {
-    const uint4 onn = lds_v4(srow + 4 * min(j + 4, n - 4));
-    const Lane<LB> n0 = lds_lane<LB>(base + on.x), n1 = lds_lane<LB>(base + on.y), n2 = lds_lane<LB>(base + on.z),
-                   n3 = lds_lane<LB>(base + on.w);
+    for (int j = 4; j < n4; j += 4) {
+      const uint4 onn = lds_v4(srow + 4 * min(j + 4, n4 - 4));
+      const Lane<LB> n0 = lds_lane<LB>(base + on.x), n1 = lds_lane<LB>(base + on.y), n2 = lds_lane<LB>(base + on.z),
+                     n3 = lds_lane<LB>(base + on.w);
+      acc_row<T, LB>(acc, r0); acc_row<T, LB>(acc, r1); acc_row<T, LB>(acc, r2); acc_row<T, LB>(acc, r3);
+      r0 = n0; r1 = n1; r2 = n2; r3 = n3;
+      on = onn;
+    }
     acc_row<T, LB>(acc, r0); acc_row<T, LB>(acc, r1); acc_row<T, LB>(acc, r2); acc_row<T, LB>(acc, r3);
-    r0 = n0; r1 = n1; r2 = n2; r3 = n3;
-    on = onn;
   }
-  acc_row<T, LB>(acc, r0); acc_row<T, LB>(acc, r1); acc_row<T, LB>(acc, r2); acc_row<T, LB>(acc, r3);
+#pragma unroll 1
+  for (int j = n4; j < n; j++) acc_row<T, LB>(acc, lds_lane<LB>(base + lds_u32(srow + 4 * j)));
 }
 
-// The lane's nv current sums at src (nv = 4, 2 or 1 consecutive floats).
+// The lane's nv current sums at src (nv = 8, 4, 2 or 1 consecutive floats, 16-byte aligned when 4+).
 __device__ __forceinline__ void load_unit(const float *src, float *v, int nv) {
-  if (nv == 4) {
+  if (nv >= 4) {
     const float4 t = *reinterpret_cast<const float4 *>(src);
     v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+    if (nv == 8) {
+      const float4 u = *reinterpret_cast<const float4 *>(src + 4);
+      v[4] = u.x; v[5] = u.y; v[6] = u.z; v[7] = u.w;
+    }
   } else if (nv == 2) {
     const float2 t = *reinterpret_cast<const float2 *>(src);
     v[0] = t.x; v[1] = t.y;
@@ -459,14 +450,23 @@ __device__ __forceinline__ void load_unit(const float *src, float *v, int nv) {
   }
 }
 // dst = old + acc (add: in_sum2 += the lane's sums, one rounding each), or dst = acc (the chunk
-// partial, for the ordered combine)
-__device__ __forceinline__ void store_unit(float *dst, const float *acc, const float *old, int nv, bool add) {
-  float o[4];
+// partial, for the ordered combine).  Returns whether every stored value is finite.
+__device__ __forceinline__ bool store_unit(float *dst, const float *acc, const float *old, int nv, bool add) {
+  float o[8];
 #pragma unroll
-  for (int c = 0; c < 4; c++) o[c] = add ? __fadd_rn(old[c], acc[c]) : acc[c];
-  if (nv == 4) *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-  else if (nv == 2) *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
-  else dst[0] = o[0];
+  for (int c = 0; c < 8; c++) o[c] = add ? __fadd_rn(old[c], acc[c]) : acc[c];
+  bool fin = true;
+  if (nv >= 4) {
+    *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+    if (nv == 8) *reinterpret_cast<float4 *>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+  } else if (nv == 2) {
+    *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
+  } else {
+    dst[0] = o[0];
+  }
+#pragma unroll
+  for (int c = 0; c < 8; c++) fin &= c >= nv || isfinite(o[c]);
+  return fin;
 }
 
 template <typename T>
@@ -474,8 +474,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
     const __grid_constant__ CUtensorMap tmap, AccArgs a) {
   constexpr int TILE = Col<T>::TILE;
   constexpr int ESZ = (int)sizeof(T);
-  constexpr uint32_t kTileBytes = kSub * kRowBytes;
-  constexpr uint32_t kSegOff = kTileBytes + kRowBytes;   // after the tile and its zero row
+  const uint32_t kTileBytes = (uint32_t)(a.sub * kRowBytes);
+  const uint32_t kSegOff = kTileBytes + kRowBytes;       // after the tile and its zero row
   const uint32_t kStageBytes = (uint32_t)a.stage_bytes;  // tile + zero row + segment, multiple of 128
   const int NS = a.nstages;
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -487,10 +487,8 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
   __shared__ int ud[kMaxConsumers][kSlots];  // the consumer warps' work units (from the plan)
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int NW = a.nconsumers;
+  constexpr int NW = kMaxConsumers;
   const int64_t col0 = (int64_t)blockIdx.x * TILE;
-  const int eb = blockIdx.z * kBatch;
-  const int ne = min(kBatch, a.E - eb);
   const bool split = a.ws.partial != nullptr;
   const int64_t kbeg = split ? blockIdx.y : 0, kend = split ? blockIdx.y + 1 : a.nchunks;
 
@@ -499,12 +497,11 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
     abort_flag = 0;
     mbar_fence_init();
   }
-  // row kSub of every stage is a zero row: a group of row indices is padded with it (adding +0 to
-  // a sum of squares leaves it unchanged)
+  // the row after the tile in every stage is a zero row: a group of row offsets is padded with it
   for (int i = threadIdx.x; i < NS * kRowBytes / 4; i += blockDim.x)
     reinterpret_cast<uint32_t *>(smem + (size_t)(i / (kRowBytes / 4)) * kStageBytes + kTileBytes)[i % (kRowBytes / 4)] = 0u;
-  for (int i = threadIdx.x; i < kMaxConsumers * kSlots; i += blockDim.x)
-    ud[i / kSlots][i % kSlots] = a.ws.plan[(size_t)blockIdx.z * kMaxConsumers * kSlots + i];
+  for (int i = threadIdx.x; i < NW * kSlots; i += blockDim.x)
+    ud[i / kSlots][i % kSlots] = a.ws.plan[(size_t)blockIdx.z * NW * kSlots + i];
   __syncthreads();
 
   if (warp == NW) {
@@ -514,14 +511,14 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
       bool ok = true;
       for (int64_t k = kbeg; k < kend && ok; k++) {
         const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
-        const int nsub = (int)((rows + kSub - 1) / kSub);
+        const int nsub = (int)((rows + a.sub - 1) / a.sub);
         for (int sub = 0; sub < nsub && ok; sub++, q++) {
           const int st = (int)(q % NS);
           if (q >= NS) ok = mbar_wait_bounded(&empty_bar[st], (uint32_t)((q / NS - 1) & 1));
           if (!ok || *(volatile int *)&abort_flag) { ok = false; break; }
           uint8_t *dst = smem + (size_t)st * kStageBytes;
           mbar_expect_tx(&full_bar[st], kTileBytes + (uint32_t)a.sl.bytes);
-          tma_load_2d(dst, &tmap, (int)col0, (int)(k * a.rpc + (int64_t)sub * kSub), &full_bar[st]);
+          tma_load_2d(dst, &tmap, (int)col0, (int)(k * a.rpc + (int64_t)sub * a.sub), &full_bar[st]);
           bulk_copy_g2s(dst + kSegOff, a.ws.seg + ((size_t)k * a.nsub + sub) * a.sl.bytes, (uint32_t)a.sl.bytes,
                         &full_bar[st]);
         }
@@ -534,19 +531,19 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
       for (int64_t u = q - NS < 0 ? 0 : q - NS; u < q; u++)
         mbar_wait_bounded(&full_bar[u % NS], (uint32_t)((u / NS) & 1));
     }
-  } else if (warp < NW) {
+  } else {
     // ---- consumers: each warp walks its units (plan) over every stage --------------------------
     int64_t q = 0;
-    bool ok = true;
+    bool ok = true, fin = true;
     for (int64_t k = kbeg; k < kend && ok; k++) {
       const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
-      const int nsub = (int)((rows + kSub - 1) / kSub);
-      float acc[kSlots][4];
+      const int nsub = (int)((rows + a.sub - 1) / a.sub);
+      float acc[kSlots][8];
       uint32_t hit = 0;   // slots whose expert has rows in this chunk
 #pragma unroll
       for (int s = 0; s < kSlots; s++)
 #pragma unroll
-        for (int c = 0; c < 4; c++) acc[s][c] = 0.0f;
+        for (int c = 0; c < 8; c++) acc[s][c] = 0.0f;
       for (int sub = 0; sub < nsub; sub++, q++) {
         const int st = (int)(q % NS);
         if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((q / NS) & 1)) || *(volatile int *)&abort_flag) {
@@ -554,19 +551,19 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
           break;
         }
         const uint32_t stage = smem_s + (uint32_t)st * kStageBytes;
-        const uint32_t soff = stage + kSegOff, srow = soff + (uint32_t)a.sl.offb;
+        const uint32_t sse = stage + kSegOff, srow = sse + (uint32_t)a.sl.offb;
 #pragma unroll
         for (int s = 0; s < kSlots; s++) {
           const int d = ud[warp][s];
           if (d < 0) continue;
           const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
-          const int beg = lds_s32(soff + 4 * e), end = lds_s32(soff + 4 * (e + 1));
-          if (beg >= end) continue;
+          const int2 se = lds_i2(sse + 8 * e);
+          if (se.y == 0) continue;
           hit |= 1u << s;
           const uint32_t base = stage + (uint32_t)(j * (kRowBytes >> lk));
-          if (lk == 0) run_unit<T, 8>(acc[s], srow + 4 * beg, end - beg, base + lane * 8);
-          else if (lk == 1) run_unit<T, 4>(acc[s], srow + 4 * beg, end - beg, base + lane * 4);
-          else run_unit<T, 2>(acc[s], srow + 4 * beg, end - beg, base + lane * 2);
+          if (lk == 0) run_unit<T, 16>(acc[s], srow + 4 * se.x, se.y, base + lane * 16);
+          else if (lk == 1) run_unit<T, 8>(acc[s], srow + 4 * se.x, se.y, base + lane * 8);
+          else run_unit<T, 4>(acc[s], srow + 4 * se.x, se.y, base + lane * 4);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);
@@ -579,23 +576,23 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
         const int d = ud[warp][s];
         if (d < 0 || !((hit >> s) & 1u)) return nullptr;
         const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
-        const int64_t c = col0 + (j * (kRowBytes >> lk) + lane * (8 >> lk)) / ESZ;
+        const int64_t c = col0 + (j * (kRowBytes >> lk) + lane * (16 >> lk)) / ESZ;
         if (c >= a.cols) return nullptr;
         return split ? a.ws.partial + ((size_t)k * a.E + e) * a.cols + c : a.in_sum2 + (size_t)e * a.cols + c;
       };
       constexpr int kHalf = (kSlots + 1) / 2;
 #pragma unroll
       for (int h = 0; h < kSlots; h += kHalf) {
-        float old[kHalf][4];
+        float old[kHalf][8];
 #pragma unroll
         for (int s = h; s < h + kHalf && s < kSlots; s++) {
           const float *p = unit_dst(s);
-          if (p && !split) load_unit(p, old[s - h], (8 >> (ud[warp][s] >> 20)) / ESZ);
+          if (p && !split) load_unit(p, old[s - h], (16 >> (ud[warp][s] >> 20)) / ESZ);
         }
 #pragma unroll
         for (int s = h; s < h + kHalf && s < kSlots; s++) {
           float *p = unit_dst(s);
-          if (p) store_unit(p, acc[s], old[s - h], (8 >> (ud[warp][s] >> 20)) / ESZ, !split);
+          if (p) fin &= store_unit(p, acc[s], old[s - h], (16 >> (ud[warp][s] >> 20)) / ESZ, !split);
         }
       }
     }
@@ -603,23 +600,12 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
       atomicExch(&abort_flag, 1);
       if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
     }
+    // non-finite sums of the touched experts (sequential mode: every touched expert's columns of
+    // this tile were stored by their unit's lanes at least once, the last time with the final
+    // sum; the combine kernel checks in per-chunk mode)
+    if (!split && a.status && __any_sync(0xffffffffu, !fin) && lane == 0) atomicOr(a.status, IQ_STATUS_NONFINITE_SUM2);
   }
   __syncthreads();
-  // non-finite check of the touched experts' final sums in this tile (sequential mode; the
-  // combine kernel checks in per-chunk mode)
-  if (!split && a.status && warp < NW) {
-    constexpr int CPL = 8 / ESZ;
-    const int64_t mycol = col0 + lane * CPL;
-    int bad = 0;
-    for (int je = warp; je < ne; je += NW) {
-      const int e = eb + je;
-      if (!a.ws.touched[e] || mycol >= a.cols) continue;
-      const float *v = a.in_sum2 + (size_t)e * a.cols + mycol;
-#pragma unroll
-      for (int c = 0; c < CPL; c++) bad |= !isfinite(v[c]);
-    }
-    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, IQ_STATUS_NONFINITE_SUM2);
-  }
 }
 
 // per-chunk mode: in_sum2 += partial[k] for k = 0, 1, ... (experts the chunk routed tokens to)
@@ -640,7 +626,7 @@ __global__ void __launch_bounds__(256) imatrix_combine(int64_t cols, int E, int6
 }
 
 // ---------------------------------------------------------------------------------------------
-// Host: 2-D tensor map of x ([tokens, cols], row-major) with a box of 256 bytes x kSub rows.
+// Host: 2-D tensor map of x ([tokens, cols], row-major) with a box of 512 bytes x `sub` rows.
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -654,13 +640,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-static bool make_tmap(CUtensorMap *m, const void *x, iq_dtype dt, int64_t tokens, int64_t cols) {
+static bool make_tmap(CUtensorMap *m, const void *x, iq_dtype dt, int64_t tokens, int64_t cols, int sub) {
   auto fn = encode_fn();
   if (!fn) return false;
   const int esz = dt == IQ_BF16 ? 2 : 4;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)tokens};
   cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
-  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esz), (cuuint32_t)kSub};
+  cuuint32_t box[2] = {(cuuint32_t)(kRowBytes / esz), (cuuint32_t)sub};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, dt == IQ_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
             const_cast<void *>(x), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -673,10 +659,14 @@ static int launch_accumulate(const CUtensorMap &tm, const AccArgs &a, const Plan
   auto kern = imatrix_accumulate_kernel<T>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
-  dim3 grid((unsigned)p.ntiles, p.split ? (unsigned)p.nchunks : 1u, (unsigned)p.nbatch);
-  kern<<<grid, 32 * (a.nconsumers + 1), smem, st>>>(tm, a);
+  dim3 grid((unsigned)p.ntiles, p.split ? (unsigned)p.nchunks : 1u, (unsigned)p.nparts);
+  kern<<<grid, 32 * (kMaxConsumers + 1), smem, st>>>(tm, a);
   return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
 }
+
+// The plan is laid out for this many SMs (the B300's count), so that the workspace size does not
+// depend on the device the call runs on; another count changes only how well the CTAs fill it.
+constexpr int kPlanSms = 148;
 
 }  // namespace iqk
 
@@ -687,7 +677,7 @@ extern "C" int iq_imatrix_workspace_size(int64_t tokens, int64_t cols, iq_dtype 
   if (!bytes || tokens < 0 || cols <= 0 || (dt != IQ_F32 && dt != IQ_BF16) || num_experts <= 0 ||
       num_experts > 1024 || top_k < 1 || top_k > kMaxTopK || rows_per_chunk <= 0 || rows_per_chunk > 4096)
     return IQ_ERR_ARG;
-  const Plan p = make_plan(tokens, cols, dt, num_experts, top_k, rows_per_chunk);
+  const Plan p = make_plan(tokens, cols, dt, num_experts, top_k, rows_per_chunk, kPlanSms);
   *bytes = route_ws_bytes(p, num_experts, cols);
   return IQ_OK;
 }
@@ -709,24 +699,21 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
   iq_imatrix_workspace_size(tokens, cols, dt, num_experts, top_k, rows_per_chunk, &need);
   if (!workspace || workspace_bytes < need || ((uintptr_t)workspace & 255)) return IQ_ERR_WORKSPACE;
   if (tokens == 0) return IQ_OK;
-  const Plan p = make_plan(tokens, cols, dt, num_experts, top_k, rows_per_chunk);
+  const Plan p = make_plan(tokens, cols, dt, num_experts, top_k, rows_per_chunk, kPlanSms);
   CUtensorMap tm;
-  if (!make_tmap(&tm, x, dt, tokens, cols)) return IQ_ERR_CUDA;
+  if (!make_tmap(&tm, x, dt, tokens, cols, p.sub)) return IQ_ERR_CUDA;
   cudaStream_t st = (cudaStream_t)stream;
   RouteWs ws = route_ws(workspace, p, num_experts, cols);
   if (cudaMemsetAsync(workspace, 0, ws.zero_bytes, st) != cudaSuccess) return IQ_ERR_CUDA;
   imatrix_route<<<dim3((unsigned)p.nsub, (unsigned)p.nchunks), 256, 0, st>>>(
-      expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.nsub, p.seg, ws, (unsigned long long *)counts, status,
-      p.maxlk);
+      expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.nsub, p.sub, p.seg, ws, (unsigned long long *)counts,
+      status, p.nparts);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   AccArgs a;
   a.tokens = tokens; a.cols = cols; a.rpc = rows_per_chunk; a.nchunks = p.nchunks;
-  a.E = num_experts; a.nsub = p.nsub; a.sl = p.seg;
-  a.stage_bytes = (kSub * kRowBytes + kRowBytes + p.seg.bytes + 127) & ~127;
-  a.nstages = (int)(kSmemBudget / (size_t)a.stage_bytes);
-  if (a.nstages > kMaxStages) a.nstages = kMaxStages;
-  if (a.nstages < 2) a.nstages = 2;
-  a.nconsumers = p.nw;
+  a.E = num_experts; a.nsub = p.nsub; a.sub = p.sub; a.sl = p.seg;
+  a.stage_bytes = p.stage_bytes;
+  a.nstages = p.nstages;
   a.ws = ws; a.in_sum2 = in_sum2; a.status = status;
   const int rc = dt == IQ_BF16 ? launch_accumulate<__nv_bfloat16>(tm, a, p, st) : launch_accumulate<float>(tm, a, p, st);
   if (rc != IQ_OK) return rc;
