@@ -8,31 +8,35 @@
 // Definition computed (bit for bit): for each chunk of rows_per_chunk tokens and each expert e the
 // chunk routes tokens to, partial[e][j] starts at +0 and, over those tokens in ascending order,
 // becomes fl(partial + fl(x*x)) -- the square rounded to fp32, then added with one more rounding
-// (for bf16 activations the square is exact, so this is the exact square added with one
-// rounding); then in_sum2[e][j] = fl(in_sum2[e][j] + partial[e][j]), chunk by chunk.
+// (for both input types: a bf16 square is exact in fp32 unless it falls below the normal range,
+// where it rounds too); then in_sum2[e][j] = fl(in_sum2[e][j] + partial[e][j]), chunk by chunk.
 //
 // Kernels per call:
-//  route       one CTA per (chunk, 128-row sub-tile): builds the sub-tile's expert bitmap in shared
-//              memory (a token's ids are a set) and writes the sub-tile's segment: for every expert
-//              the offset of its rows and the rows themselves (as 32-bit byte offsets into a staged
-//              tile, ascending, each run padded to a multiple of 4 with the offset of a zero row);
-//              per-chunk counts are added atomically, and the last CTA to finish plans the work:
-//              experts ranked by their count over the whole call, heavy ones cut into 2 or 4 column
-//              parts, and the resulting units dealt to the consumer warps so that their loads match
-//              (the same plan for every chunk, so each (expert, column) sum has one owner);
-//  accumulate  one CTA per column tile (128 bf16 / 64 fp32 columns, 256 bytes of a row) and,
-//              when there are too few tiles to fill the GPU, per chunk as well.  A producer warp
-//              streams the tile's rows through a ring of up to 4 shared-memory stages: each stage is
-//              one 2-D TMA tensor copy of 128 rows plus one bulk copy of the sub-tile's segment,
-//              both completing on the stage's mbarrier (waits bounded by the global timer).  Each
-//              consumer warp walks its units' rows 4 at a time from shared memory (a unit's lane
-//              reads 8, 4 or 2 bytes of a row) and keeps one register accumulator per (unit,
-//              column of its lane);
+//  route       one CTA per (chunk, sub-tile of 128 or 64 rows): builds the sub-tile's expert bitmap
+//              in shared memory (a token's ids are a set) and writes the sub-tile's segment: for
+//              every expert the offset and length of its run of rows, then the runs themselves
+//              (32-bit byte offsets into a staged tile, ascending, each run padded to a multiple
+//              of 4 with the offset of a zero row); counts per (chunk, expert) and per expert over
+//              the call are added atomically;
+//  accumulate  one CTA per (column tile of 512 bytes: 256 bf16 / 128 fp32 columns, part) and, when
+//              there are too few to fill the GPU, per chunk as well; the parts split the experts.
+//              Launched as a programmatic dependent of the route kernel, it sets up while that
+//              runs.  A producer warp streams the tile's rows through a ring of up to 4
+//              shared-memory stages: each stage is one 2-D TMA tensor copy of the sub-tile's rows
+//              plus one bulk copy of its segment, both completing on the stage's mbarrier (all
+//              waits bounded by the global timer).  Meanwhile the 12 consumer warps plan their
+//              part (ranked experts, heavy ones cut into 2 or 4 column parts, units dealt so the
+//              warps' loads match); then each walks its units' rows, 4 at a time, from shared
+//              memory (a unit's lane reads 16, 8 or 4 bytes of a row) into one register
+//              accumulator per (unit, column of its lane).  For bf16, two screening warps check
+//              each landed stage for values whose squares are inexact in fp32; stages without
+//              any take one mixed-precision FMA per value, the others square and add separately;
 //  combine     (per-chunk mode only) adds the chunk partials to in_sum2 in chunk order.
 // No atomics touch in_sum2, so the sums are the sequential definition above.
 #include <cudaTypedefs.h>
 
 #include <climits>
+#include <type_traits>
 #include <mutex>
 
 #include "iq_common.cuh"
@@ -78,14 +82,13 @@ __host__ __device__ inline SegLayout seg_layout(int E, int top_k, int sub) {
 }
 
 // A work unit of the accumulation: expert e over part j of the 2^lk column parts of a tile row.
-// plan[part][warp][slot] = e | j << 16 | lk << 20, or -1 (no unit).
+// A consumer warp's plan slot holds e | j << 16 | lk << 20, or -1 (no unit).
 __host__ __device__ inline int unit_desc(int e, int j, int lk) { return e | (j << 16) | (lk << 20); }
 
 struct RouteWs {
-  int32_t *touched;    // [E]   experts this call routed at least one token to; [E] = CTAs done
+  int32_t *touched;    // [E]   experts this call routed at least one token to
   int32_t *ccount;     // [nchunks][E] tokens per (chunk, expert)
   int32_t *ecount;     // [E]   tokens per expert over the call
-  int32_t *plan;       // [nparts][kMaxConsumers][kSlots] work units of each consumer warp
   uint8_t *seg;        // [nchunks][nsub] segments of seg_bytes
   float *partial;      // [nchunks][E][cols] (per-chunk mode only)
   size_t zero_bytes;   // bytes from the start to clear before the call (touched, ccount, ecount)
@@ -130,77 +133,73 @@ static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_
 static RouteWs route_ws(void *ws, const Plan &p, int E, int64_t cols) {
   uint8_t *q = (uint8_t *)ws;
   RouteWs r;
-  r.touched = (int32_t *)q; q += align256((size_t)(E + 1) * 4);
+  r.touched = (int32_t *)q; q += align256((size_t)E * 4);
   r.ccount = (int32_t *)q; q += align256((size_t)p.nchunks * E * 4);
   r.ecount = (int32_t *)q; q += align256((size_t)E * 4);
   r.zero_bytes = (size_t)(q - (uint8_t *)ws);
-  r.plan = (int32_t *)q; q += align256((size_t)p.nparts * kMaxConsumers * kSlots * 4);
   r.seg = q; q += align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   r.partial = p.split ? (float *)q : nullptr;
   return r;
 }
 static size_t route_ws_bytes(const Plan &p, int E, int64_t cols) {
-  size_t n = align256((size_t)(E + 1) * 4) + align256((size_t)p.nchunks * E * 4) + align256((size_t)E * 4) +
-             align256((size_t)p.nparts * kMaxConsumers * kSlots * 4) +
+  size_t n = align256((size_t)E * 4) + align256((size_t)p.nchunks * E * 4) + align256((size_t)E * 4) +
              align256((size_t)p.nchunks * p.nsub * p.seg.bytes);
   if (p.split) n += align256((size_t)p.nchunks * E * cols * 4);
   return n;
 }
 
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ int snake(int r, int n) {
-  const int q = r / n, m = r - q * n;
-  return (q & 1) ? n - 1 - m : m;
+// bar.sync on barrier `id` (1..15) for `nthreads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// The last route CTA: the work plan.  Experts are ranked by their count over the call (ties: lower
-// id) with a bitonic sort and dealt to the parts (the CTAs sharing a column tile) in snake order.
-// In a part, an expert whose rows cost more than a sixth of the part's work is cut into 2 or 4
-// column parts while the part has room (one warp's share of the part is a twelfth, and a warp's
-// own pace cannot keep up with more than about twice that); every column part or whole expert is a
-// unit.  A part's units, in rank order, are dealt in snake order to the four warp schedulers (warp w
-// issues on scheduler w % 4) and each scheduler's to its three warps, so heavy and light units mix.
-__device__ void build_plan(const int *cnt, int E, int nparts, int32_t *plan, unsigned long long *key, float *ptot) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
-  int n2 = 1;
-  while (n2 < E) n2 <<= 1;
-  for (int i = t; i < n2; i += blockDim.x)   // ascending keys: larger count first, then lower id
-    key[i] = i < E ? ((unsigned long long)(0x7fffffffu - (uint32_t)cnt[i]) << 32) | (uint32_t)i : ~0ull;
-  for (int i = t; i < kMaxParts; i += blockDim.x) ptot[i] = 0.0f;
-  __syncthreads();
-  for (int k = 2; k <= n2; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = t; i < n2; i += blockDim.x) {
-        const int l = i ^ j;
-        if (l > i) {
-          const unsigned long long a = key[i], b = key[l];
-          if (((i & k) == 0) == (a > b)) { key[i] = b; key[l] = a; }
-        }
-      }
-      __syncthreads();
+// The work plan of one part (the CTAs with this blockIdx.z share a column tile's experts), built by
+// the consumer warps of every CTA from the counts over the whole call (the same plan for every
+// chunk and tile, so each (expert, column) sum has one owner).  Experts are ranked by count (ties:
+// lower id) and dealt to the parts in snake order of rank.  In a part, an expert whose rows cost
+// more than one warp's share of the part (a twelfth) is cut into 2 or 4 column parts while the part
+// has room; each column part or whole expert is a unit.  The units, in rank order, go one by one to
+// the consumer warp with the least work so far among those with a free slot (ties: lower warp), so
+// the warps' loads, and with them the four warp schedulers', come out level.
+//   rank: [E] scratch, ul: [kPartUnits] scratch, ud: the plan slots; bar: a named barrier over the
+//   nthreads consumer threads (tid = their index).
+__device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts, int p, int16_t *rank, int2 *ul,
+                          int (*ud)[kSlots], int tid, int nthreads, int bar) {
+  // rank by counting: experts ahead of e have a larger count, or the same count and a lower id
+  for (int e = tid; e < E; e += nthreads) {
+    const int c = __ldg(ecount + e);
+    int r = 0;
+    for (int j = 0; j < E; j++) {
+      const int cj = __ldg(ecount + j);
+      r += (cj > c) | ((cj == c) & (j < e));
     }
-  // parts in snake order of rank; each part's work (unsplit costs)
-  for (int r = t; r < E; r += blockDim.x) {
-    const int e = (int)(key[r] & 0xffffffffu), c = cnt[e];
-    if (c > 0) atomicAdd(&ptot[snake(r, nparts)], (float)c * (float)unit_cost(0));
+    rank[r] = (int16_t)e;
   }
-  __syncthreads();
-  // one warp per part: its experts in rank order (ranks p, 2P - 1 - p, 2P + p, ...), split
-  // decisions, unit positions (a scan), and the units dealt to schedulers and warps
-  for (int p = warp; p < nparts; p += nwarps) {
-    for (int i = lane; i < kMaxConsumers * kSlots; i += 32) plan[(size_t)p * kMaxConsumers * kSlots + i] = -1;
-    __syncwarp();
-    const float limit = ptot[p] / 6.0f;
-    const int nexp = (E + nparts - 1) / nparts;        // bound on the part's experts (ranks < E)
+  for (int i = tid; i < kMaxConsumers * kSlots; i += nthreads) ud[i / kSlots][i % kSlots] = -1;
+  named_barrier(bar, nthreads);
+  if (tid < 32) {
+    const int lane = tid;
+    const int nexp = (E + nparts - 1) / nparts;          // bound on the part's experts (ranks < E)
+    auto part_expert = [&](int l, int &e, int &c) {       // l-th expert of the part, rank order
+      const int r = l * nparts + ((l & 1) ? nparts - 1 - p : p);
+      e = 0; c = 0;
+      if (l < nexp && r < E) { e = rank[r]; c = __ldg(ecount + e); }
+    };
+    float tot = 0.0f;                                     // the part's work, unsplit
+    for (int l = lane; l < nexp; l += 32) {
+      int e, c;
+      part_expert(l, e, c);
+      tot += (float)c * (float)unit_cost(0);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    const float limit = tot / (float)kMaxConsumers;
     int base = 0;
     for (int l0 = 0; l0 < nexp; l0 += 32) {
       const int l = l0 + lane;
-      int e = 0, c = 0;
-      const int r = l * nparts + ((l & 1) ? nparts - 1 - p : p);
-      if (l < nexp && r < E) {
-        e = (int)(key[r] & 0xffffffffu);
-        c = cnt[e];
-      }
+      int e, c;
+      part_expert(l, e, c);
       int lk = 0;
       while (c > 0 && lk < 2 && (float)c * (float)unit_cost(lk) > limit) lk++;
       int n = c > 0 ? 1 << lk : 0;
@@ -219,28 +218,41 @@ __device__ void build_plan(const int *cnt, int E, int nparts, int32_t *plan, uns
         if (lane >= o) incl += v;
       }
       for (int jj = 0; jj < n; jj++) {
-        const int ui = base + incl - n + jj;           // the unit's index in the part
-        if (ui < kPartUnits) {
-          const int sb = snake(ui, 4), si = ui / 4;
-          const int wi = snake(si, 3), slot = si / 3;
-          plan[((size_t)p * kMaxConsumers + wi * 4 + sb) * kSlots + slot] = unit_desc(e, jj, lk);
-        }
+        const int ui = base + incl - n + jj;
+        if (ui < kPartUnits) ul[ui] = make_int2(unit_desc(e, jj, lk), min(c, 1 << 23) * unit_cost(lk));
       }
       base += __shfl_sync(0xffffffffu, incl, 31);
     }
+    __syncwarp();
+    // deal: the (load, warp) minimum over the warps with a free slot is one warp-wide reduction of
+    // load << 4 | warp (loads saturate at 2^28 - 1; a warp with a free slot always wins over one
+    // without, as the all-ones key needs lane 15)
+    const int nu = min(base, kPartUnits);
+    uint32_t load = 0;
+    int nslot = 0;
+    for (int u = 0; u < nu; u++) {
+      const int2 d = ul[u];
+      const uint32_t k = lane < kMaxConsumers && nslot < kSlots ? load << 4 | (uint32_t)lane : 0xffffffffu;
+      const uint32_t w = __reduce_min_sync(0xffffffffu, k) & 15u;
+      if (lane == (int)w) {
+        ud[w][nslot] = d.x;
+        load = min(load + (uint32_t)d.y, 0x0fffffffu);
+        nslot++;
+      }
+    }
   }
+  named_barrier(bar, nthreads);
 }
 
 // One CTA per (sub-tile s, chunk k): rows [sub * s, sub * s + sub) of chunk k.
 __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__ ids, int64_t tokens, int top_k,
                                                      int E, int64_t rpc, int nsub, int sub, SegLayout sl, RouteWs ws,
                                                      unsigned long long *__restrict__ counts,
-                                                     int32_t *__restrict__ status, int nparts) {
+                                                     int32_t *__restrict__ status) {
   __shared__ uint32_t bm[1024][kMaxSub / 32];   // expert x row bitmap of the sub-tile
   __shared__ int cnt[1024 + 1], off[1024 + 1];
-  __shared__ unsigned long long key[1024];
-  __shared__ float ptot[kMaxParts];
-  __shared__ int last;
+  // the accumulate kernel may be scheduled now: it waits for this grid's completion itself
+  asm volatile("griddepcontrol.launch_dependents;");
   const int words = sub / 32;
   const int s = blockIdx.x;
   const int64_t k = blockIdx.y;
@@ -314,16 +326,6 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
       ws.touched[e] = 1;
     }
   }
-  // the last CTA to finish builds the work plan from the counts over the whole call
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(&ws.touched[E], 1) == (int)(gridDim.x * gridDim.y) - 1;
-  __syncthreads();
-  if (!last) return;
-  __threadfence();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = *(volatile int32_t *)&ws.ecount[e];
-  __syncthreads();
-  build_plan(cnt, E, nparts, ws.plan, key, ptot);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -334,6 +336,7 @@ struct AccArgs {
   RouteWs ws;
   float *in_sum2;
   int32_t *status;
+  uint64_t neg0;   // -0.0f in both 32-bit halves
 };
 
 // Shared-memory loads through 32-bit shared-window addresses (explicitly the shared state space;
@@ -376,42 +379,76 @@ template <> __device__ __forceinline__ Lane<4> lds_lane<4>(uint32_t a) {
   return r;
 }
 
-// acc += x^2 for the lane's values of one row.  bf16: the square of a bf16 value is exact in fp32,
-// so the mixed-precision FMA (one rounding) equals fl(acc + fl(x*x)); fp32: the square rounded,
-// then added with one more rounding.
-__device__ __forceinline__ void fma_bf16x2(float &a0, float &a1, uint32_t u) {
-  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n}\n"
-      : "+f"(a0), "+f"(a1) : "r"(u));
+// acc += x^2 for the lane's values of one row: the square rounded to fp32, then added with one more
+// rounding, two columns per instruction (packed fp32x2, round to nearest, no flush).  The square is
+// formed as fma(x, x, z) with z = -0 in both halves (x*x + -0 = x*x, also for +0, so it is x*x
+// rounded once).  z is a kernel argument: with a literal -0 the compiler turns the fma into a
+// multiply and fuses that with the add, which rounds once and differs where the square is inexact
+// (fp32 inputs; bf16 inputs whose squares fall below the normal range).  A bf16 value widens to
+// fp32 exactly by moving its bits to the upper half.
+__device__ __forceinline__ void sq_add2(float &a0, float &a1, float x0, float x1, uint64_t z) {
+  unsigned long long acc, x;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+  asm("fma.rn.f32x2 %0, %0, %0, %1;" : "+l"(x) : "l"(z));
+  asm("add.rn.f32x2 %0, %0, %1;" : "+l"(acc) : "l"(x));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+// bf16, EX: the square rounded, then added (packed as above).  bf16, !EX: one mixed-precision FMA
+// per value, acc = fl(acc + x*x) with one rounding -- the same value whenever x*x is exact in fp32,
+// which holds for every bf16 x with |x| >= 2^-67 or x = 0 (8 significant bits, so x*x has at
+// most 16 and stays above the subnormal step 2^-149); stages holding a value below that take EX.
+template <bool EX> __device__ __forceinline__ void sq_add_bf16x2(float &a0, float &a1, uint32_t u, uint64_t z) {
+  if (EX) {
+    sq_add2(a0, a1, __uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u), z);
+  } else {
+    asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n fma.rn.f32.bf16 %0, l, l, %0;\n fma.rn.f32.bf16 %1, h, h, %1;\n}\n"
+        : "+f"(a0), "+f"(a1) : "r"(u));
+  }
 }
 __device__ __forceinline__ void sq_add(float &acc, uint32_t u) {
   const float x = __uint_as_float(u);
   acc = __fadd_rn(acc, __fmul_rn(x, x));
 }
-template <typename T, int LB> __device__ __forceinline__ void acc_row(float *acc, const Lane<LB> &r);
-template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 16>(float *acc, const Lane<16> &r) {
-  fma_bf16x2(acc[0], acc[1], r.v.x); fma_bf16x2(acc[2], acc[3], r.v.y);
-  fma_bf16x2(acc[4], acc[5], r.v.z); fma_bf16x2(acc[6], acc[7], r.v.w);
-}
-template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 8>(float *acc, const Lane<8> &r) {
-  fma_bf16x2(acc[0], acc[1], r.v.x); fma_bf16x2(acc[2], acc[3], r.v.y);
-}
-template <> __device__ __forceinline__ void acc_row<__nv_bfloat16, 4>(float *acc, const Lane<4> &r) {
-  fma_bf16x2(acc[0], acc[1], r.v);
-}
-template <> __device__ __forceinline__ void acc_row<float, 16>(float *acc, const Lane<16> &r) {
-  sq_add(acc[0], r.v.x); sq_add(acc[1], r.v.y); sq_add(acc[2], r.v.z); sq_add(acc[3], r.v.w);
-}
-template <> __device__ __forceinline__ void acc_row<float, 8>(float *acc, const Lane<8> &r) {
-  sq_add(acc[0], r.v.x); sq_add(acc[1], r.v.y);
-}
-template <> __device__ __forceinline__ void acc_row<float, 4>(float *acc, const Lane<4> &r) { sq_add(acc[0], r.v); }
+template <typename T, int LB, bool EX> struct AccRow;
+template <bool EX> struct AccRow<__nv_bfloat16, 16, EX> {
+  static __device__ __forceinline__ void run(float *acc, const Lane<16> &r, uint64_t z) {
+    sq_add_bf16x2<EX>(acc[0], acc[1], r.v.x, z); sq_add_bf16x2<EX>(acc[2], acc[3], r.v.y, z);
+    sq_add_bf16x2<EX>(acc[4], acc[5], r.v.z, z); sq_add_bf16x2<EX>(acc[6], acc[7], r.v.w, z);
+  }
+};
+template <bool EX> struct AccRow<__nv_bfloat16, 8, EX> {
+  static __device__ __forceinline__ void run(float *acc, const Lane<8> &r, uint64_t z) {
+    sq_add_bf16x2<EX>(acc[0], acc[1], r.v.x, z); sq_add_bf16x2<EX>(acc[2], acc[3], r.v.y, z);
+  }
+};
+template <bool EX> struct AccRow<__nv_bfloat16, 4, EX> {
+  static __device__ __forceinline__ void run(float *acc, const Lane<4> &r, uint64_t z) {
+    sq_add_bf16x2<EX>(acc[0], acc[1], r.v, z);
+  }
+};
+template <bool EX> struct AccRow<float, 16, EX> {
+  static __device__ __forceinline__ void run(float *acc, const Lane<16> &r, uint64_t z) {
+    sq_add2(acc[0], acc[1], __uint_as_float(r.v.x), __uint_as_float(r.v.y), z);
+    sq_add2(acc[2], acc[3], __uint_as_float(r.v.z), __uint_as_float(r.v.w), z);
+  }
+};
+template <bool EX> struct AccRow<float, 8, EX> {
+  static __device__ __forceinline__ void run(float *acc, const Lane<8> &r, uint64_t z) {
+    sq_add2(acc[0], acc[1], __uint_as_float(r.v.x), __uint_as_float(r.v.y), z);
+  }
+};
+template <bool EX> struct AccRow<float, 4, EX> {
+  static __device__ __forceinline__ void run(float *acc, const Lane<4> &r, uint64_t) { sq_add(acc[0], r.v); }
+};
 
 // The n rows of one unit in this stage, in ascending order.  srow: shared address of the unit's
 // first row offset (16-byte aligned); base: the lane's first byte in the staged tile.  Whole groups
 // of 4 rows are software pipelined (offsets one group ahead of the rows, rows one group ahead of
 // the additions); the last n % 4 rows follow one by one.
-template <typename T, int LB>
-__device__ __forceinline__ void run_unit(float *acc, uint32_t srow, int n, uint32_t base) {
+template <typename T, int LB, bool EX>
+__device__ __forceinline__ void run_unit(float *acc, uint32_t srow, int n, uint32_t base, uint64_t z) {
+  using A = AccRow<T, LB, EX>;
   const int n4 = n & ~3;
   if (n4) {
     const uint4 o = lds_v4(srow);
@@ -423,14 +460,14 @@ __device__ __forceinline__ void run_unit(float *acc, uint32_t srow, int n, uint3
       const uint4 onn = lds_v4(srow + 4 * min(j + 4, n4 - 4));
       const Lane<LB> n0 = lds_lane<LB>(base + on.x), n1 = lds_lane<LB>(base + on.y), n2 = lds_lane<LB>(base + on.z),
                      n3 = lds_lane<LB>(base + on.w);
-      acc_row<T, LB>(acc, r0); acc_row<T, LB>(acc, r1); acc_row<T, LB>(acc, r2); acc_row<T, LB>(acc, r3);
+      A::run(acc, r0, z); A::run(acc, r1, z); A::run(acc, r2, z); A::run(acc, r3, z);
       r0 = n0; r1 = n1; r2 = n2; r3 = n3;
       on = onn;
     }
-    acc_row<T, LB>(acc, r0); acc_row<T, LB>(acc, r1); acc_row<T, LB>(acc, r2); acc_row<T, LB>(acc, r3);
+    A::run(acc, r0, z); A::run(acc, r1, z); A::run(acc, r2, z); A::run(acc, r3, z);
   }
 #pragma unroll 1
-  for (int j = n4; j < n; j++) acc_row<T, LB>(acc, lds_lane<LB>(base + lds_u32(srow + 4 * j)));
+  for (int j = n4; j < n; j++) A::run(acc, lds_lane<LB>(base + lds_u32(srow + 4 * j)), z);
 }
 
 // The lane's nv current sums at src (nv = 8, 4, 2 or 1 consecutive floats, 16-byte aligned when 4+).
@@ -469,8 +506,60 @@ __device__ __forceinline__ bool store_unit(float *dst, const float *acc, const f
   return fin;
 }
 
+// One stage for one consumer warp: every unit of the warp (udw: its plan slots) adds the rows the
+// stage routes to its expert.  hit gathers the slots that saw rows.
+template <typename T, bool EX>
+__device__ __forceinline__ void stage_units(float (*acc)[8], const int *udw, uint32_t stage, uint32_t sse,
+                                            uint32_t srow, int lane, uint32_t &hit, uint64_t z) {
+#pragma unroll
+  for (int s = 0; s < kSlots; s++) {
+    const int d = udw[s];
+    if (d < 0) continue;
+    const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
+    const int2 se = lds_i2(sse + 8 * e);
+    if (se.y == 0) continue;
+    hit |= 1u << s;
+    const uint32_t base = stage + (uint32_t)(j * (kRowBytes >> lk));
+    if (lk == 0) run_unit<T, 16, EX>(acc[s], srow + 4 * se.x, se.y, base + lane * 16, z);
+    else if (lk == 1) run_unit<T, 8, EX>(acc[s], srow + 4 * se.x, se.y, base + lane * 8, z);
+    else run_unit<T, 4, EX>(acc[s], srow + 4 * se.x, se.y, base + lane * 4, z);
+  }
+}
+
+constexpr int kScreenWarps = 2;
+
+// Whether a landed bf16 stage holds a value whose square is inexact in fp32 (flagged
+// conservatively: 0 < |x| < 2^-63, exponent field below 64).  The whole warp reads the tile (lane:
+// 16 bytes of every row): first a screen that also lets zeros through, then, only if it fires, the
+// exact test.
+__device__ __forceinline__ bool stage_has_tiny(uint32_t tile, int rows, int lane) {
+  uint32_t m = 0xffffffffu;
+#pragma unroll 8
+  for (int r = 0; r < rows; r++) {   // rows is a multiple of 8
+    const uint4 v = lds_v4(tile + (uint32_t)r * kRowBytes + lane * 16);
+    m &= (v.x | v.x << 1) & (v.y | v.y << 1) & (v.z | v.z << 1) & (v.w | v.w << 1);
+  }
+  // bit 14 of each half: exponent bit 7 or 6 set, i.e. exponent field >= 64
+  if (!__any_sync(0xffffffffu, (m & 0x40004000u) != 0x40004000u)) return false;
+  auto tiny = [](uint32_t h) { return ((h & 0x7fffu) - 1u) < 0x1fffu; };
+  bool t = false;
+#pragma unroll 4
+  for (int r = 0; r < rows; r++) {
+    const uint4 v = lds_v4(tile + (uint32_t)r * kRowBytes + lane * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; i++) t |= tiny(w[i] & 0xffffu) | tiny(w[i] >> 16);
+  }
+  return __any_sync(0xffffffffu, t);
+}
+
+// 13 warps (fp32) or 15 (bf16: two screening warps): at most 128 registers a thread, as each warp
+// scheduler's quarter of the register file (16,384) must hold its warps (4 x 32 x 128).
+template <typename T> constexpr int acc_warps() {
+  return kMaxConsumers + 1 + (std::is_same<T, __nv_bfloat16>::value ? kScreenWarps : 0);
+}
 template <typename T>
-__global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulate_kernel(
+__global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
     const __grid_constant__ CUtensorMap tmap, AccArgs a) {
   constexpr int TILE = Col<T>::TILE;
   constexpr int ESZ = (int)sizeof(T);
@@ -482,9 +571,12 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
   // stage buffers start on a 128-byte boundary (one spare 128 bytes is allocated for this)
   uint8_t *smem = smem_raw + ((128 - (smem_u32(smem_raw) & 127)) & 127);
   const uint32_t smem_s = smem_u32(smem);
-  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages];
-  __shared__ int abort_flag;
-  __shared__ int ud[kMaxConsumers][kSlots];  // the consumer warps' work units (from the plan)
+  __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], chk_bar[kMaxStages];
+  __shared__ int abort_flag, tiny_flag[kMaxStages][kScreenWarps];
+  constexpr bool kScan = std::is_same<T, __nv_bfloat16>::value;   // bf16 stages are screened
+  __shared__ int ud[kMaxConsumers][kSlots];  // the consumer warps' work units (the plan)
+  __shared__ int16_t rank[1024];              // plan scratch: experts by rank
+  __shared__ int2 ul[kPartUnits];             // plan scratch: the part's units
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   constexpr int NW = kMaxConsumers;
@@ -493,16 +585,18 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
   const int64_t kbeg = split ? blockIdx.y : 0, kend = split ? blockIdx.y + 1 : a.nchunks;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < NS; s++) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], NW); }
+    for (int s = 0; s < NS; s++) { mbar_init(&full_bar[s], 1); mbar_init(&empty_bar[s], NW); mbar_init(&chk_bar[s], kScreenWarps); }
     abort_flag = 0;
     mbar_fence_init();
   }
   // the row after the tile in every stage is a zero row: a group of row offsets is padded with it
   for (int i = threadIdx.x; i < NS * kRowBytes / 4; i += blockDim.x)
     reinterpret_cast<uint32_t *>(smem + (size_t)(i / (kRowBytes / 4)) * kStageBytes + kTileBytes)[i % (kRowBytes / 4)] = 0u;
-  for (int i = threadIdx.x; i < NW * kSlots; i += blockDim.x)
-    ud[i / kSlots][i % kSlots] = a.ws.plan[(size_t)blockIdx.z * NW * kSlots + i];
+  // the route kernel (segments, counts) is complete and visible after this
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
+  // the consumers plan the part while the producer starts the first stages
+  if (warp < NW) plan_part(a.ws.ecount, a.E, gridDim.z, blockIdx.z, rank, ul, ud, threadIdx.x, NW * 32, 1);
 
   if (warp == NW) {
     // ---- producer: lane 0 issues the tile's row stages in consumption order --------------
@@ -531,6 +625,30 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
       for (int64_t u = q - NS < 0 ? 0 : q - NS; u < q; u++)
         mbar_wait_bounded(&full_bar[u % NS], (uint32_t)((u / NS) & 1));
     }
+  } else if (warp > NW) {
+    // ---- bf16 screening warps: each stage as it lands, half of its rows each ------------------
+    const int sw = warp - NW - 1, half = a.sub / kScreenWarps;
+    int64_t q = 0;
+    bool ok = true;
+    for (int64_t k = kbeg; k < kend && ok; k++) {
+      const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
+      const int nsub = (int)((rows + a.sub - 1) / a.sub);
+      for (int sub = 0; sub < nsub && ok; sub++, q++) {
+        const int st = (int)(q % NS);
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[st], (uint32_t)((q / NS) & 1)));
+        if (!ok || *(volatile int *)&abort_flag) { ok = false; break; }
+        const bool t =
+            stage_has_tiny(smem_s + (uint32_t)st * kStageBytes + (uint32_t)(sw * half) * kRowBytes, half, lane);
+        if (lane == 0) {
+          *(volatile int *)&tiny_flag[st][sw] = t ? 1 : 0;
+          mbar_arrive(&chk_bar[st]);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      atomicExch(&abort_flag, 1);
+      if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+    }
   } else {
     // ---- consumers: each warp walks its units (plan) over every stage --------------------------
     int64_t q = 0;
@@ -546,25 +664,18 @@ __global__ void __launch_bounds__(32 * (kMaxConsumers + 1), 1) imatrix_accumulat
         for (int c = 0; c < 8; c++) acc[s][c] = 0.0f;
       for (int sub = 0; sub < nsub; sub++, q++) {
         const int st = (int)(q % NS);
-        if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((q / NS) & 1)) || *(volatile int *)&abort_flag) {
+        const uint32_t par = (uint32_t)((q / NS) & 1);
+        if ((kScan && !mbar_wait_bounded(&chk_bar[st], par)) || !mbar_wait_bounded(&full_bar[st], par) ||
+            *(volatile int *)&abort_flag) {
           ok = false;
           break;
         }
         const uint32_t stage = smem_s + (uint32_t)st * kStageBytes;
         const uint32_t sse = stage + kSegOff, srow = sse + (uint32_t)a.sl.offb;
-#pragma unroll
-        for (int s = 0; s < kSlots; s++) {
-          const int d = ud[warp][s];
-          if (d < 0) continue;
-          const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
-          const int2 se = lds_i2(sse + 8 * e);
-          if (se.y == 0) continue;
-          hit |= 1u << s;
-          const uint32_t base = stage + (uint32_t)(j * (kRowBytes >> lk));
-          if (lk == 0) run_unit<T, 16>(acc[s], srow + 4 * se.x, se.y, base + lane * 16);
-          else if (lk == 1) run_unit<T, 8>(acc[s], srow + 4 * se.x, se.y, base + lane * 8);
-          else run_unit<T, 4>(acc[s], srow + 4 * se.x, se.y, base + lane * 4);
-        }
+        if (!kScan || (*(volatile int *)&tiny_flag[st][0] | *(volatile int *)&tiny_flag[st][1]))
+          stage_units<T, true>(acc, ud[warp], stage, sse, srow, lane, hit, a.neg0);
+        else
+          stage_units<T, false>(acc, ud[warp], stage, sse, srow, lane, hit, a.neg0);
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[st]);
       }
@@ -659,8 +770,19 @@ static int launch_accumulate(const CUtensorMap &tm, const AccArgs &a, const Plan
   auto kern = imatrix_accumulate_kernel<T>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
-  dim3 grid((unsigned)p.ntiles, p.split ? (unsigned)p.nchunks : 1u, (unsigned)p.nparts);
-  kern<<<grid, 32 * (kMaxConsumers + 1), smem, st>>>(tm, a);
+  // programmatic dependent launch: the CTAs start (barriers, zero rows) while the route kernel
+  // runs and wait for its completion before reading what it wrote
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)p.ntiles, p.split ? (unsigned)p.nchunks : 1u, (unsigned)p.nparts);
+  cfg.blockDim = dim3(32 * acc_warps<T>());
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tm, a) != cudaSuccess) return IQ_ERR_CUDA;
   return cudaPeekAtLastError() == cudaSuccess ? IQ_OK : IQ_ERR_CUDA;
 }
 
@@ -707,7 +829,7 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
   if (cudaMemsetAsync(workspace, 0, ws.zero_bytes, st) != cudaSuccess) return IQ_ERR_CUDA;
   imatrix_route<<<dim3((unsigned)p.nsub, (unsigned)p.nchunks), 256, 0, st>>>(
       expert_ids, tokens, top_k, num_experts, rows_per_chunk, p.nsub, p.sub, p.seg, ws, (unsigned long long *)counts,
-      status, p.nparts);
+      status);
   if (cudaPeekAtLastError() != cudaSuccess) return IQ_ERR_CUDA;
   AccArgs a;
   a.tokens = tokens; a.cols = cols; a.rpc = rows_per_chunk; a.nchunks = p.nchunks;
@@ -715,6 +837,7 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
   a.stage_bytes = p.stage_bytes;
   a.nstages = p.nstages;
   a.ws = ws; a.in_sum2 = in_sum2; a.status = status;
+  a.neg0 = 0x8000000080000000ull;
   const int rc = dt == IQ_BF16 ? launch_accumulate<__nv_bfloat16>(tm, a, p, st) : launch_accumulate<float>(tm, a, p, st);
   if (rc != IQ_OK) return rc;
   if (p.split) {

@@ -136,8 +136,8 @@ void or_float_from_half_n(const uint16_t *in, float *out, int64_t n) {
  * fl(x*x), and it is added with one rounded fp32 add, partial = fl(partial + sq) (the page squares
  * the rows, then sums them; this file is built without FMA contraction, so the two steps stay
  * apart); then in_sum2 += partial (one rounded fp32 add), chunk by chunk, for experts the chunk
- * routed at least one token to.  For bf16 activations the square is exact, so there the result
- * equals the exact square added with a single rounding.
+ * routed at least one token to.  The same two steps serve bf16 activations (widened exactly):
+ * their squares are exact in fp32 except below its normal range, where they round as well.
  * A token's top-k slots are read as a set: a repeated id counts once (and is reported). */
 int or_imatrix_accumulate(const float *x, int64_t tokens, int64_t cols, const int32_t *ids, int top_k,
                           int E, int64_t rows_per_chunk, float *in_sum2, int64_t *counts,

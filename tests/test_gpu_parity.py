@@ -104,6 +104,33 @@ def test_imatrix_bit_exact(dtype, T, C, E, K, R):
     assert int(st.item()) == ref_st
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_imatrix_tiny_values_round_the_square_first(dtype):
+    """Activations near 2^-70, whose squares fall below fp32's normal range and round there: the
+    sums must take the square's rounding before the addition's, as the definition does (a fused
+    multiply-add rounds once and differs on such inputs)."""
+    rng = np.random.default_rng(11)
+    T, C, E = 300, 192, 3
+    mant = rng.integers(128, 256, (T, C)).astype(np.float64) / 128.0
+    x32 = (mant * np.exp2(rng.integers(-76, -64, (T, C))) * rng.choice([-1.0, 1.0], (T, C))).astype(np.float32)
+    store, xv = synth.as_dtype(x32, dtype)
+    ids = np.stack([rng.permutation(E)[:2] for _ in range(T)]).astype(np.int32)
+    ref_s, ref_c, _ = oracle.imatrix_accumulate(xv, ids, E, rows_per_chunk=128)
+    # what one rounding per row would give: the values have 8 significant bits, so x^2 and every
+    # partial + x^2 below 2^-100 are exact in fp64 and the cast to fp32 is the single rounding
+    fused = np.zeros_like(ref_s)
+    for k0 in range(0, T, 128):
+        part = np.zeros_like(ref_s)
+        for t in range(k0, min(T, k0 + 128)):
+            for e in ids[t]:
+                part[e] = (part[e].astype(np.float64) + xv[t].astype(np.float64) ** 2).astype(np.float32)
+        fused = fused + part
+    assert not np.array_equal(fused, ref_s)              # the case does tell the two apart
+    s2, cn = api.imatrix_accumulate(dev_tensor(store, dtype), torch.from_numpy(ids).to(DEV), E, 128)
+    assert np.array_equal(host(s2).view(np.uint32), ref_s.view(np.uint32))
+    assert np.array_equal(host(cn), ref_c)
+
+
 def test_imatrix_status_and_sets():
     x = synth.activations(64, 128, seed=5)
     ids = np.tile(np.array([[0, 1]], np.int32), (64, 1))
