@@ -56,7 +56,6 @@ constexpr size_t kSmemBudget = 220 * 1024;
 
 // cost of one (row, unit) pair in half instructions by column split (1, 2 or 4 parts of a row);
 // a unit with more parts covers fewer columns per lane for the same per-row overhead
-__host__ __device__ inline int unit_cost(int lk) { return lk == 0 ? 21 : lk == 1 ? 13 : 9; }
 
 template <typename T> struct Col;
 template <> struct Col<__nv_bfloat16> { static constexpr int TILE = 256; };
@@ -81,9 +80,8 @@ __host__ __device__ inline SegLayout seg_layout(int E, int top_k, int sub) {
   return l;
 }
 
-// A work unit of the accumulation: expert e over part j of the 2^lk column parts of a tile row.
-// A consumer warp's plan slot holds e | j << 16 | lk << 20, or -1 (no unit).
-__host__ __device__ inline int unit_desc(int e, int j, int lk) { return e | (j << 16) | (lk << 20); }
+// A work unit of the accumulation is one expert over the tile's columns; a consumer warp's plan
+// slot holds its id, or -1 (no unit).
 
 struct RouteWs {
   int32_t *touched;    // [E]   experts this call routed at least one token to
@@ -156,16 +154,17 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 
 // The work plan of one part (the CTAs with this blockIdx.z share a column tile's experts), built by
 // the consumer warps of every CTA from the counts over the whole call (the same plan for every
-// chunk and tile, so each (expert, column) sum has one owner).  Experts are ranked by count (ties:
-// lower id) and dealt to the parts in snake order of rank.  In a part, an expert whose rows cost
-// more than one warp's share of the part (a twelfth) is cut into 2 or 4 column parts while the part
-// has room; each column part or whole expert is a unit.  The units, in rank order, go one by one to
-// the consumer warp with the least work so far among those with a free slot (ties: lower warp), so
-// the warps' loads, and with them the four warp schedulers', come out level.
+// chunk and tile, so each (expert, column) sum has one owner warp).  Experts are ranked by count
+// (ties: lower id) and dealt to the parts in snake order of rank; a part's experts, in rank order,
+// go one by one to the consumer warp with the least work so far among those with a free slot
+// (ties: lower warp).  An expert's work is its rows plus a fixed cost for each stage it has rows
+// in (a run starts with two dependent shared-memory loads, and is padded to whole groups of 4):
+// c + 4 min(c, stages).  Cutting heavy experts into column parts was measured slower: the narrower
+// loads cost more per row than the better balance gains, as a long run streams at full speed.
 //   rank: [E] scratch, ul: [kPartUnits] scratch, ud: the plan slots; bar: a named barrier over the
 //   nthreads consumer threads (tid = their index).
-__device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts, int p, int16_t *rank, int2 *ul,
-                          int (*ud)[kSlots], int tid, int nthreads, int bar) {
+__device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts, int p, int64_t stages,
+                          int16_t *rank, int2 *ul, int (*ud)[kSlots], int tid, int nthreads, int bar) {
   // rank by counting: experts ahead of e have a larger count, or the same count and a lower id
   for (int e = tid; e < E; e += nthreads) {
     const int c = __ldg(ecount + e);
@@ -181,47 +180,19 @@ __device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts,
   if (tid < 32) {
     const int lane = tid;
     const int nexp = (E + nparts - 1) / nparts;          // bound on the part's experts (ranks < E)
-    auto part_expert = [&](int l, int &e, int &c) {       // l-th expert of the part, rank order
-      const int r = l * nparts + ((l & 1) ? nparts - 1 - p : p);
-      e = 0; c = 0;
-      if (l < nexp && r < E) { e = rank[r]; c = __ldg(ecount + e); }
-    };
-    float tot = 0.0f;                                     // the part's work, unsplit
-    for (int l = lane; l < nexp; l += 32) {
-      int e, c;
-      part_expert(l, e, c);
-      tot += (float)c * (float)unit_cost(0);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    const float limit = tot / (float)kMaxConsumers;
     int base = 0;
-    for (int l0 = 0; l0 < nexp; l0 += 32) {
+    for (int l0 = 0; l0 < nexp; l0 += 32) {              // the part's experts with rows, in rank order
       const int l = l0 + lane;
-      int e, c;
-      part_expert(l, e, c);
-      int lk = 0;
-      while (c > 0 && lk < 2 && (float)c * (float)unit_cost(lk) > limit) lk++;
-      int n = c > 0 ? 1 << lk : 0;
-      int incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
+      const int r = l * nparts + ((l & 1) ? nparts - 1 - p : p);
+      int e = 0, c = 0;
+      if (l < nexp && r < E) { e = rank[r]; c = __ldg(ecount + e); }
+      const unsigned has = __ballot_sync(0xffffffffu, c > 0);
+      const int ui = base + __popc(has & ((1u << lane) - 1u));
+      if (c > 0 && ui < kPartUnits) {
+        const int64_t w = (int64_t)c + 4 * min((int64_t)c, stages);
+        ul[ui] = make_int2(e, (int)min(w, (int64_t)0x0fffffff));
       }
-      // a split must leave room for one unit of every later expert of the part
-      if (n > 1 && base + incl + (nexp - 1 - l) > kPartUnits) { lk = 0; n = 1; }
-      incl = n;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      for (int jj = 0; jj < n; jj++) {
-        const int ui = base + incl - n + jj;
-        if (ui < kPartUnits) ul[ui] = make_int2(unit_desc(e, jj, lk), min(c, 1 << 23) * unit_cost(lk));
-      }
-      base += __shfl_sync(0xffffffffu, incl, 31);
+      base += __popc(has);
     }
     __syncwarp();
     // deal: the (load, warp) minimum over the warps with a free slot is one warp-wide reduction of
@@ -357,28 +328,6 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
   return v;
 }
 
-// One row's share of a lane: LB bytes (16, 8 or 4).
-template <int LB> struct Lane;
-template <> struct Lane<16> { uint4 v; };
-template <> struct Lane<8> { uint2 v; };
-template <> struct Lane<4> { uint32_t v; };
-template <int LB> __device__ __forceinline__ Lane<LB> lds_lane(uint32_t a);
-template <> __device__ __forceinline__ Lane<16> lds_lane<16>(uint32_t a) {
-  Lane<16> r;
-  r.v = lds_v4(a);
-  return r;
-}
-template <> __device__ __forceinline__ Lane<8> lds_lane<8>(uint32_t a) {
-  Lane<8> r;
-  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(r.v.x), "=r"(r.v.y) : "r"(a));
-  return r;
-}
-template <> __device__ __forceinline__ Lane<4> lds_lane<4>(uint32_t a) {
-  Lane<4> r;
-  r.v = lds_u32(a);
-  return r;
-}
-
 // acc += x^2 for the lane's values of one row: the square rounded to fp32, then added with one more
 // rounding, two columns per instruction (packed fp32x2, round to nearest, no flush).  The square is
 // formed as fma(x, x, z) with z = -0 in both halves (x*x + -0 = x*x, also for +0, so it is x*x
@@ -406,103 +355,65 @@ template <bool EX> __device__ __forceinline__ void sq_add_bf16x2(float &a0, floa
         : "+f"(a0), "+f"(a1) : "r"(u));
   }
 }
-__device__ __forceinline__ void sq_add(float &acc, uint32_t u) {
-  const float x = __uint_as_float(u);
-  acc = __fadd_rn(acc, __fmul_rn(x, x));
-}
-template <typename T, int LB, bool EX> struct AccRow;
-template <bool EX> struct AccRow<__nv_bfloat16, 16, EX> {
-  static __device__ __forceinline__ void run(float *acc, const Lane<16> &r, uint64_t z) {
-    sq_add_bf16x2<EX>(acc[0], acc[1], r.v.x, z); sq_add_bf16x2<EX>(acc[2], acc[3], r.v.y, z);
-    sq_add_bf16x2<EX>(acc[4], acc[5], r.v.z, z); sq_add_bf16x2<EX>(acc[6], acc[7], r.v.w, z);
+// One row of a unit: the lane's 16 bytes of the staged tile (8 bf16 or 4 fp32 values).
+template <typename T, bool EX> struct AccRow;
+template <bool EX> struct AccRow<__nv_bfloat16, EX> {
+  static __device__ __forceinline__ void run(float *acc, const uint4 &v, uint64_t z) {
+    sq_add_bf16x2<EX>(acc[0], acc[1], v.x, z); sq_add_bf16x2<EX>(acc[2], acc[3], v.y, z);
+    sq_add_bf16x2<EX>(acc[4], acc[5], v.z, z); sq_add_bf16x2<EX>(acc[6], acc[7], v.w, z);
   }
 };
-template <bool EX> struct AccRow<__nv_bfloat16, 8, EX> {
-  static __device__ __forceinline__ void run(float *acc, const Lane<8> &r, uint64_t z) {
-    sq_add_bf16x2<EX>(acc[0], acc[1], r.v.x, z); sq_add_bf16x2<EX>(acc[2], acc[3], r.v.y, z);
+template <bool EX> struct AccRow<float, EX> {
+  static __device__ __forceinline__ void run(float *acc, const uint4 &v, uint64_t z) {
+    sq_add2(acc[0], acc[1], __uint_as_float(v.x), __uint_as_float(v.y), z);
+    sq_add2(acc[2], acc[3], __uint_as_float(v.z), __uint_as_float(v.w), z);
   }
 };
-template <bool EX> struct AccRow<__nv_bfloat16, 4, EX> {
-  static __device__ __forceinline__ void run(float *acc, const Lane<4> &r, uint64_t z) {
-    sq_add_bf16x2<EX>(acc[0], acc[1], r.v, z);
-  }
-};
-template <bool EX> struct AccRow<float, 16, EX> {
-  static __device__ __forceinline__ void run(float *acc, const Lane<16> &r, uint64_t z) {
-    sq_add2(acc[0], acc[1], __uint_as_float(r.v.x), __uint_as_float(r.v.y), z);
-    sq_add2(acc[2], acc[3], __uint_as_float(r.v.z), __uint_as_float(r.v.w), z);
-  }
-};
-template <bool EX> struct AccRow<float, 8, EX> {
-  static __device__ __forceinline__ void run(float *acc, const Lane<8> &r, uint64_t z) {
-    sq_add2(acc[0], acc[1], __uint_as_float(r.v.x), __uint_as_float(r.v.y), z);
-  }
-};
-template <bool EX> struct AccRow<float, 4, EX> {
-  static __device__ __forceinline__ void run(float *acc, const Lane<4> &r, uint64_t) { sq_add(acc[0], r.v); }
-};
-
-// The n rows of one unit in this stage, in ascending order.  srow: shared address of the unit's
-// first row offset (16-byte aligned); base: the lane's first byte in the staged tile.  Whole groups
-// of 4 rows are software pipelined (offsets one group ahead of the rows, rows one group ahead of
-// the additions); the last n % 4 rows follow one by one.
-template <typename T, int LB, bool EX>
+// The n >= 1 rows of one unit in this stage, in ascending order.  srow: shared address of the unit's
+// first row offset (16-byte aligned); base: the lane's first byte in the staged tile.  The run is
+// padded with the zero row's offset to whole groups of 4, and a zero row adds exactly nothing
+// (fl(acc + 0) = acc for acc >= +0), so every group is whole; groups are software pipelined
+// (offsets two groups ahead of the additions, rows one group ahead).
+template <typename T, bool EX>
 __device__ __forceinline__ void run_unit(float *acc, uint32_t srow, int n, uint32_t base, uint64_t z) {
-  using A = AccRow<T, LB, EX>;
-  const int n4 = n & ~3;
-  if (n4) {
-    const uint4 o = lds_v4(srow);
-    uint4 on = lds_v4(srow + 4 * min(4, n4 - 4));
-    Lane<LB> r0 = lds_lane<LB>(base + o.x), r1 = lds_lane<LB>(base + o.y), r2 = lds_lane<LB>(base + o.z),
-             r3 = lds_lane<LB>(base + o.w);
+  using A = AccRow<T, EX>;
+  const int n4 = (n + 3) & ~3;
+  const uint4 o = lds_v4(srow);
+  uint4 on = lds_v4(srow + 4 * min(4, n4 - 4));
+  uint4 r0 = lds_v4(base + o.x), r1 = lds_v4(base + o.y), r2 = lds_v4(base + o.z), r3 = lds_v4(base + o.w);
 #pragma unroll 1
-    for (int j = 4; j < n4; j += 4) {
-      const uint4 onn = lds_v4(srow + 4 * min(j + 4, n4 - 4));
-      const Lane<LB> n0 = lds_lane<LB>(base + on.x), n1 = lds_lane<LB>(base + on.y), n2 = lds_lane<LB>(base + on.z),
-                     n3 = lds_lane<LB>(base + on.w);
-      A::run(acc, r0, z); A::run(acc, r1, z); A::run(acc, r2, z); A::run(acc, r3, z);
-      r0 = n0; r1 = n1; r2 = n2; r3 = n3;
-      on = onn;
-    }
+  for (int j = 4; j < n4; j += 4) {
+    const uint4 onn = lds_v4(srow + 4 * min(j + 4, n4 - 4));
+    const uint4 n0 = lds_v4(base + on.x), n1 = lds_v4(base + on.y), n2 = lds_v4(base + on.z), n3 = lds_v4(base + on.w);
     A::run(acc, r0, z); A::run(acc, r1, z); A::run(acc, r2, z); A::run(acc, r3, z);
+    r0 = n0; r1 = n1; r2 = n2; r3 = n3;
+    on = onn;
   }
-#pragma unroll 1
-  for (int j = n4; j < n; j++) A::run(acc, lds_lane<LB>(base + lds_u32(srow + 4 * j)), z);
+  A::run(acc, r0, z); A::run(acc, r1, z); A::run(acc, r2, z); A::run(acc, r3, z);
 }
 
-// The lane's nv current sums at src (nv = 8, 4, 2 or 1 consecutive floats, 16-byte aligned when 4+).
-__device__ __forceinline__ void load_unit(const float *src, float *v, int nv) {
-  if (nv >= 4) {
-    const float4 t = *reinterpret_cast<const float4 *>(src);
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-    if (nv == 8) {
-      const float4 u = *reinterpret_cast<const float4 *>(src + 4);
-      v[4] = u.x; v[5] = u.y; v[6] = u.z; v[7] = u.w;
-    }
-  } else if (nv == 2) {
-    const float2 t = *reinterpret_cast<const float2 *>(src);
-    v[0] = t.x; v[1] = t.y;
-  } else {
-    v[0] = src[0];
+// The lane's NV (8 for bf16, 4 for fp32) current sums at src (16-byte aligned).
+template <int NV> __device__ __forceinline__ void load_unit(const float *src, float *v) {
+#pragma unroll
+  for (int i = 0; i < NV; i += 4) {
+    const float4 t = *reinterpret_cast<const float4 *>(src + i);
+    v[i] = t.x; v[i + 1] = t.y; v[i + 2] = t.z; v[i + 3] = t.w;
   }
 }
 // dst = old + acc (add: in_sum2 += the lane's sums, one rounding each), or dst = acc (the chunk
 // partial, for the ordered combine).  Returns whether every stored value is finite.
-__device__ __forceinline__ bool store_unit(float *dst, const float *acc, const float *old, int nv, bool add) {
-  float o[8];
-#pragma unroll
-  for (int c = 0; c < 8; c++) o[c] = add ? __fadd_rn(old[c], acc[c]) : acc[c];
+template <int NV> __device__ __forceinline__ bool store_unit(float *dst, const float *acc, const float *old, bool add) {
   bool fin = true;
-  if (nv >= 4) {
-    *reinterpret_cast<float4 *>(dst) = make_float4(o[0], o[1], o[2], o[3]);
-    if (nv == 8) *reinterpret_cast<float4 *>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
-  } else if (nv == 2) {
-    *reinterpret_cast<float2 *>(dst) = make_float2(o[0], o[1]);
-  } else {
-    dst[0] = o[0];
-  }
 #pragma unroll
-  for (int c = 0; c < 8; c++) fin &= c >= nv || isfinite(o[c]);
+  for (int i = 0; i < NV; i += 4) {
+    float o[4];
+#pragma unroll
+    for (int c = 0; c < 4; c++) {
+      o[c] = add ? __fadd_rn(old[i + c], acc[i + c]) : acc[i + c];
+      fin &= isfinite(o[c]);
+    }
+    *reinterpret_cast<float4 *>(dst + i) = make_float4(o[0], o[1], o[2], o[3]);
+  }
   return fin;
 }
 
@@ -515,14 +426,10 @@ __device__ __forceinline__ void stage_units(float (*acc)[8], const int *udw, uin
   for (int s = 0; s < kSlots; s++) {
     const int d = udw[s];
     if (d < 0) continue;
-    const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
-    const int2 se = lds_i2(sse + 8 * e);
+    const int2 se = lds_i2(sse + 8 * d);
     if (se.y == 0) continue;
     hit |= 1u << s;
-    const uint32_t base = stage + (uint32_t)(j * (kRowBytes >> lk));
-    if (lk == 0) run_unit<T, 16, EX>(acc[s], srow + 4 * se.x, se.y, base + lane * 16, z);
-    else if (lk == 1) run_unit<T, 8, EX>(acc[s], srow + 4 * se.x, se.y, base + lane * 8, z);
-    else run_unit<T, 4, EX>(acc[s], srow + 4 * se.x, se.y, base + lane * 4, z);
+    run_unit<T, EX>(acc[s], srow + 4 * se.x, se.y, stage + lane * 16, z);
   }
 }
 
@@ -596,7 +503,8 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   // the consumers plan the part while the producer starts the first stages
-  if (warp < NW) plan_part(a.ws.ecount, a.E, gridDim.z, blockIdx.z, rank, ul, ud, threadIdx.x, NW * 32, 1);
+  if (warp < NW)
+    plan_part(a.ws.ecount, a.E, gridDim.z, blockIdx.z, a.nchunks * a.nsub, rank, ul, ud, threadIdx.x, NW * 32, 1);
 
   if (warp == NW) {
     // ---- producer: lane 0 issues the tile's row stages in consumption order --------------
@@ -686,8 +594,8 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
       auto unit_dst = [&](int s) -> float * {
         const int d = ud[warp][s];
         if (d < 0 || !((hit >> s) & 1u)) return nullptr;
-        const int e = d & 0xffff, j = (d >> 16) & 15, lk = d >> 20;
-        const int64_t c = col0 + (j * (kRowBytes >> lk) + lane * (16 >> lk)) / ESZ;
+        const int e = d;
+        const int64_t c = col0 + lane * (16 / ESZ);
         if (c >= a.cols) return nullptr;
         return split ? a.ws.partial + ((size_t)k * a.E + e) * a.cols + c : a.in_sum2 + (size_t)e * a.cols + c;
       };
@@ -698,12 +606,12 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
 #pragma unroll
         for (int s = h; s < h + kHalf && s < kSlots; s++) {
           const float *p = unit_dst(s);
-          if (p && !split) load_unit(p, old[s - h], (16 >> (ud[warp][s] >> 20)) / ESZ);
+          if (p && !split) load_unit<16 / ESZ>(p, old[s - h]);
         }
 #pragma unroll
         for (int s = h; s < h + kHalf && s < kSlots; s++) {
           float *p = unit_dst(s);
-          if (p) fin &= store_unit(p, acc[s], old[s - h], (16 >> (ud[warp][s] >> 20)) / ESZ, !split);
+          if (p) fin &= store_unit<16 / ESZ>(p, acc[s], old[s - h], !split);
         }
       }
     }
