@@ -392,6 +392,26 @@ __device__ __forceinline__ void run_unit(float *acc, uint32_t srow, int n, uint3
   A::run(acc, r0, z); A::run(acc, r1, z); A::run(acc, r2, z); A::run(acc, r3, z);
 }
 
+// One expert over the whole tile (a dense statistic): a warp takes 128 bytes of each row, a lane 4
+// (2 bf16 or 1 fp32 value), squared then added with two roundings; the run is padded to whole
+// groups of 4 as above.
+template <typename T>
+__device__ __forceinline__ void run_dense(float *acc, uint32_t srow, int n, uint32_t base, uint64_t z) {
+  auto add = [&](uint32_t u) {
+    if (std::is_same<T, __nv_bfloat16>::value) sq_add_bf16x2<true>(acc[0], acc[1], u, z);
+    else { const float x = __uint_as_float(u); acc[0] = __fadd_rn(acc[0], __fmul_rn(x, x)); }
+  };
+  const int n4 = (n + 3) & ~3;
+  uint4 o = lds_v4(srow);
+#pragma unroll 1
+  for (int j = 0; j < n4; j += 4) {
+    const uint4 on = lds_v4(srow + 4 * min(j + 4, n4 - 4));
+    const uint32_t r0 = lds_u32(base + o.x), r1 = lds_u32(base + o.y), r2 = lds_u32(base + o.z), r3 = lds_u32(base + o.w);
+    add(r0); add(r1); add(r2); add(r3);
+    o = on;
+  }
+}
+
 // The lane's NV (8 for bf16, 4 for fp32) current sums at src (16-byte aligned).
 template <int NV> __device__ __forceinline__ void load_unit(const float *src, float *v) {
 #pragma unroll
@@ -461,11 +481,13 @@ __device__ __forceinline__ bool stage_has_tiny(uint32_t tile, int rows, int lane
 }
 
 // 13 warps (fp32) or 15 (bf16: two screening warps): at most 128 registers a thread, as each warp
-// scheduler's quarter of the register file (16,384) must hold its warps (4 x 32 x 128).
-template <typename T> constexpr int acc_warps() {
-  return kMaxConsumers + 1 + (std::is_same<T, __nv_bfloat16>::value ? kScreenWarps : 0);
+// scheduler's quarter of the register file (16,384) must hold its warps (4 x 32 x 128).  A dense
+// statistic (one expert) runs 4 consumer warps, one per 128 bytes of the tile, and the producer.
+constexpr int kDenseWarps = 4;
+template <typename T, bool DENSE> constexpr int acc_warps() {
+  return DENSE ? kDenseWarps + 1 : kMaxConsumers + 1 + (std::is_same<T, __nv_bfloat16>::value ? kScreenWarps : 0);
 }
-template <typename T>
+template <typename T, bool DENSE>
 __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
     const __grid_constant__ CUtensorMap tmap, AccArgs a) {
   constexpr int TILE = Col<T>::TILE;
@@ -480,13 +502,13 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
   const uint32_t smem_s = smem_u32(smem);
   __shared__ uint64_t full_bar[kMaxStages], empty_bar[kMaxStages], chk_bar[kMaxStages];
   __shared__ int abort_flag, tiny_flag[kMaxStages][kScreenWarps];
-  constexpr bool kScan = std::is_same<T, __nv_bfloat16>::value;   // bf16 stages are screened
+  constexpr bool kScan = std::is_same<T, __nv_bfloat16>::value && !DENSE;   // bf16 stages are screened
   __shared__ int ud[kMaxConsumers][kSlots];  // the consumer warps' work units (the plan)
   __shared__ int16_t rank[1024];              // plan scratch: experts by rank
   __shared__ int2 ul[kPartUnits];             // plan scratch: the part's units
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  constexpr int NW = kMaxConsumers;
+  constexpr int NW = DENSE ? kDenseWarps : kMaxConsumers;
   const int64_t col0 = (int64_t)blockIdx.x * TILE;
   const bool split = a.ws.partial != nullptr;
   const int64_t kbeg = split ? blockIdx.y : 0, kend = split ? blockIdx.y + 1 : a.nchunks;
@@ -503,7 +525,7 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
   asm volatile("griddepcontrol.wait;" ::: "memory");
   __syncthreads();
   // the consumers plan the part while the producer starts the first stages
-  if (warp < NW)
+  if (!DENSE && warp < NW)
     plan_part(a.ws.ecount, a.E, gridDim.z, blockIdx.z, a.nchunks * a.nsub, rank, ul, ud, threadIdx.x, NW * 32, 1);
 
   if (warp == NW) {
@@ -557,6 +579,50 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
       atomicExch(&abort_flag, 1);
       if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
     }
+  } else if (DENSE) {
+    // ---- dense consumers: warp w takes bytes [128 w, 128 w + 128) of every row --------------------
+    constexpr int NV = 4 / ESZ;
+    const uint32_t lb = (uint32_t)(warp * 128 + lane * 4);
+    int64_t q = 0;
+    bool ok = true, fin = true;
+    for (int64_t k = kbeg; k < kend && ok; k++) {
+      const int64_t rows = min(a.rpc, a.tokens - k * a.rpc);
+      const int nsub = (int)((rows + a.sub - 1) / a.sub);
+      float acc[2] = {0.0f, 0.0f};
+      bool hit = false;
+      for (int sub = 0; sub < nsub; sub++, q++) {
+        const int st = (int)(q % NS);
+        if (!mbar_wait_bounded(&full_bar[st], (uint32_t)((q / NS) & 1)) || *(volatile int *)&abort_flag) {
+          ok = false;
+          break;
+        }
+        const uint32_t stage = smem_s + (uint32_t)st * kStageBytes;
+        const uint32_t sse = stage + kSegOff, srow = sse + (uint32_t)a.sl.offb;
+        const int2 se = lds_i2(sse);
+        if (se.y > 0) {
+          hit = true;
+          run_dense<T>(acc, srow + 4 * se.x, se.y, stage + lb, a.neg0);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[st]);
+      }
+      if (!ok) break;
+      const int64_t c = col0 + lb / ESZ;
+      if (hit && c < a.cols) {
+        float *p = split ? a.ws.partial + (size_t)k * a.cols + c : a.in_sum2 + c;
+#pragma unroll
+        for (int i = 0; i < NV; i++) {
+          const float v = split ? acc[i] : __fadd_rn(p[i], acc[i]);
+          p[i] = v;
+          fin &= isfinite(v);
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      atomicExch(&abort_flag, 1);
+      if (a.status) atomicOr(a.status, IQ_STATUS_TIMEOUT);
+    }
+    if (!split && a.status && __any_sync(0xffffffffu, !fin) && lane == 0) atomicOr(a.status, IQ_STATUS_NONFINITE_SUM2);
   } else {
     // ---- consumers: each warp walks its units (plan) over every stage --------------------------
     int64_t q = 0;
@@ -672,17 +738,17 @@ static bool make_tmap(CUtensorMap *m, const void *x, iq_dtype dt, int64_t tokens
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <typename T>
+template <typename T, bool DENSE>
 static int launch_accumulate(const CUtensorMap &tm, const AccArgs &a, const Plan &p, cudaStream_t st) {
   const size_t smem = (size_t)a.nstages * a.stage_bytes + 128;
-  auto kern = imatrix_accumulate_kernel<T>;
+  auto kern = imatrix_accumulate_kernel<T, DENSE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return IQ_ERR_CUDA;
   // programmatic dependent launch: the CTAs start (barriers, zero rows) while the route kernel
   // runs and wait for its completion before reading what it wrote
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.ntiles, p.split ? (unsigned)p.nchunks : 1u, (unsigned)p.nparts);
-  cfg.blockDim = dim3(32 * acc_warps<T>());
+  cfg.blockDim = dim3(32 * acc_warps<T, DENSE>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -746,7 +812,11 @@ extern "C" int iq_imatrix_accumulate(const void *x, iq_dtype dt, int64_t tokens,
   a.nstages = p.nstages;
   a.ws = ws; a.in_sum2 = in_sum2; a.status = status;
   a.neg0 = 0x8000000080000000ull;
-  const int rc = dt == IQ_BF16 ? launch_accumulate<__nv_bfloat16>(tm, a, p, st) : launch_accumulate<float>(tm, a, p, st);
+  const bool dense = num_experts == 1;
+  const int rc = dt == IQ_BF16 ? (dense ? launch_accumulate<__nv_bfloat16, true>(tm, a, p, st)
+                                        : launch_accumulate<__nv_bfloat16, false>(tm, a, p, st))
+                               : (dense ? launch_accumulate<float, true>(tm, a, p, st)
+                                        : launch_accumulate<float, false>(tm, a, p, st));
   if (rc != IQ_OK) return rc;
   if (p.split) {
     const int64_t n = (int64_t)num_experts * cols;

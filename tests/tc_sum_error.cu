@@ -9,6 +9,8 @@
 //   split sums     a . h with h = g^2 of integers g up to 127 (up to 14 significant bits) split
 //                  into exact tf32 parts hi + lo: a hi . h hi + a lo . h hi + a hi . h lo +
 //                  a lo . h lo (4 MMAs)
+//   encoder operands  plain sums whose a is the encoder's own per-vector operand (w, or
+//                  -2 w t) for blocks drawn like the bench weight and importance
 // Each result is compared with the exact value in fp64; the program prints the worst
 // |D - exact| / sum |terms| in units u = 2^-24 per operand kind.  All waits are bounded.
 #include <cstdio>
@@ -234,5 +236,42 @@ int main() {
     spl = std::max(spl, worst_of(D, ex, ab));
   }
   printf("split g2wide %.3f\n", spl);
+  // the encoder's own operands: for a block of 256 weights drawn like the bench weight (Student-t,
+  // 4 degrees of freedom) with importance drawn like the bench's (root mean square over 4096
+  // activation rows of N(0, 1) times a log-normal column scale), the per-vector operands are w and
+  // nw2 = -2 w t, with t the magnitude in grid units under a random choice c: |x| / (d (2c+1)/8),
+  // d = amax / 166.625 (the IQ2 anchor).  Both go against the four codebook operand kinds.
+  std::student_t_distribution<float> td(4.0f);
+  std::uniform_int_distribution<int> cd(0, 15);
+  double enc = 0;
+  for (int trial = 0; trial < 160; trial++) {
+    const int bk = trial % 4, wk = (trial / 4) % 2;
+    for (int blk = 0; blk < M * K / 256; blk++) {
+      float x[256], amax = 0.f;
+      for (int i = 0; i < 256; i++) { x[i] = 0.02f * td(rng); amax = std::max(amax, std::fabs(x[i])); }
+      const float d = amax / 166.625f;
+      for (int i = 0; i < 256; i++) {
+        const float sc = std::exp(nd(rng));
+        double ss = 0;
+        for (int r = 0; r < 4096; r += 64) { const double v = nd(rng) * sc; ss += v * v; }  // 64 of the rows
+        const float w = (float)std::sqrt(ss / 64.0);
+        const float t = std::fabs(x[i]) / (d * (2 * cd(rng) + 1) / 8.0f);
+        A[blk * 256 + i] = wk ? -2.0f * w * t : w;
+      }
+    }
+    for (auto &b : H) {
+      const int dd = ud(rng);
+      b = bk == 0 ? vals[dd] * vals[dd] : bk == 1 ? vals[dd] : bk == 2 ? (float)(dd - 1) : (float)std::abs(dd - 1);
+    }
+    if (!launch(2, 1.0f)) return 1;
+    for (int m = 0; m < M; m++)
+      for (int n = 0; n < N; n++) {
+        double e = 0, s = 0;
+        for (int k = 0; k < K; k++) { const double t = (double)A[m * K + k] * H[n * K + k]; e += t; s += std::fabs(t); }
+        ex[m * N + n] = e; ab[m * N + n] = s;
+      }
+    enc = std::max(enc, worst_of(D, ex, ab));
+  }
+  printf("plain encoder-operands %.3f\n", enc);
   return 0;
 }

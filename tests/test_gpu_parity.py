@@ -83,12 +83,14 @@ def test_decode_hand_assembled_fixtures():
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("T,C,E,K,R", [(2500, 192, 16, 4, 1024), (777, 64, 5, 2, 300), (4096, 128, 128, 8, 1024),
                                        (300, 256, 200, 3, 64), (600, 14336, 16, 2, 256), (301, 7168, 9, 3, 128),
-                                       (130, 14400, 1, 1, 1024), (1500, 14336, 16, 3, 256)])
+                                       (130, 14400, 1, 1, 1024), (1500, 14336, 16, 3, 256),
+                                       (3000, 320, 1, 1, 256), (4096, 2048, 1, 1, 1024)])
 def test_imatrix_bit_exact(dtype, T, C, E, K, R):
     """Both launch layouts: few column tiles (chunks in parallel, partials combined in chunk order)
     and many tiles (one CTA walks a tile's chunks in order); ragged chunks and column tiles; many
     chunks of two stages each, where consumer warps drift a whole chunk apart (each expert's sums
-    must keep one owner warp so their chunk-order additions stay ordered)."""
+    must keep one owner warp so their chunk-order additions stay ordered); the one-expert (dense)
+    layout, with a ragged tile and with the bench's 4096 x 2048 pass."""
     x32 = synth.activations(T, C, seed=T + C)
     store, xv = synth.as_dtype(x32, dtype)
     ids = synth.router(T, E, K, idle=max(1, E // 16) if E > 1 else 0, seed=E + K)
@@ -144,6 +146,20 @@ def test_imatrix_status_and_sets():
     xn = x.copy(); xn[7, 3] = np.inf
     st.zero_()
     api.imatrix_accumulate(torch.from_numpy(xn).to(DEV), torch.zeros(64, 1, dtype=torch.int32, device=DEV), 4, status=st)
+    assert int(st.item()) & api.STATUS_BITS["NONFINITE_SUM2"]
+    # one expert (the dense layout): ids other than 0 are skipped and reported, a non-finite value
+    # reaches the sums and is reported
+    x1 = synth.activations(700, 128, seed=6)
+    ids1 = np.zeros((700, 1), np.int32)
+    ids1[[5, 300, 650]] = [[1], [-1], [7]]
+    ref_s, ref_c, ref_st = oracle.imatrix_accumulate(x1, ids1, 1, rows_per_chunk=256)
+    st.zero_()
+    s2, cn = api.imatrix_accumulate(torch.from_numpy(x1).to(DEV), torch.from_numpy(ids1).to(DEV), 1, 256, status=st)
+    assert np.array_equal(host(s2).view(np.uint32), ref_s.view(np.uint32)) and np.array_equal(host(cn), ref_c)
+    assert int(st.item()) == ref_st == oracle.ST_BAD_EXPERT_ID
+    x1[10, 7] = np.nan
+    st.zero_()
+    api.imatrix_accumulate(torch.from_numpy(x1).to(DEV), torch.from_numpy(ids1).to(DEV), 1, 256, status=st)
     assert int(st.item()) & api.STATUS_BITS["NONFINITE_SUM2"]
 
 

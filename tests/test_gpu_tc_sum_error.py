@@ -8,7 +8,9 @@ on measurement.  tests/tc_sum_error.cu forms the sums as the encoder does (tf32 
 fp32 per-vector operand, the parts' MMAs accumulated into one tensor-memory column) for the plain
 sums (a . b with the four codebook operand kinds), the deferred-shift sums (w . h +- (w/4) . g,
 four MMAs into one column) and the split sums of IQ2 grids whose squares need more bits than tf32
-(a . (h hi + h lo), four MMAs), and prints the worst error over 160 random trials each.
+(a . (h hi + h lo), four MMAs), and the plain sums again with the encoder's own per-vector
+operands (w and -2 w t for blocks drawn like the bench weight and its imatrix importance), and
+prints the worst error over 160 random trials each.
 """
 import os
 import shutil
@@ -33,6 +35,6 @@ def test_tensor_core_sums_stay_within_the_margins_allowance(tmp_path):
         *name, value = line.split()
         worst[" ".join(name)] = float(value)
     assert set(worst) == {"plain g2", "plain g", "plain ternary", "plain absternary", "deferred plus",
-                          "deferred minus", "split g2wide"}, r.stdout
+                          "deferred minus", "split g2wide", "plain encoder-operands"}, r.stdout
     for name, u in worst.items():
         assert u <= ALLOWANCE_U, f"{name}: {u:.2f} u above the margin's {ALLOWANCE_U} u"
