@@ -52,10 +52,7 @@ constexpr int kPartUnits = kMaxConsumers * kSlots;  // units one CTA (part) can 
 constexpr int kMaxParts = 16;       // CTAs that share a column tile, each with its own experts
 constexpr int kMinSeqCtas = 112;    // below this many (tile, part) CTAs, chunks also run in parallel
 constexpr int kMaxTopK = 64;        // bounds the rows a segment holds
-constexpr size_t kSmemBudget = 220 * 1024;
-
-// cost of one (row, unit) pair in half instructions by column split (1, 2 or 4 parts of a row);
-// a unit with more parts covers fewer columns per lane for the same per-row overhead
+constexpr size_t kSmemBudget = 216 * 1024;   // stages; the kernel's static arrays take 7 KB more
 
 template <typename T> struct Col;
 template <> struct Col<__nv_bfloat16> { static constexpr int TILE = 256; };
@@ -161,21 +158,24 @@ __device__ __forceinline__ void named_barrier(int id, int nthreads) {
 // in (a run starts with two dependent shared-memory loads, and is padded to whole groups of 4):
 // c + 4 min(c, stages).  Cutting heavy experts into column parts was measured slower: the narrower
 // loads cost more per row than the better balance gains, as a long run streams at full speed.
-//   rank: [E] scratch, ul: [kPartUnits] scratch, ud: the plan slots; bar: a named barrier over the
-//   nthreads consumer threads (tid = their index).
-__device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts, int p, int64_t stages,
+//   cnt: [E] scratch (the counts), rank: [E] scratch, ul: [kPartUnits] scratch, ud: the plan slots;
+//   bar: a named barrier over the nthreads consumer threads (tid = their index).
+__device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts, int p, int64_t stages, int *cnt,
                           int16_t *rank, int2 *ul, int (*ud)[kSlots], int tid, int nthreads, int bar) {
+  for (int e = tid; e < E; e += nthreads) cnt[e] = ecount[e];
+  for (int i = tid; i < kMaxConsumers * kSlots; i += nthreads) ud[i / kSlots][i % kSlots] = -1;
+  named_barrier(bar, nthreads);
   // rank by counting: experts ahead of e have a larger count, or the same count and a lower id
   for (int e = tid; e < E; e += nthreads) {
-    const int c = __ldg(ecount + e);
+    const int c = cnt[e];
     int r = 0;
+#pragma unroll 8
     for (int j = 0; j < E; j++) {
-      const int cj = __ldg(ecount + j);
+      const int cj = cnt[j];
       r += (cj > c) | ((cj == c) & (j < e));
     }
     rank[r] = (int16_t)e;
   }
-  for (int i = tid; i < kMaxConsumers * kSlots; i += nthreads) ud[i / kSlots][i % kSlots] = -1;
   named_barrier(bar, nthreads);
   if (tid < 32) {
     const int lane = tid;
@@ -185,7 +185,7 @@ __device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts,
       const int l = l0 + lane;
       const int r = l * nparts + ((l & 1) ? nparts - 1 - p : p);
       int e = 0, c = 0;
-      if (l < nexp && r < E) { e = rank[r]; c = __ldg(ecount + e); }
+      if (l < nexp && r < E) { e = rank[r]; c = cnt[e]; }
       const unsigned has = __ballot_sync(0xffffffffu, c > 0);
       const int ui = base + __popc(has & ((1u << lane) - 1u));
       if (c > 0 && ui < kPartUnits) {
@@ -201,14 +201,19 @@ __device__ void plan_part(const int32_t *__restrict__ ecount, int E, int nparts,
     const int nu = min(base, kPartUnits);
     uint32_t load = 0;
     int nslot = 0;
-    for (int u = 0; u < nu; u++) {
-      const int2 d = ul[u];
-      const uint32_t k = lane < kMaxConsumers && nslot < kSlots ? load << 4 | (uint32_t)lane : 0xffffffffu;
-      const uint32_t w = __reduce_min_sync(0xffffffffu, k) & 15u;
-      if (lane == (int)w) {
-        ud[w][nslot] = d.x;
-        load = min(load + (uint32_t)d.y, 0x0fffffffu);
-        nslot++;
+    for (int u0 = 0; u0 < nu; u0 += 32) {                // 32 units at a time, one per lane
+      const int2 mine = u0 + lane < nu ? ul[u0 + lane] : make_int2(-1, 0);
+      const int n = min(32, nu - u0);
+#pragma unroll 4
+      for (int j = 0; j < n; j++) {
+        const int dx = __shfl_sync(0xffffffffu, mine.x, j), dy = __shfl_sync(0xffffffffu, mine.y, j);
+        const uint32_t k = lane < kMaxConsumers && nslot < kSlots ? load << 4 | (uint32_t)lane : 0xffffffffu;
+        const uint32_t w = __reduce_min_sync(0xffffffffu, k) & 15u;
+        if (lane == (int)w) {
+          ud[w][nslot] = dx;
+          load = min(load + (uint32_t)dy, 0x0fffffffu);
+          nslot++;
+        }
       }
     }
   }
@@ -456,22 +461,26 @@ __device__ __forceinline__ void stage_units(float (*acc)[8], const int *udw, uin
 constexpr int kScreenWarps = 2;
 
 // Whether a landed bf16 stage holds a value whose square is inexact in fp32 (flagged
-// conservatively: 0 < |x| < 2^-63, exponent field below 64).  The whole warp reads the tile (lane:
-// 16 bytes of every row): first a screen that also lets zeros through, then, only if it fires, the
-// exact test.
-__device__ __forceinline__ bool stage_has_tiny(uint32_t tile, int rows, int lane) {
-  uint32_t m = 0xffffffffu;
-#pragma unroll 8
-  for (int r = 0; r < rows; r++) {   // rows is a multiple of 8
+// conservatively: 0 < |x| < 2^-63, exponent field below 64).  Screening warp sw of kScreenWarps
+// reads rows sw, sw + kScreenWarps, ... (lane: 16 bytes of each): first the least magnitude per
+// lane and half (one bf16x2 minimum of magnitudes per word; NaN operands are passed over), then,
+// only if that is below 2^-63 or zero, the exact test.
+__device__ __forceinline__ bool stage_has_tiny(uint32_t tile, int rows, int sw, int lane) {
+  uint32_t m = 0x7f7f7f7fu;   // the largest finite bf16 in both halves
+#pragma unroll 4
+  for (int r = sw; r < rows; r += kScreenWarps) {
     const uint4 v = lds_v4(tile + (uint32_t)r * kRowBytes + lane * 16);
-    m &= (v.x | v.x << 1) & (v.y | v.y << 1) & (v.z | v.z << 1) & (v.w | v.w << 1);
+    asm("min.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.x));
+    asm("min.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.y));
+    asm("min.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.z));
+    asm("min.xorsign.abs.bf16x2 %0, %0, %1;" : "+r"(m) : "r"(v.w));
   }
-  // bit 14 of each half: exponent bit 7 or 6 set, i.e. exponent field >= 64
-  if (!__any_sync(0xffffffffu, (m & 0x40004000u) != 0x40004000u)) return false;
+  const bool low = (m & 0x7fffu) < 0x2000u || ((m >> 16) & 0x7fffu) < 0x2000u;
+  if (!__any_sync(0xffffffffu, low)) return false;
   auto tiny = [](uint32_t h) { return ((h & 0x7fffu) - 1u) < 0x1fffu; };
   bool t = false;
 #pragma unroll 4
-  for (int r = 0; r < rows; r++) {
+  for (int r = sw; r < rows; r += kScreenWarps) {
     const uint4 v = lds_v4(tile + (uint32_t)r * kRowBytes + lane * 16);
     const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -505,6 +514,7 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
   constexpr bool kScan = std::is_same<T, __nv_bfloat16>::value && !DENSE;   // bf16 stages are screened
   __shared__ int ud[kMaxConsumers][kSlots];  // the consumer warps' work units (the plan)
   __shared__ int16_t rank[1024];              // plan scratch: experts by rank
+  __shared__ int cnts[1024];                  // plan scratch: the counts over the call
   __shared__ int2 ul[kPartUnits];             // plan scratch: the part's units
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -526,7 +536,7 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
   __syncthreads();
   // the consumers plan the part while the producer starts the first stages
   if (!DENSE && warp < NW)
-    plan_part(a.ws.ecount, a.E, gridDim.z, blockIdx.z, a.nchunks * a.nsub, rank, ul, ud, threadIdx.x, NW * 32, 1);
+    plan_part(a.ws.ecount, a.E, gridDim.z, blockIdx.z, a.nchunks * a.nsub, cnts, rank, ul, ud, threadIdx.x, NW * 32, 1);
 
   if (warp == NW) {
     // ---- producer: lane 0 issues the tile's row stages in consumption order --------------
@@ -556,8 +566,8 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
         mbar_wait_bounded(&full_bar[u % NS], (uint32_t)((u / NS) & 1));
     }
   } else if (warp > NW) {
-    // ---- bf16 screening warps: each stage as it lands, half of its rows each ------------------
-    const int sw = warp - NW - 1, half = a.sub / kScreenWarps;
+    // ---- bf16 screening warps: each stage as it lands, every kScreenWarps-th row each ------------
+    const int sw = warp - NW - 1;
     int64_t q = 0;
     bool ok = true;
     for (int64_t k = kbeg; k < kend && ok; k++) {
@@ -567,8 +577,7 @@ __global__ void __launch_bounds__(32 * 16, 1) imatrix_accumulate_kernel(
         const int st = (int)(q % NS);
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full_bar[st], (uint32_t)((q / NS) & 1)));
         if (!ok || *(volatile int *)&abort_flag) { ok = false; break; }
-        const bool t =
-            stage_has_tiny(smem_s + (uint32_t)st * kStageBytes + (uint32_t)(sw * half) * kRowBytes, half, lane);
+        const bool t = stage_has_tiny(smem_s + (uint32_t)st * kStageBytes, a.sub, sw, lane);
         if (lane == 0) {
           *(volatile int *)&tiny_flag[st][sw] = t ? 1 : 0;
           mbar_arrive(&chk_bar[st]);
