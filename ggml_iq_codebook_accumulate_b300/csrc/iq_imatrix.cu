@@ -237,16 +237,27 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
   const int rows = (int)max((int64_t)0, min((int64_t)sub, rend - r0));
   for (int i = threadIdx.x; i < E * words; i += blockDim.x) bm[i / words][i % words] = 0u;
   __syncthreads();
+  // a warp takes one slot of 32 consecutive rows at a time; the lanes holding the same expert set
+  // their bits with one atomic (the rows of a 32-row group are one bitmap word)
   int st = 0;
-  for (int i = threadIdx.x; i < rows * top_k; i += blockDim.x) {
-    const int r = i / top_k, a = i % top_k;
-    const int32_t *row = ids + (r0 + r) * top_k;
-    const int e = row[a];
-    if (e < 0 || e >= E) { st |= IQ_STATUS_BAD_EXPERT_ID; continue; }
-    bool dup = false;
-    for (int b = 0; b < a; b++) dup |= (row[b] == e);
-    if (dup) { st |= IQ_STATUS_DUP_EXPERT_ID; continue; }
-    atomicOr(&bm[e][r >> 5], 1u << (r & 31));
+  const int lane = threadIdx.x & 31, groups = (rows + 31) / 32;
+  for (int idx = threadIdx.x >> 5; idx < groups * top_k; idx += blockDim.x >> 5) {
+    const int g = idx % groups, a = idx / groups, r = g * 32 + lane;
+    int e = -1;
+    if (r < rows) {
+      const int32_t *row = ids + (r0 + r) * top_k;
+      e = row[a];
+      if (e < 0 || e >= E) {
+        st |= IQ_STATUS_BAD_EXPERT_ID;
+        e = -1;
+      } else {
+        bool dup = false;
+        for (int b = 0; b < a; b++) dup |= (row[b] == e);
+        if (dup) { st |= IQ_STATUS_DUP_EXPERT_ID; e = -1; }
+      }
+    }
+    const unsigned same = __match_any_sync(0xffffffffu, e);
+    if (e >= 0 && lane == __ffs(same) - 1) atomicOr(&bm[e][g], same);
   }
   if (st && status) atomicOr(status, st);
   __syncthreads();
