@@ -480,12 +480,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   constexpr int NA = tc_na<F, MODE>();
   constexpr int NB = tc_nbuf<F, MODE>();
   float *aop0 = hlo + TcCfg<F>::HLO / 4;                    // [NB][NA][128 x 8] per-vector operands
-  float *xchg = aop0 + NB * NA * 1024;                      // [2][128][16] per-choice minima
+  float *xchg = aop0 + NB * NA * 1024;                      // [2][16][128] per-choice minima
   float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
   uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
-  float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][128][16] (every mode)
-  uint32_t *evk = reinterpret_cast<uint32_t *>(evm + 2 * 128 * 16); // [2][128][16] (every mode)
-  float *evt = reinterpret_cast<float *>(evk + 2 * 128 * 16);       // [2][128][16] (every mode)
+  float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][16][128] (every mode)
+  uint32_t *evk = reinterpret_cast<uint32_t *>(evm + 2 * 128 * 16); // [2][16][128] (every mode)
+  float *evt = reinterpret_cast<float *>(evk + 2 * 128 * 16);       // [2][16][128] (every mode)
   float4 *vst = reinterpret_cast<float4 *>(MODE == MODE_EVERY ? evt + 2 * 128 * 16 : evm);  // [NB][128]
   uint32_t *bst = reinterpret_cast<uint32_t *>(vst + NB * 128);     // [NB][4]
   __shared__ uint64_t cb_bar, full_bar[2], empty_bar[2], op_bar, op_full[2], op_empty[2];
@@ -811,10 +811,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       }
       // minima of the two consumer warps of this block
 #pragma unroll
-      for (int c = 0; c < C; c++) xchg[(sub * 128 + row) * 16 + c] = m[c];
+      for (int c = 0; c < C; c++) xchg[(sub * 16 + c) * 128 + row] = m[c];   // lanes on consecutive banks
       named_bar(2, kTcConsumers * 32);
 #pragma unroll
-      for (int c = 0; c < C; c++) m[c] = fminf(xchg[row * 16 + c], xchg[(128 + row) * 16 + c]);
+      for (int c = 0; c < C; c++) m[c] = fminf(xchg[c * 128 + row], xchg[(16 + c) * 128 + row]);
       if constexpr (MODE == MODE_EVERY) {
         // every choice's minimum and the bound above it that holds every candidate whose error
         // could be within the near-tie margin of the minimum (as in the searched second sweep)
@@ -823,10 +823,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           const float al = alpha_choice<F>(d, c);
           const float e1 = __fmul_rn(al, m[c]);
           const float De = 1.01f * kMargin * fmaxf(4.0f * vCs + 2.0f * e1, 0.0f);
-          evt[(sub * 128 + row) * 16 + c] =
+          evt[(sub * 16 + c) * 128 + row] =
               active ? m[c] + 1.01f * (De / al) + 9.5367431640625e-07f * fabsf(m[c]) : -INFINITY;
-          evm[(sub * 128 + row) * 16 + c] = m[c];
-          evk[(sub * 128 + row) * 16 + c] = 0xffffu;  // no key yet, no near candidate
+          evm[(sub * 16 + c) * 128 + row] = m[c];
+          evk[(sub * 16 + c) * 128 + row] = 0xffffu;  // no key yet, no near candidate
         }
       } else if (active) {
         float D1 = INFINITY, D2 = INFINITY;
@@ -865,9 +865,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       // minimum (the lowest entry whose score equals it exactly; the same MMAs and rounded packed
       // FMAs reproduce sweep 1's values) and the number of candidates at most T[c] (two or more
       // mean a near tie, which the exact rescoring re-decides under that choice).
-      const float *mrow = evm + (sub * 128 + row) * 16;
-      const float *trow = evt + (sub * 128 + row) * 16;
-      uint32_t *krow = evk + (sub * 128 + row) * 16;
+      // this vector's entries, choice c at [128 c] (lanes on consecutive banks)
+      const float *mrow = evm + sub * 16 * 128 + row;
+      const float *trow = evt + sub * 16 * 128 + row;
+      uint32_t *krow = evk + sub * 16 * 128 + row;
       for (int ch = 0; ch < NCH; ch++) {
         const int eb = ch * kChunk + ebase0;
         run_chunk(std::false_type{}, [&](int h, const float *An, const float *Cq, const float *Bq) {
@@ -903,15 +904,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           uint32_t hits = 0;  // choices whose minimum over this part is within the near bound
 #pragma unroll
           for (int c = 0; c < C; c += 4) {
-            const float4 t4 = *reinterpret_cast<const float4 *>(trow + c);
+            const float4 t4 = make_float4(trow[128 * c], trow[128 * (c + 1)], trow[128 * (c + 2)], trow[128 * (c + 3)]);
             hits |= (mn[c] <= t4.x ? 1u : 0u) << c | (mn[c + 1] <= t4.y ? 2u : 0u) << c |
                     (mn[c + 2] <= t4.z ? 4u : 0u) << c | (mn[c + 3] <= t4.w ? 8u : 0u) << c;
           }
           while (hits) {
             const int c = __ffs(hits) - 1;
             hits &= hits - 1u;
-            const float Tc = trow[c], mc = mrow[c];
-            uint32_t key = krow[c] & 0xffffu, cnt = krow[c] >> 16;
+            const float Tc = trow[128 * c], mc = mrow[128 * c];
+            uint32_t key = krow[128 * c] & 0xffffu, cnt = krow[128 * c] >> 16;
             const int sc = F == IQ1_S ? (c & 7) : c;
             const int db = F == IQ1_S ? (c >> 3) : 0;
             const float alf = alpha_of<F>(d, sc);  // as alp[sc]
@@ -947,7 +948,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
                 }
               }
             }
-            krow[c] = key | (min(cnt, 3u) << 16);
+            krow[128 * c] = key | (min(cnt, 3u) << 16);
           }
         });
       }
@@ -955,7 +956,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       if (sub == 0 && active) {
         uint32_t *pb = packbuf + quarter * 24;
         for (int c = 0; c < C; c++) {
-          const uint32_t w0 = evk[row * 16 + c], w1 = evk[(128 + row) * 16 + c];
+          const uint32_t w0 = evk[c * 128 + row], w1 = evk[(16 + c) * 128 + row];
           const uint32_t key = min(w0 & 0xffffu, w1 & 0xffffu);
           const uint32_t cnt = (w0 >> 16) + (w1 >> 16);
           // near ties under choice c: one item (block | c << 27, vectors) for the exact rescoring
