@@ -57,8 +57,8 @@ REF_CONFIG = {"workload": CONFIG["workload"], "rows": R, "cols": C, "activation_
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of the searched encode
 # kernel on this workload, from ncu captures of that launch, and the SHA-256 of the encoder
 # sources they were taken on: the figure is reported only while the sources are unchanged.
-PROFILED_ENCODE_TRAFFIC = {"IQ2_XXS": 23198464, "IQ1_S": 23277824, "IQ1_M": 23282432}
-PROFILED_ENCODE_SHA256 = "730093de705c8b4b63d613d01f9eca35ac8a8d474bbf4a970b708f1167110505"
+PROFILED_ENCODE_TRAFFIC = {"IQ2_XXS": 23197952, "IQ1_S": 23277056, "IQ1_M": 23280640}
+PROFILED_ENCODE_SHA256 = "7aa7c68e19b97fa1eb81e01c1ff6d864f75025704e9869072a1a1d74855b0b69"
 ENCODE_SOURCES = ("ggml_iq_codebook_accumulate_b300/csrc/iq_encode.cu", "ggml_iq_codebook_accumulate_b300/csrc/iq_common.cuh")
 
 
@@ -716,8 +716,11 @@ def measure_write_back(args, dev, flush, W0, G, w):
 def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
     """The same step through the public API with host inputs: pinned host -> device copies of the
     weight and activations, and device -> host copies of the five searched payloads and their
-    every-choice error tables, timed.  Each format's copies run on a second stream while the next
-    format is encoded; the step ends when both streams are done."""
+    every-choice error tables, all inside the timed region.  The steps are pipelined as a
+    production loop would run them: each step's inputs are copied into one of two device buffers
+    on their own stream while the previous step computes (the first step's copy is not
+    overlapped), and each format's outputs are copied back on a second stream while the next
+    format is encoded; the region ends when every stream is done."""
     import torch
 
     from ggml_iq_codebook_accumulate_b300 import api
@@ -727,16 +730,29 @@ def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
     outs = {f: torch.empty(B, info[f]["block_bytes"], dtype=torch.uint8).pin_memory() for f in FORMATS}
     touts = {f: torch.empty(B, info[f]["choice_groups"], info[f]["num_choices"], dtype=torch.float32).pin_memory()
              for f in FORMATS}
-    W = torch.empty(R, C, dtype=torch.bfloat16, device=dev)
-    X = torch.empty(T_ACT, C, dtype=torch.bfloat16, device=dev)
+    Wd = [torch.empty(R, C, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    Xd = [torch.empty(T_ACT, C, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     ch7 = {f: torch.full((B, info[f]["choice_groups"]), 7, dtype=torch.uint8, device=dev) for f in FORMATS}
 
     compute = torch.cuda.current_stream(dev)
-    copier = torch.cuda.Stream(dev)
+    copier = torch.cuda.Stream(dev)     # results back to the host
+    loader = torch.cuda.Stream(dev)     # the next step's inputs to the device
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
 
-    def step():
-        W.copy_(Wh, non_blocking=True)
-        X.copy_(Xh, non_blocking=True)
+    def load(k):
+        with torch.cuda.stream(loader):
+            if k >= 2:
+                loader.wait_event(free[k % 2])        # step k - 2 is done with this buffer
+            Wd[k % 2].copy_(Wh, non_blocking=True)
+            Xd[k % 2].copy_(Xh, non_blocking=True)
+            ready[k % 2].record(loader)
+
+    def step(k, last):
+        compute.wait_event(ready[k % 2])
+        if not last:
+            load(k + 1)
+        W, X = Wd[k % 2], Xd[k % 2]
         s2, cn = api.imatrix_accumulate(X, ids, 1, 1024)
         w = api.imatrix_weights(s2, cn)
         for f in FORMATS:
@@ -749,20 +765,27 @@ def measure_e2e(args, dev, Wst, Xst, grids, G, ids, info):
             t.record_stream(copier)
             api.encode(f, W, G[f], importance=w[0], choices=ch7[f])
             api.decode(f, p, R, C, G[f])
+        free[k % 2].record(compute)
+
+    def run(n):
+        load(0)
+        for k in range(n):
+            step(k, k == n - 1)
         compute.synchronize()
         copier.synchronize()
+        loader.synchronize()
 
-    for _ in range(2):
-        step()
-    t0 = time.perf_counter()
+    run(2)
     n = max(1, args.steps)
-    for _ in range(n):
-        step()
+    t0 = time.perf_counter()
+    run(n)
     dt = (time.perf_counter() - t0) / n
     h2d = Wh.numel() * 2 + Xh.numel() * 2
     d2h = sum(o.numel() for o in outs.values()) + sum(t.numel() * 4 for t in touts.values())
     return {"value": round(5 * R * C / dt / 1e6, 2), "unit": "M elem/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3)}
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(dt * 1e3, 3),
+            "pipelining": "inputs of step k+1 copied during step k (double-buffered); outputs copied "
+                          "back during the next format's encode"}
 
 
 def main():

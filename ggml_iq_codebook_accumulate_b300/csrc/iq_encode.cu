@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   constexpr int NA = tc_na<F, MODE>();
   constexpr int NB = tc_nbuf<F, MODE>();
   float *aop0 = hlo + TcCfg<F>::HLO / 4;                    // [NB][NA][128 x 8] per-vector operands
-  float *xchg = aop0 + NB * NA * 1024;                      // [2][16][128] per-choice minima
+  float *xchg = aop0 + NB * NA * 1024;                      // [2][4][128][4] per-choice minima
   float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
   uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
   float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][16][128] (every mode)
@@ -810,11 +810,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
         });
       }
       // minima of the two consumer warps of this block
+      // 4 choices per 16-byte word, lanes on consecutive words: one conflict-free vector store each
 #pragma unroll
-      for (int c = 0; c < C; c++) xchg[(sub * 16 + c) * 128 + row] = m[c];   // lanes on consecutive banks
+      for (int c = 0; c < C; c += 4)
+        *reinterpret_cast<float4 *>(xchg + ((sub * 4 + c / 4) * 128 + row) * 4) = make_float4(m[c], m[c + 1], m[c + 2], m[c + 3]);
       named_bar(2, kTcConsumers * 32);
 #pragma unroll
-      for (int c = 0; c < C; c++) m[c] = fminf(xchg[c * 128 + row], xchg[(16 + c) * 128 + row]);
+      for (int c = 0; c < C; c += 4) {
+        const float4 u = *reinterpret_cast<const float4 *>(xchg + ((c / 4) * 128 + row) * 4);
+        const float4 v = *reinterpret_cast<const float4 *>(xchg + ((4 + c / 4) * 128 + row) * 4);
+        m[c] = fminf(u.x, v.x); m[c + 1] = fminf(u.y, v.y); m[c + 2] = fminf(u.z, v.z); m[c + 3] = fminf(u.w, v.w);
+      }
       if constexpr (MODE == MODE_EVERY) {
         // every choice's minimum and the bound above it that holds every candidate whose error
         // could be within the near-tie margin of the minimum (as in the searched second sweep)
