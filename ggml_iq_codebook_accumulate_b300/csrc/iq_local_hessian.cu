@@ -160,9 +160,12 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
     for (int r = 0; r < R; r++)
       Xs[tid * R + r] = r < nr ? to_f(W[(size_t)(r0 + r) * cols + j * 256 + tid]) : 0.0f;
     // ---- every (row, choice) block of the tile: bytes staged, then unpacked --------------------
-    for (int t = tid; t < R * NC * BB; t += kLhThreads) {
-      const int rc = t / BB, bi = t % BB, r = rc / NC, c = rc % NC;
-      pstage[t] = r < nr ? payloads[((size_t)c * rows * nb + (size_t)(r0 + r) * nb + j) * BB + bi] : (uint8_t)0;
+    static_assert(BB % 2 == 0, "payload blocks are whole 16-bit words");
+    for (int t = tid; t < R * NC * (BB / 2); t += kLhThreads) {   // 16-bit words (blocks start even)
+      const int rc = t / (BB / 2), bi = t % (BB / 2), r = rc / NC, c = rc % NC;
+      reinterpret_cast<uint16_t *>(pstage)[t] =
+          r < nr ? reinterpret_cast<const uint16_t *>(payloads + ((size_t)c * rows * nb + (size_t)(r0 + r) * nb + j) * BB)[bi]
+                 : (uint16_t)0;
     }
     __syncthreads();
     if (tid < R * NC) lh_unpack<F>(pstage + tid * BB, alph + tid * G, code + tid * 32);
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
       for (int r = 0; r < R; r++) acc[r] = 0.0f;
       for (int kg = 0; kg < G; kg++) {
         if (kg == gi) continue;
-#pragma unroll 4
+#pragma unroll 16
         for (int kk = 0; kk < GS; kk++) {
           const int k = kg * GS + kk;
           const float h = __ldg(Hj + (size_t)k * 256 + tid);
@@ -255,6 +258,13 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
     // ---- step 3: two revisits ------------------------------------------------------------------
     for (int pass = 0; pass < 2; pass++) {
       for (int g = 0; g < G; g++) {
+        // group g's Hessian panel for this thread's column, loaded now so its latency overlaps the
+        // move evaluation (used only if a row moves)
+        float hp[GS];
+        if (tid / GS != g) {
+#pragma unroll
+          for (int k = 0; k < GS; k++) hp[k] = __ldg(Hj + (size_t)(g * GS + k) * 256 + tid);
+        }
         if (tid == 0) moved = 0;
         if (tid / GS == g) {
 #pragma unroll
@@ -311,9 +321,9 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
         __syncthreads();
         // (c) U of the other groups' columns += H'[., g panel] * change
         if (moved && tid / GS != g) {
-#pragma unroll 4
+#pragma unroll
           for (int k = 0; k < GS; k++) {
-            const float h = __ldg(Hj + (size_t)(g * GS + k) * 256 + tid);
+            const float h = hp[k];
             const float4 *d4 = reinterpret_cast<const float4 *>(Dl + k * R);
 #pragma unroll
             for (int q = 0; q < R / 4; q++) {
@@ -373,7 +383,8 @@ extern "C" int iq_local_hessian_choices(iq_format f, const void *W, iq_dtype dt,
   const int64_t nb = rows * (cols / 256);
   if (nb == 0) return IQ_OK;
   if (!W || !grid || !payloads || !hessian || !choices) return IQ_ERR_ARG;
-  if (((uintptr_t)W & 15) || ((uintptr_t)grid & 15) || ((uintptr_t)hessian & 15)) return IQ_ERR_ARG;
+  if (((uintptr_t)W & 15) || ((uintptr_t)grid & 15) || ((uintptr_t)hessian & 15) || ((uintptr_t)payloads & 1))
+    return IQ_ERR_ARG;
   (void)workspace;
   (void)workspace_bytes;
   cudaStream_t st = (cudaStream_t)stream;

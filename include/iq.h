@@ -228,7 +228,8 @@ IQ_API int iq_encode_every_choice(iq_format f, const void *W, iq_dtype dt, int64
  * from an exact evaluation only where two choices' errors are within fp32 rounding of each other.
  *   W          device [rows, cols] of dtype dt, 16-byte aligned (the weight being encoded)
  *   grid       device fp32 [grid_entries, 8], 16-byte aligned
- *   payloads   device uint8 [num_choices, B, block_bytes] (iq_encode_every_choice)
+ *   payloads   device uint8 [num_choices, B, block_bytes] (iq_encode_every_choice), 2-byte
+ *              aligned (read as 16-bit words; every block_bytes is even)
  *   hessian    device fp32 [cols / 256, 256, 256]: the diagonal blocks of the symmetric input
  *              Hessian, block j for columns 256 j ... 256 j + 255; 16-byte aligned
  *   perc_damp  finite, >= 0

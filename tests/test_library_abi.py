@@ -86,6 +86,7 @@ def test_local_hessian_host_checks():
     assert call(f=9) == -1                           # no such format
     assert call(H=None) == -1 and call(pay=None) == -1 and call(ch=None) == -1
     assert call(H=fake + 4) == -1                    # Hessian not 16-byte aligned
+    assert call(pay=fake + 1) == -1                  # payloads read as 16-bit words
     assert L.iq_encode_every_choice(0, fake, api.IQ_BF16, 4, 500, None, 0, fake, None, fake, None, fake, 1 << 30,
                                     None) == -1      # cols % 256
 
