@@ -94,6 +94,35 @@ __device__ __forceinline__ float lh_value(const float *alph, const uint32_t *cod
   return __fmul_rn(al, __fadd_rn(gv, (cd >> 24) ? -0.125f : 0.125f));
 }
 
+// Packed fp32x2 multiply-add: two IEEE fp32 fma, each rounded on its own (the same values as two
+// scalar __fmaf_rn).
+__device__ __forceinline__ uint64_t lh_pk2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 lh_up2(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t lh_fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+// acc[4q .. 4q + 3] += h * d[q] for q < n4, as packed pairs
+template <int n4>
+__device__ __forceinline__ void lh_axpy4(uint64_t *acc2, float h, const float4 *d4) {
+  const uint64_t hh = lh_pk2(h, h);
+#pragma unroll
+  for (int q = 0; q < n4; q++) {
+    const float4 d = d4[q];
+    acc2[2 * q] = lh_fma2(hh, lh_pk2(d.x, d.y), acc2[2 * q]);
+    acc2[2 * q + 1] = lh_fma2(hh, lh_pk2(d.z, d.w), acc2[2 * q + 1]);
+  }
+}
+
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
@@ -178,34 +207,26 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
       if (r < nr) {
         // every choice side by side: NC independent multiply-add chains over the group
         const float x = Xs[i * R + r];
-        float dw[NC], y[NC];
+        float dw[NC];
+        uint64_t y2[NC / 2];
         float *ds = Ds + warp * 32 * NC;  // lane's row: the NC values of its element
 #pragma unroll
-        for (int c = 0; c < NC; c++) {
-          dw[c] = __fsub_rn(x, qv(r, c, i));
-          y[c] = 0.0f;
-        }
+        for (int c = 0; c < NC; c++) dw[c] = __fsub_rn(x, qv(r, c, i));
+#pragma unroll
+        for (int c = 0; c < NC / 2; c++) y2[c] = 0ull;
 #pragma unroll
         for (int c = 0; c < NC; c += 4)
           *reinterpret_cast<float4 *>(ds + lane * NC + c) = make_float4(dw[c], dw[c + 1], dw[c + 2], dw[c + 3]);
         __syncwarp();
         const float *seg = ds + (lane / GS) * GS * NC;  // the lane's group's elements
 #pragma unroll 2
-        for (int b = 0; b < GS; b++) {
-          const float h = Hgg[(g * GS + b) * GS + a];
-#pragma unroll
-          for (int c = 0; c < NC; c += 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(seg + b * NC + c);
-            y[c] = __fmaf_rn(h, v.x, y[c]);
-            y[c + 1] = __fmaf_rn(h, v.y, y[c + 1]);
-            y[c + 2] = __fmaf_rn(h, v.z, y[c + 2]);
-            y[c + 3] = __fmaf_rn(h, v.w, y[c + 3]);
-          }
-        }
+        for (int b = 0; b < GS; b++)
+          lh_axpy4<NC / 4>(y2, Hgg[(g * GS + b) * GS + a], reinterpret_cast<const float4 *>(seg + b * NC));
         __syncwarp();
 #pragma unroll
         for (int c = 0; c < NC; c++) {
-          float p = __fmul_rn(dw[c], y[c]);
+          const float2 yp = lh_up2(y2[c / 2]);
+          float p = __fmul_rn(dw[c], (c & 1) ? yp.y : yp.x);
 #pragma unroll
           for (int off = GS / 2; off >= 1; off >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, off, GS));
           if (a == 0) Qe[(r * G + g) * NC + c] = p;
@@ -231,27 +252,17 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
     __syncthreads();
     // ---- U = H'_offdiag dw: thread tid owns column tid (in registers; the visited group's slice is
     // published to shared memory before each visit) ----------------------------------------------
-    float ureg[R];
+    uint64_t ureg2[R / 2];   // U of this thread's column for the tile's rows, as packed pairs
     {
       const int gi = tid / GS;
-      float *acc = ureg;
 #pragma unroll
-      for (int r = 0; r < R; r++) acc[r] = 0.0f;
+      for (int r = 0; r < R / 2; r++) ureg2[r] = 0ull;
       for (int kg = 0; kg < G; kg++) {
         if (kg == gi) continue;
 #pragma unroll 16
         for (int kk = 0; kk < GS; kk++) {
           const int k = kg * GS + kk;
-          const float h = __ldg(Hj + (size_t)k * 256 + tid);
-          const float4 *d4 = reinterpret_cast<const float4 *>(DWt + k * R);
-#pragma unroll
-          for (int q = 0; q < R / 4; q++) {
-            const float4 d = d4[q];
-            acc[4 * q] = __fmaf_rn(h, d.x, acc[4 * q]);
-            acc[4 * q + 1] = __fmaf_rn(h, d.y, acc[4 * q + 1]);
-            acc[4 * q + 2] = __fmaf_rn(h, d.z, acc[4 * q + 2]);
-            acc[4 * q + 3] = __fmaf_rn(h, d.w, acc[4 * q + 3]);
-          }
+          lh_axpy4<R / 4>(ureg2, __ldg(Hj + (size_t)k * 256 + tid), reinterpret_cast<const float4 *>(DWt + k * R));
         }
       }
     }
@@ -268,7 +279,11 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
         if (tid == 0) moved = 0;
         if (tid / GS == g) {
 #pragma unroll
-          for (int r = 0; r < R; r++) U[tid * R + r] = ureg[r];
+          for (int r = 0; r < R / 2; r++) {
+            const float2 u2 = lh_up2(ureg2[r]);
+            U[tid * R + 2 * r] = u2.x;
+            U[tid * R + 2 * r + 1] = u2.y;
+          }
         }
         __syncthreads();
         // (a) every row's best move for group g: a warp per row, GPW choices side by side
@@ -322,18 +337,7 @@ __global__ void __launch_bounds__(kLhThreads, 1) lh_search_kernel(const TIn *__r
         // (c) U of the other groups' columns += H'[., g panel] * change
         if (moved && tid / GS != g) {
 #pragma unroll
-          for (int k = 0; k < GS; k++) {
-            const float h = hp[k];
-            const float4 *d4 = reinterpret_cast<const float4 *>(Dl + k * R);
-#pragma unroll
-            for (int q = 0; q < R / 4; q++) {
-              const float4 d = d4[q];
-              ureg[4 * q] = __fmaf_rn(h, d.x, ureg[4 * q]);
-              ureg[4 * q + 1] = __fmaf_rn(h, d.y, ureg[4 * q + 1]);
-              ureg[4 * q + 2] = __fmaf_rn(h, d.z, ureg[4 * q + 2]);
-              ureg[4 * q + 3] = __fmaf_rn(h, d.w, ureg[4 * q + 3]);
-            }
-          }
+          for (int k = 0; k < GS; k++) lh_axpy4<R / 4>(ureg2, hp[k], reinterpret_cast<const float4 *>(Dl + k * R));
         }
         __syncthreads();
       }
