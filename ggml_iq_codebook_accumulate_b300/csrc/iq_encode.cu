@@ -153,11 +153,16 @@ __global__ void prep_codebook(const float *__restrict__ grid, EncWs ws) {
 }
 
 struct Entry { float g[8], h[8]; };
+// Entry e from the caller's codebook [N][8] (two 16-byte loads), with h formed as prep_codebook
+// forms it (g^2 for IQ2, |g| for IQ1; exact).
 template <int F>
-__device__ __forceinline__ void load_entry(const float4 *tab, int e, Entry &en) {
-  const float *tf = reinterpret_cast<const float *>(tab);
+__device__ __forceinline__ void load_entry(const float *grid, int e, Entry &en) {
+  const float4 p = __ldg(reinterpret_cast<const float4 *>(grid + 8 * e));
+  const float4 q = __ldg(reinterpret_cast<const float4 *>(grid + 8 * e) + 1);
+  en.g[0] = p.x; en.g[1] = p.y; en.g[2] = p.z; en.g[3] = p.w;
+  en.g[4] = q.x; en.g[5] = q.y; en.g[6] = q.z; en.g[7] = q.w;
 #pragma unroll
-  for (int i = 0; i < 8; i++) { en.g[i] = tf[kmaj(e, i)]; en.h[i] = tf[Fmt<F>::N * 8 + kmaj(e, i)]; }
+  for (int i = 0; i < 8; i++) en.h[i] = Fmt<F>::IQ1 ? fabsf(en.g[i]) : __fmul_rn(en.g[i], en.g[i]);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1333,9 +1338,10 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
           cand_of_choice<F>(c, s, db0, db1);
           alc[c] = alpha_of<F>(d, s);
         }
+#pragma unroll 4
         for (int e = js * SL + lane; kvflag && e < (js + 1) * SL; e += 32) {
           Entry en;
-          load_entry<F>(tab, e, en);
+          load_entry<F>(a.grid, e, en);
           // the entry's sums once, then every choice's score as cand_score forms it
           float An = 0.0f, Bs = 0.0f, Anp = 0.0f, Bp = 0.0f, Anm = 0.0f, Bm = 0.0f;
           if (!Fmt<F>::IQ1) ab2(u.nw2, u.w, en, An, Bs);
@@ -1401,9 +1407,10 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         const float emin = __fmul_rn(al, sm.mh[k][c]);
         double bestE = INFINITY;
         int bestK = 0x7fffffff;
+#pragma unroll 4
         for (int e = j * SL + lane; e < (j + 1) * SL; e += 32) {
           Entry en;
-          load_entry<F>(tab, e, en);
+          load_entry<F>(a.grid, e, en);
           for (int db = db0; db <= db1; db++) {
             const float sc = cand_score<F>(u, en, al, db);
             const float ec = __fmul_rn(al, sc);
@@ -1531,9 +1538,10 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
           cand_of_choice<F>(c, s, db0, db1);
           alc[c] = alpha_of<F>(d, s);
         }
+#pragma unroll 4
         for (int e = lane; e < N; e += 32) {
           Entry en;
-          load_entry<F>(tab, e, en);
+          load_entry<F>(a.grid, e, en);
           // the entry's sums once, then every choice's score as cand_score forms it
           float An = 0.0f, Bs = 0.0f, Anp = 0.0f, Bp = 0.0f, Anm = 0.0f, Bm = 0.0f;
           if (!Fmt<F>::IQ1) ab2(u.nw2, u.w, en, An, Bs);
@@ -1589,9 +1597,10 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
           const float emin = __fmul_rn(al, mh);
           double bestE = INFINITY;
           int bestK = 0x7fffffff;
-          for (int e = lane; e < N; e += 32) {
+  #pragma unroll 4
+        for (int e = lane; e < N; e += 32) {
             Entry en;
-            load_entry<F>(tab, e, en);
+            load_entry<F>(a.grid, e, en);
             for (int db = db0; db <= db1; db++) {
               const float sc = cand_score<F>(u, en, al, db);
               const float ec = __fmul_rn(al, sc);
