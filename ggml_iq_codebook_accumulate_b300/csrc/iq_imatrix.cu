@@ -25,12 +25,13 @@
 //              shared-memory stages: each stage is one 2-D TMA tensor copy of the sub-tile's rows
 //              plus one bulk copy of its segment, both completing on the stage's mbarrier (all
 //              waits bounded by the global timer).  Meanwhile the 12 consumer warps plan their
-//              part (ranked experts, heavy ones cut into 2 or 4 column parts, units dealt so the
-//              warps' loads match); then each walks its units' rows, 4 at a time, from shared
-//              memory (a unit's lane reads 16, 8 or 4 bytes of a row) into one register
-//              accumulator per (unit, column of its lane).  For bf16, two screening warps check
-//              each landed stage for values whose squares are inexact in fp32; stages without
-//              any take one mixed-precision FMA per value, the others square and add separately;
+//              part (ranked experts, each dealt whole to the least-loaded warp); then each walks
+//              its experts' rows, 4 at a time, from shared memory (a lane reads 16 bytes of a
+//              row) into one register accumulator per (expert, column of its lane).  For bf16,
+//              two screening warps check each landed stage for values whose squares are inexact
+//              in fp32; stages without any take one mixed-precision FMA per value, the others
+//              square and add separately.  With one expert (a dense statistic) 4 consumer warps
+//              take 128 bytes of every row each, with no plan and no screening;
 //  combine     (per-chunk mode only) adds the chunk partials to in_sum2 in chunk order.
 // No atomics touch in_sum2, so the sums are the sequential definition above.
 #include <cudaTypedefs.h>
@@ -113,8 +114,8 @@ static Plan make_plan(int64_t tokens, int64_t cols, iq_dtype dt, int E, int top_
   p.nsub = (int)((rpc + p.sub - 1) / p.sub);
   const int tile = dt == IQ_BF16 ? Col<__nv_bfloat16>::TILE : Col<float>::TILE;
   p.ntiles = (cols + tile - 1) / tile;
-  // parts per tile: enough to hold one unit per expert (splits take only the room left), and as
-  // many as fill the SMs (at most one per expert)
+  // parts per tile: enough that a part's experts fit its warps' slots, and as many as fill the
+  // SMs (at most one per expert)
   const int need = (E + kPartUnits - 1) / kPartUnits;
   int fill = (int)(sms / p.ntiles);
   if (fill > E) fill = E;
