@@ -485,7 +485,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
   constexpr int NA = tc_na<F, MODE>();
   constexpr int NB = tc_nbuf<F, MODE>();
   float *aop0 = hlo + TcCfg<F>::HLO / 4;                    // [NB][NA][128 x 8] per-vector operands
-  float *xchg = aop0 + NB * NA * 1024;                      // [2][4][128][4] per-choice minima
+  float *xchg = aop0 + NB * NA * 1024;                      // [2][128][4] float4 per-choice minima, swizzled
+  // the 16-byte word w (choices 4w .. 4w + 3) of vector r in warp half h: its 128-byte segment's
+  // slots permuted by (r / 4) mod 8, so that a warp reading its own rows, or the rows of its lanes'
+  // groups at per-lane words, spreads over all bank groups
+  auto xw = [&](int h, int r, int w) -> float4 * {
+    return reinterpret_cast<float4 *>(xchg) + h * 512 + ((r * 4 + w) ^ ((r >> 2) & 7));
+  };
   float4 *xchg2 = reinterpret_cast<float4 *>(xchg + 2 * 128 * 16);  // [2][128] (best, second, key)
   uint32_t *packbuf = reinterpret_cast<uint32_t *>(xchg2 + 2 * 128); // [4][24]
   float *evm = reinterpret_cast<float *>(packbuf + 4 * 24);        // [2][16][128] (every mode)
@@ -817,16 +823,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
       // minima of the two consumer warps of this block
       // 4 choices per 16-byte word, lanes on consecutive words: one conflict-free vector store each
 #pragma unroll
-      for (int c = 0; c < C; c += 4)
-        *reinterpret_cast<float4 *>(xchg + ((sub * 4 + c / 4) * 128 + row) * 4) = make_float4(m[c], m[c + 1], m[c + 2], m[c + 3]);
+      for (int c = 0; c < C; c += 4) *xw(sub, row, c / 4) = make_float4(m[c], m[c + 1], m[c + 2], m[c + 3]);
       named_bar(2, kTcConsumers * 32);
-#pragma unroll
-      for (int c = 0; c < C; c += 4) {
-        const float4 u = *reinterpret_cast<const float4 *>(xchg + ((c / 4) * 128 + row) * 4);
-        const float4 v = *reinterpret_cast<const float4 *>(xchg + ((4 + c / 4) * 128 + row) * 4);
-        m[c] = fminf(u.x, v.x); m[c + 1] = fminf(u.y, v.y); m[c + 2] = fminf(u.z, v.z); m[c + 3] = fminf(u.w, v.w);
-      }
       if constexpr (MODE == MODE_EVERY) {
+#pragma unroll
+        for (int c = 0; c < C; c += 4) {
+          const float4 u = *xw(0, row, c / 4), v = *xw(1, row, c / 4);
+          m[c] = fminf(u.x, v.x); m[c + 1] = fminf(u.y, v.y); m[c + 2] = fminf(u.z, v.z); m[c + 3] = fminf(u.w, v.w);
+        }
         // every choice's minimum and the bound above it that holds every candidate whose error
         // could be within the near-tie margin of the minimum (as in the searched second sweep)
 #pragma unroll
@@ -840,15 +844,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) encode_tc_kernel(EncArgs a, Enc
           evk[(sub * 16 + c) * 128 + row] = 0xffffu;  // no key yet, no near candidate
         }
       } else if (active) {
+        // the group's VPG lanes share its choices: lane kq forms the group errors of choices
+        // kq * CPL .. kq * CPL + CPL - 1 (the group's minima of both warps, summed in vector order),
+        // then the lanes merge (least error, lowest choice on equal errors, and the runner-up)
+        constexpr int CPL = C / VPG;
+        static_assert(CPL % 4 == 0, "whole 16-byte words of choices");
+        const int kq = lane - g0;
         float D1 = INFINITY, D2 = INFINITY;
 #pragma unroll
-        for (int c = 0; c < C; c++) {
-          const float S = group_sum<VPG>(m[c], g0);
-          const float D = __fmul_rn(alpha_of<F>(d, F == IQ1_S ? (c & 7) : c), S);
-          if (a.table && sub == 0 && lane == g0) a.table[(b * G + cg) * C + c] = __fadd_rn(Cgrp, D);
-          D2 = fminf(D2, fmaxf(D1, D));
-          if (D < D1) { D1 = D; c1 = c; smin = m[c]; }
+        for (int j = 0; j < CPL; j += 4) {
+          const int cw = (kq * CPL + j) / 4;   // the 16-byte word of these 4 choices
+          float4 S;
+#pragma unroll
+          for (int v = 0; v < VPG; v++) {
+            const int rv = 32 * quarter + g0 + v;
+            const float4 u = *xw(0, rv, cw), w = *xw(1, rv, cw);
+            const float4 mv = make_float4(fminf(u.x, w.x), fminf(u.y, w.y), fminf(u.z, w.z), fminf(u.w, w.w));
+            S = v == 0 ? mv : make_float4(__fadd_rn(S.x, mv.x), __fadd_rn(S.y, mv.y), __fadd_rn(S.z, mv.z), __fadd_rn(S.w, mv.w));
+          }
+          const float Sv[4] = {S.x, S.y, S.z, S.w};
+#pragma unroll
+          for (int t = 0; t < 4; t++) {
+            const int c = kq * CPL + j + t;
+            const float D = __fmul_rn(alpha_of<F>(d, F == IQ1_S ? (c & 7) : c), Sv[t]);
+            if (a.table && sub == 0) a.table[(b * G + cg) * C + c] = __fadd_rn(Cgrp, D);
+            D2 = fminf(D2, fmaxf(D1, D));
+            if (D < D1) { D1 = D; c1 = c; }
+          }
         }
+#pragma unroll
+        for (int off = 1; off < VPG; off <<= 1) {
+          const float oD1 = __shfl_xor_sync(0xffffffffu, D1, off), oD2 = __shfl_xor_sync(0xffffffffu, D2, off);
+          const int oc = __shfl_xor_sync(0xffffffffu, c1, off);
+          D2 = fminf(fmaxf(D1, oD1), fminf(D2, oD2));
+          if (oD1 < D1 || (oD1 == D1 && oc < c1)) { D1 = oD1; c1 = oc; }
+        }
+        smin = fminf(reinterpret_cast<const float *>(xw(0, row, c1 / 4))[c1 & 3],
+                     reinterpret_cast<const float *>(xw(1, row, c1 / 4))[c1 & 3]);
         gflag = __fsub_rn(D2, D1) <= kMargin * (4.0f * Cgrp + D1 + D2);
       }
     } else if (active) {
