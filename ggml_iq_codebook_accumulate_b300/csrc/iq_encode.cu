@@ -1300,18 +1300,25 @@ __device__ __forceinline__ void write_back_bytes(const EncArgs &a, const float4 
 // CTA per item (used when the items are fewer than the resident warps): one CTA of 8 warps
 // re-decides one flagged item at a time.  Per flagged group, warp w takes the
 // group's vector w % VPG over entry slice w / VPG (8 / VPG slices of the codebook) for the fp32
-// minima, and the (near choice, vector, slice) units in turn for the exact minima; the partial
-// results meet in shared memory.  Every reduction (a minimum; the least exact error, lowest key on
-// equal errors) gives the same value in any order, so the result does not depend on the split.
+// minima, and the (near choice, vector, slice) units in turn for the fp32 screen of the exact
+// minima.  The screen lists its survivors in shared memory and the CTA evaluates the list in fp64
+// at once, one thread per candidate: fp64 issues at a small fraction of the fp32 rate on this
+// part, so the evaluations are packed into as few warp instructions as possible.  Every reduction
+// (a minimum; the least exact error, lowest key on equal errors) gives the same value in any
+// order, so the result does not depend on the split.
 constexpr int kRsWarps = 8;
+constexpr int kRsCap = kRsWarps * 32;  // listed candidates per group: one per thread
+constexpr unsigned long long kInfBits = 0x7ff0000000000000ull;  // +inf as a double's bits
 struct RescoreSmem {
   uint32_t pay[24];                  // the item's payload bytes
   float part[kRsWarps][16];          // (a) per-warp minima over its slice, per choice
   float mh[4][16];                   // (a) per-vector minima
-  double pex[16][4][4];              // (c) least exact error per (choice, vector, slice)
+  double pex[16][4][4];              // (c) long lists: least exact error per (choice, vector, slice)
   int pkey[16][4][4];                //     and its key
-  double ex[4][16];                  // (c) per (vector, choice)
-  int exkey[4][16];
+  unsigned long long exb[4][16];     // (c) least exact error per (vector, choice), as its bits
+  int exkey[4][16];                  //     and its key
+  uint32_t cand[kRsCap];             // (c) listed candidates: choice | vector << 4 | key << 8
+  int ncand;
 };
 
 template <int F, int MODE, typename TIn>
@@ -1405,7 +1412,10 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         float x = INFINITY;
         for (int j = 0; j < NSL; j++) x = fminf(x, sm.part[j * VPG + k][c]);
         sm.mh[k][c] = x;
+        sm.exb[k][c] = kInfBits;
+        sm.exkey[k][c] = 0x7fffffff;
       }
+      if (threadIdx.x == 0) sm.ncand = 0;
       __syncthreads();
       // (b) near set of choices (every thread alike)
       uint32_t near = 0;
@@ -1424,56 +1434,97 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         if (kFixedLike) near = 1u << cfix;
       }
       // (c) exact minimum per (near choice, vector) over the candidates the bound cannot exclude:
-      // units (near choice, vector, slice) dealt to the warps
+      // units (near choice, vector, slice) dealt to the warps screen in fp32.  LISTED: the
+      // survivors go to the shared list; otherwise (a list longer than its capacity: many
+      // candidates within the bound) each unit evaluates its own survivors in fp64.
       const int nunits = __popc(near) * VPG * NSL;
-      for (int unit = wid; unit < nunits; unit += kRsWarps) {
-        const int ci = unit / (VPG * NSL), k = (unit / NSL) % VPG, j = unit % NSL;
-        if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
-        uint32_t rest = near;
-        for (int q = 0; q < ci; q++) rest &= rest - 1u;
-        const int c = __ffs(rest) - 1;
-        int s, db0, db1;
-        cand_of_choice<F>(c, s, db0, db1);
-        const float al = alpha_of<F>(d, s);
-        const Vec u = shfl_vec(v, g * VPG + k);
-        const float emin = __fmul_rn(al, sm.mh[k][c]);
-        double bestE = INFINITY;
-        int bestK = 0x7fffffff;
+      auto run_units = [&](auto listed_t) {
+        constexpr bool LISTED = decltype(listed_t)::value;
+        for (int unit = wid; unit < nunits; unit += kRsWarps) {
+          const int ci = unit / (VPG * NSL), k = (unit / NSL) % VPG, j = unit % NSL;
+          if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
+          uint32_t rest = near;
+          for (int q = 0; q < ci; q++) rest &= rest - 1u;
+          const int c = __ffs(rest) - 1;
+          int s, db0, db1;
+          cand_of_choice<F>(c, s, db0, db1);
+          const float al = alpha_of<F>(d, s);
+          const Vec u = shfl_vec(v, g * VPG + k);
+          const float emin = __fmul_rn(al, sm.mh[k][c]);
+          double bestE = INFINITY;
+          int bestK = 0x7fffffff;
 #pragma unroll 4
-        for (int e = j * SL + lane; e < (j + 1) * SL; e += 32) {
-          Entry en;
-          load_entry<F>(a.grid, e, en);
-          for (int db = db0; db <= db1; db++) {
-            const float sc = cand_score<F>(u, en, al, db);
-            const float ec = __fmul_rn(al, sc);
-            if (__fsub_rn(ec, emin) <= kMargin * (4.0f * u.Cs + emin + ec)) {
-              const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
+          for (int e = j * SL + lane; e < (j + 1) * SL; e += 32) {  // the same trip count in every lane
+            Entry en;
+            load_entry<F>(a.grid, e, en);
+            for (int db = db0; db <= db1; db++) {
+              const float sc = cand_score<F>(u, en, al, db);
+              const float ec = __fmul_rn(al, sc);
+              const bool pass = __fsub_rn(ec, emin) <= kMargin * (4.0f * u.Cs + emin + ec);
               const int kk = (F == IQ1_M ? db * N : 0) + e;
-              if (E < bestE || (E == bestE && kk < bestK)) { bestE = E; bestK = kk; }
+              if constexpr (LISTED) {
+                const uint32_t pm = __ballot_sync(0xffffffffu, pass);
+                if (pm) {
+                  int base = 0;
+                  if (lane == 0) base = atomicAdd(&sm.ncand, __popc(pm));
+                  base = __shfl_sync(0xffffffffu, base, 0);
+                  const int slot = base + __popc(pm & ((1u << lane) - 1u));
+                  if (pass && slot < kRsCap) sm.cand[slot] = (uint32_t)c | ((uint32_t)k << 4) | ((uint32_t)kk << 8);
+                }
+              } else if (pass) {
+                const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
+                if (E < bestE || (E == bestE && kk < bestK)) { bestE = E; bestK = kk; }
+              }
             }
           }
-        }
+          if constexpr (!LISTED) {
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const double oE = __shfl_xor_sync(0xffffffffu, bestE, off);
-          const int oK = __shfl_xor_sync(0xffffffffu, bestK, off);
-          if (oE < bestE || (oE == bestE && oK < bestK)) { bestE = oE; bestK = oK; }
+            for (int off = 16; off >= 1; off >>= 1) {
+              const double oE = __shfl_xor_sync(0xffffffffu, bestE, off);
+              const int oK = __shfl_xor_sync(0xffffffffu, bestK, off);
+              if (oE < bestE || (oE == bestE && oK < bestK)) { bestE = oE; bestK = oK; }
+            }
+            if (lane == 0) { sm.pex[c][k][j] = bestE; sm.pkey[c][k][j] = bestK; }
+          }
         }
-        if (lane == 0) { sm.pex[c][k][j] = bestE; sm.pkey[c][k][j] = bestK; }
-      }
+      };
+      run_units(std::true_type{});
       __syncthreads();
-      for (int t = threadIdx.x; t < VPG * C; t += blockDim.x) {
-        const int k = t / C, c = t % C;
-        if (!((near >> c) & 1)) continue;
-        double E = sm.pex[c][k][0];
-        int K = sm.pkey[c][k][0];
-        for (int j = 1; j < NSL; j++) {
-          const double oE = sm.pex[c][k][j];
-          const int oK = sm.pkey[c][k][j];
-          if (oE < E || (oE == E && oK < K)) { E = oE; K = oK; }
+      const int ncand = sm.ncand;
+      if (ncand <= kRsCap) {
+        // one listed candidate per thread; the exact error E >= +0 (non-negative weights), so the
+        // least error is the least bit pattern, and the lowest key is taken among the equal ones
+        const int i = threadIdx.x;
+        const uint32_t cd = i < ncand ? sm.cand[i] : 0u;
+        const int c = cd & 15u, k = (cd >> 4) & 15u, kk = (int)(cd >> 8);
+        const Vec u = shfl_vec(v, g * VPG + k);
+        unsigned long long eb = 0;
+        if (i < ncand) {
+          int s, db0, db1;
+          cand_of_choice<F>(c, s, db0, db1);
+          Entry en;
+          load_entry<F>(a.grid, F == IQ1_M ? kk % N : kk, en);
+          eb = (unsigned long long)__double_as_longlong(exact_err<F>(u.x, u.w, en, d, s, u.sgn, F == IQ1_M ? kk / N : db0));
+          atomicMin(&sm.exb[k][c], eb);
         }
-        sm.ex[k][c] = E;
-        sm.exkey[k][c] = K;
+        __syncthreads();
+        if (i < ncand && eb == sm.exb[k][c]) atomicMin(&sm.exkey[k][c], kk);
+      } else {
+        run_units(std::false_type{});
+        __syncthreads();
+        for (int t = threadIdx.x; t < VPG * C; t += blockDim.x) {
+          const int k = t / C, c = t % C;
+          if (!((near >> c) & 1)) continue;
+          double E = sm.pex[c][k][0];
+          int K = sm.pkey[c][k][0];
+          for (int j = 1; j < NSL; j++) {
+            const double oE = sm.pex[c][k][j];
+            const int oK = sm.pkey[c][k][j];
+            if (oE < E || (oE == E && oK < K)) { E = oE; K = oK; }
+          }
+          sm.exb[k][c] = (unsigned long long)__double_as_longlong(E);
+          sm.exkey[k][c] = K;
+        }
       }
       __syncthreads();
       // (d) exact choice: least sum over the vectors, lowest choice on equal error; (e) rewrite the
@@ -1483,8 +1534,8 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         double bestG = INFINITY;
         for (int c = 0; c < C; c++) {
           if (!((near >> c) & 1)) continue;
-          double Eg = sm.ex[0][c];
-          for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, sm.ex[k][c]);
+          double Eg = __longlong_as_double((long long)sm.exb[0][c]);
+          for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, __longlong_as_double((long long)sm.exb[k][c]));
           if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
         }
         if (kFixedLike) cstar = cfix;
@@ -1688,7 +1739,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
 }
 
 template <int F, int MODE, typename TIn>
-__global__ void __launch_bounds__(kRsWarps * 32) rescore_kernel(EncArgs a, EncWs ws) {
+__global__ void __launch_bounds__(kRsWarps * 32, 2) rescore_kernel(EncArgs a, EncWs ws) {
   __shared__ RescoreSmem sm;
   __shared__ RescoreWarpSmem smw[kRsWarps];
   const int nflag = ws.hdr[1];  // the same for every CTA, so every CTA takes the same layout

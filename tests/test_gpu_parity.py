@@ -311,6 +311,31 @@ def test_zero_blocks_and_empty():
     assert e.shape == (0, 50)
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("mode", ["searched", "fixed"])
+def test_zero_importance_vectors_tie_exactly(fmt, mode):
+    # importance 0 over whole 8-column vectors (one vector, a whole choice group, scattered
+    # columns): every codebook entry then has error exactly 0 for such a vector, so the exact
+    # rescoring sees more candidates within its bound than it lists at once and takes its
+    # per-unit path; the lowest key (and, for a tied group, the lowest choice) must win as in the
+    # oracle, bit for bit
+    info = oracle.format_info(fmt)
+    store, wv = synth.as_dtype(synth.weight_t4(6, 1024, seed=21), "bf16")
+    imp = importance_from_acts(1024, seed=22).copy()
+    imp[0:8] = 0; imp[256:288] = 0; imp[520:528] = 0; imp[768:1024:3] = 0
+    grid = synth.grid(fmt)
+    ch = None
+    if mode == "fixed":
+        rng = np.random.default_rng(23)
+        ch = rng.integers(0, info["num_choices"], (6 * 4, info["groups"])).astype(np.uint8)
+    p_orc, st_orc = oracle.encode(fmt, wv, grid, importance=imp, choices=ch)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    p = api.encode(fmt, dev_tensor(store, "bf16"), torch.from_numpy(grid).to(DEV), importance=torch.from_numpy(imp).to(DEV),
+                   choices=None if ch is None else torch.from_numpy(ch).to(DEV), status=st)
+    assert int(st.item()) == st_orc == 0
+    assert np.array_equal(host(p), p_orc)
+
+
 def test_argument_errors_change_nothing():
     with pytest.raises(api.IQError):
         api.encode("IQ2_XXS", torch.zeros(2, 300, device=DEV), torch.from_numpy(synth.grid("IQ2_XXS")).to(DEV))
