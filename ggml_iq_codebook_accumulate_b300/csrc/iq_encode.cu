@@ -1297,16 +1297,29 @@ __device__ __forceinline__ void write_back_bytes(const EncArgs &a, const float4 
 
 // Exact rescoring of the flagged items, in one of two layouts chosen by their number.
 //
-// CTA per item (used when the items are fewer than the resident warps): one CTA of 8 warps
-// re-decides one flagged item at a time.  Per flagged group, warp w takes the
-// group's vector w % VPG over entry slice w / VPG (8 / VPG slices of the codebook) for the fp32
+// The choice a block's payload holds for group g (IQ1_S: scale index + delta bit << 3).
+template <int F>
+__device__ __forceinline__ int payload_choice(const uint8_t *pb, int g) {
+  const int c = (int)get_bits(pb, f_scale<F>(g));
+  return F == IQ1_S ? c | (int)get_bits(pb, f_dbit_grp<F>(g)) << 3 : c;
+}
+
+// A group of which only some vectors are flagged had no near tie between choices, since the sweep
+// flags every vector of a group whose choice is near-tied: its choice, which the payload holds, is
+// exact, and only its flagged vectors are re-decided under that choice, as with fixed choices.
+
+// CTA per item (used when the items are fewer than the resident warps): one CTA of 4 warps
+// re-decides one flagged item at a time, and 4 CTAs share an SM, so that the latency-bound items
+// overlap.  Per flagged group, warp w takes the
+// group's vector w % VPG over entry slice w / VPG (4 / VPG slices of the codebook) for the fp32
 // minima, and the (near choice, vector, slice) units in turn for the fp32 screen of the exact
 // minima.  The screen lists its survivors in shared memory and the CTA evaluates the list in fp64
 // at once, one thread per candidate: fp64 issues at a small fraction of the fp32 rate on this
 // part, so the evaluations are packed into as few warp instructions as possible.  Every reduction
 // (a minimum; the least exact error, lowest key on equal errors) gives the same value in any
 // order, so the result does not depend on the split.
-constexpr int kRsWarps = 8;
+constexpr int kRsWarps = 4;
+constexpr int kRsCtasPerSm = 4;  // 128 registers a thread
 constexpr int kRsCap = kRsWarps * 32;  // listed candidates per group: one per thread
 constexpr unsigned long long kInfBits = 0x7ff0000000000000ull;  // +inf as a double's bits
 struct RescoreSmem {
@@ -1356,7 +1369,9 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
     for (int g = 0; g < G; g++) {
       const uint32_t gm = ((1u << VPG) - 1u) << (g * VPG);
       if (!(mask & gm)) continue;
-      const int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : MODE == MODE_EVERY ? cpass : -1;
+      const bool fx = kFixedLike || (mask & gm) != gm;  // the group's choice is known
+      const int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : MODE == MODE_EVERY ? cpass
+                       : fx ? payload_choice<F>(pbytes, g) : -1;
       float Cg = 0.0f;  // the group's sum of w t^2, in vector order (every thread alike)
       for (int k = 0; k < VPG; k++) {
         const float cs = __shfl_sync(0xffffffffu, v.Cs, g * VPG + k);
@@ -1366,7 +1381,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
       // sweep computes them
       // (with the group's choice fixed only the flagged vectors are re-decided: the entries of the
       // others are independent decisions the sweep already made exactly)
-      const bool kvflag = !kFixedLike || ((mask >> (g * VPG + kv)) & 1u);
+      const bool kvflag = !fx || ((mask >> (g * VPG + kv)) & 1u);
       {
         const Vec u = shfl_vec(v, g * VPG + kv);
         float lm[C], alc[C];
@@ -1387,7 +1402,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
           else ab1(u, en, Anp, Bp, Anm, Bm);
 #pragma unroll
           for (int c = 0; c < C; c++) {
-            if (kFixedLike && c != cfix) continue;
+            if (fx && c != cfix) continue;
             int s, db0, db1;
             cand_of_choice<F>(c, s, db0, db1);
             if (!Fmt<F>::IQ1) {
@@ -1423,7 +1438,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         float D[C];
         float D1 = INFINITY;
         for (int c = 0; c < C; c++) {
-          if (kFixedLike && c != cfix) { D[c] = INFINITY; continue; }
+          if (fx && c != cfix) { D[c] = INFINITY; continue; }
           float S = sm.mh[0][c];
           for (int k = 1; k < VPG; k++) S = __fadd_rn(S, sm.mh[k][c]);
           D[c] = __fmul_rn(alpha_choice<F>(d, c), S);
@@ -1431,7 +1446,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         }
         for (int c = 0; c < C; c++)
           if (D[c] != INFINITY && __fsub_rn(D[c], D1) <= kMargin * (4.0f * Cg + D1 + D[c])) near |= 1u << c;
-        if (kFixedLike) near = 1u << cfix;
+        if (fx) near = 1u << cfix;
       }
       // (c) exact minimum per (near choice, vector) over the candidates the bound cannot exclude:
       // units (near choice, vector, slice) dealt to the warps screen in fp32.  LISTED: the
@@ -1442,7 +1457,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         constexpr bool LISTED = decltype(listed_t)::value;
         for (int unit = wid; unit < nunits; unit += kRsWarps) {
           const int ci = unit / (VPG * NSL), k = (unit / NSL) % VPG, j = unit % NSL;
-          if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
+          if (fx && !((mask >> (g * VPG + k)) & 1u)) continue;
           uint32_t rest = near;
           for (int q = 0; q < ci; q++) rest &= rest - 1u;
           const int c = __ffs(rest) - 1;
@@ -1538,13 +1553,13 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
           for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, __longlong_as_double((long long)sm.exb[k][c]));
           if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
         }
-        if (kFixedLike) cstar = cfix;
+        if (fx) cstar = cfix;
         if (cstar >= 0) {
           set_bits_bytes(pbytes, f_scale<F>(g), (uint32_t)(F == IQ1_S ? (cstar & 7) : cstar));
           if (F == IQ1_S) set_bits_bytes(pbytes, f_dbit_grp<F>(g), (uint32_t)(cstar >> 3));
           for (int k = 0; k < VPG; k++) {
             const int vv = g * VPG + k;
-            if (kFixedLike && !((mask >> vv) & 1u)) continue;
+            if (fx && !((mask >> vv) & 1u)) continue;
             const int key = sm.exkey[k][cstar];
             const int idx = F == IQ1_M ? key % N : key;
             const Bits lo = f_idx_lo<F>(vv);
@@ -1579,7 +1594,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
   // an item is (block, flagged vectors); every-choice payloads: (block | choice << 27, flagged
   // vectors), re-decided as a fixed-choice block in that choice's payload
   constexpr bool kFixedLike = MODE == MODE_FIXED || MODE == MODE_EVERY;
-  for (int it = blockIdx.x * 8 + wid; it < nflag; it += gridDim.x * 8) {
+  for (int it = blockIdx.x * kRsWarps + wid; it < nflag; it += gridDim.x * kRsWarps) {
    const uint2 item = ws.fb[it];
    {
     const int cpass = MODE == MODE_EVERY ? (int)(item.x >> 27) : 0;
@@ -1605,14 +1620,16 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       const uint32_t gm = ((1u << VPG) - 1u) << (g * VPG);
       if (!(mask & gm)) continue;
       float Cg = 0.0f;
-      // (a) fp32 per-vector minima for every choice (or the fixed one), as the sweep computes them.
-      // With the group's choice fixed, the vectors' entries are independent decisions: only the
+      // (a) fp32 per-vector minima for every choice (or the known one), as the sweep computes them.
+      // With the group's choice known, the vectors' entries are independent decisions: only the
       // flagged vectors are re-decided, the others keep the sweep's exact pick.
-      int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : MODE == MODE_EVERY ? cpass : -1;
+      const bool fx = kFixedLike || (mask & gm) != gm;
+      const int cfix = MODE == MODE_FIXED ? fixed_choice<G>(a, b, g) : MODE == MODE_EVERY ? cpass
+                       : fx ? payload_choice<F>(pbytes, g) : -1;
       for (int k = 0; k < VPG; k++) {
         const Vec u = shfl_vec(v, g * VPG + k);
         Cg = k == 0 ? u.Cs : __fadd_rn(Cg, u.Cs);
-        if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
+        if (fx && !((mask >> (g * VPG + k)) & 1u)) continue;
         float lm[C], alc[C];
 #pragma unroll
         for (int c = 0; c < C; c++) {
@@ -1631,7 +1648,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
           else ab1(u, en, Anp, Bp, Anm, Bm);
 #pragma unroll
           for (int c = 0; c < C; c++) {
-            if (kFixedLike && c != cfix) continue;
+            if (fx && c != cfix) continue;
             int s, db0, db1;
             cand_of_choice<F>(c, s, db0, db1);
             if (!Fmt<F>::IQ1) {
@@ -1657,7 +1674,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       float D[C];
       float D1 = INFINITY;
       for (int c = 0; c < C; c++) {
-        if (kFixedLike && c != cfix) { D[c] = INFINITY; continue; }
+        if (fx && c != cfix) { D[c] = INFINITY; continue; }
         float S = sm.mh[0][c];
         for (int k = 1; k < VPG; k++) S = __fadd_rn(S, sm.mh[k][c]);
         D[c] = __fmul_rn(alpha_choice<F>(d, c), S);
@@ -1666,7 +1683,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       uint32_t near = 0;
       for (int c = 0; c < C; c++)
         if (D[c] != INFINITY && __fsub_rn(D[c], D1) <= kMargin * (4.0f * Cg + D1 + D[c])) near |= 1u << c;
-      if (kFixedLike) near = 1u << cfix;
+      if (fx) near = 1u << cfix;
       // (c) exact minimum per (vector, near choice) over the candidates the bound cannot exclude
       for (int c = 0; c < C; c++) {
         if (!((near >> c) & 1)) continue;
@@ -1674,7 +1691,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
         cand_of_choice<F>(c, s, db0, db1);
         const float al = alpha_of<F>(d, s);
         for (int k = 0; k < VPG; k++) {
-          if (kFixedLike && !((mask >> (g * VPG + k)) & 1u)) continue;
+          if (fx && !((mask >> (g * VPG + k)) & 1u)) continue;
           const Vec u = shfl_vec(v, g * VPG + k);
           const float mh = sm.mh[k][c];
           const float emin = __fmul_rn(al, mh);
@@ -1713,14 +1730,14 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
         for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, sm.ex[k][c]);
         if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
       }
-      if (kFixedLike) cstar = cfix;
+      if (fx) cstar = cfix;
       // (e) rewrite the group's fields (keep the sweep's decision if nothing was comparable)
       if (lane == 0 && cstar >= 0) {
         set_bits_bytes(pbytes, f_scale<F>(g), (uint32_t)(F == IQ1_S ? (cstar & 7) : cstar));
         if (F == IQ1_S) set_bits_bytes(pbytes, f_dbit_grp<F>(g), (uint32_t)(cstar >> 3));
         for (int k = 0; k < VPG; k++) {
           const int vv = g * VPG + k;
-          if (kFixedLike && !((mask >> vv) & 1u)) continue;
+          if (fx && !((mask >> vv) & 1u)) continue;
           const int key = sm.exkey[k][cstar];
           const int idx = F == IQ1_M ? key % N : key;
           const Bits lo = f_idx_lo<F>(vv);
@@ -1739,7 +1756,7 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
 }
 
 template <int F, int MODE, typename TIn>
-__global__ void __launch_bounds__(kRsWarps * 32, 2) rescore_kernel(EncArgs a, EncWs ws) {
+__global__ void __launch_bounds__(kRsWarps * 32, kRsCtasPerSm) rescore_kernel(EncArgs a, EncWs ws) {
   __shared__ RescoreSmem sm;
   __shared__ RescoreWarpSmem smw[kRsWarps];
   const int nflag = ws.hdr[1];  // the same for every CTA, so every CTA takes the same layout
