@@ -1577,10 +1577,13 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
   }
 }
 
+constexpr int kRsWarpCap = 64;  // listed candidates per group, warp per item
 struct RescoreWarpSmem {
   float mh[4][16];
-  double ex[4][16];
-  int exkey[4][16];
+  unsigned long long exb[4][16];     // least exact error per (vector, choice), as its bits
+  int exkey[4][16];                  // and its key
+  uint32_t cand[kRsWarpCap];         // listed candidates: choice | vector << 4 | key << 8
+  unsigned long long ceb[kRsWarpCap];  // their exact errors' bits
   uint32_t pay[24];
 };
 
@@ -1684,41 +1687,86 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       for (int c = 0; c < C; c++)
         if (D[c] != INFINITY && __fsub_rn(D[c], D1) <= kMargin * (4.0f * Cg + D1 + D[c])) near |= 1u << c;
       if (fx) near = 1u << cfix;
-      // (c) exact minimum per (vector, near choice) over the candidates the bound cannot exclude
-      for (int c = 0; c < C; c++) {
-        if (!((near >> c) & 1)) continue;
-        int s, db0, db1;
-        cand_of_choice<F>(c, s, db0, db1);
-        const float al = alpha_of<F>(d, s);
-        for (int k = 0; k < VPG; k++) {
-          if (fx && !((mask >> (g * VPG + k)) & 1u)) continue;
-          const Vec u = shfl_vec(v, g * VPG + k);
-          const float mh = sm.mh[k][c];
-          const float emin = __fmul_rn(al, mh);
-          double bestE = INFINITY;
-          int bestK = 0x7fffffff;
-  #pragma unroll 4
-        for (int e = lane; e < N; e += 32) {
-            Entry en;
-            load_entry<F>(a.grid, e, en);
-            for (int db = db0; db <= db1; db++) {
-              const float sc = cand_score<F>(u, en, al, db);
-              const float ec = __fmul_rn(al, sc);
-              if (__fsub_rn(ec, emin) <= kMargin * (4.0f * u.Cs + emin + ec)) {
-                const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
+      // (c) exact minimum per (vector, near choice) over the candidates the bound cannot exclude:
+      // the fp32 screen lists its survivors and the warp evaluates the list in fp64 together, one
+      // lane per candidate; the least error is the least bit pattern (E >= +0), the lowest key is
+      // taken among the equal ones.  A list longer than its capacity: each (vector, choice) in turn.
+      for (int t = lane; t < VPG * C; t += 32) { sm.exb[t / C][t % C] = kInfBits; sm.exkey[t / C][t % C] = 0x7fffffff; }
+      __syncwarp();
+      auto run_pairs = [&](auto listed_t) -> int {
+        constexpr bool LISTED = decltype(listed_t)::value;
+        int ncand = 0;
+        for (int c = 0; c < C; c++) {
+          if (!((near >> c) & 1)) continue;
+          int s, db0, db1;
+          cand_of_choice<F>(c, s, db0, db1);
+          const float al = alpha_of<F>(d, s);
+          for (int k = 0; k < VPG; k++) {
+            if (fx && !((mask >> (g * VPG + k)) & 1u)) continue;
+            const Vec u = shfl_vec(v, g * VPG + k);
+            const float emin = __fmul_rn(al, sm.mh[k][c]);
+            double bestE = INFINITY;
+            int bestK = 0x7fffffff;
+#pragma unroll 4
+            for (int e = lane; e < N; e += 32) {  // the same trip count in every lane
+              Entry en;
+              load_entry<F>(a.grid, e, en);
+              for (int db = db0; db <= db1; db++) {
+                const float sc = cand_score<F>(u, en, al, db);
+                const float ec = __fmul_rn(al, sc);
+                const bool pass = __fsub_rn(ec, emin) <= kMargin * (4.0f * u.Cs + emin + ec);
                 const int kk = (F == IQ1_M ? db * N : 0) + e;
-                if (E < bestE || (E == bestE && kk < bestK)) { bestE = E; bestK = kk; }
+                if constexpr (LISTED) {
+                  const uint32_t pm = __ballot_sync(0xffffffffu, pass);
+                  const int slot = ncand + __popc(pm & ((1u << lane) - 1u));
+                  if (pass && slot < kRsWarpCap) sm.cand[slot] = (uint32_t)c | ((uint32_t)k << 4) | ((uint32_t)kk << 8);
+                  ncand += __popc(pm);
+                } else if (pass) {
+                  const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
+                  if (E < bestE || (E == bestE && kk < bestK)) { bestE = E; bestK = kk; }
+                }
               }
             }
-          }
+            if constexpr (!LISTED) {
 #pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            const double oE = __shfl_xor_sync(0xffffffffu, bestE, off);
-            const int oK = __shfl_xor_sync(0xffffffffu, bestK, off);
-            if (oE < bestE || (oE == bestE && oK < bestK)) { bestE = oE; bestK = oK; }
+              for (int off = 16; off >= 1; off >>= 1) {
+                const double oE = __shfl_xor_sync(0xffffffffu, bestE, off);
+                const int oK = __shfl_xor_sync(0xffffffffu, bestK, off);
+                if (oE < bestE || (oE == bestE && oK < bestK)) { bestE = oE; bestK = oK; }
+              }
+              if (lane == 0) { sm.exb[k][c] = (unsigned long long)__double_as_longlong(bestE); sm.exkey[k][c] = bestK; }
+            }
           }
-          if (lane == 0) { sm.ex[k][c] = bestE; sm.exkey[k][c] = bestK; }
         }
+        return ncand;
+      };
+      const int ncand = run_pairs(std::true_type{});
+      __syncwarp();
+      if (ncand <= kRsWarpCap) {
+        for (int i0 = 0; i0 < ncand; i0 += 32) {  // the same trip count in every lane
+          const int i = i0 + lane;
+          const uint32_t cd = i < ncand ? sm.cand[i] : 0u;
+          const int c = cd & 15u, k = (cd >> 4) & 15u, kk = (int)(cd >> 8);
+          const Vec u = shfl_vec(v, g * VPG + k);
+          if (i < ncand) {
+            int s, db0, db1;
+            cand_of_choice<F>(c, s, db0, db1);
+            Entry en;
+            load_entry<F>(a.grid, F == IQ1_M ? kk % N : kk, en);
+            const unsigned long long eb =
+                (unsigned long long)__double_as_longlong(exact_err<F>(u.x, u.w, en, d, s, u.sgn, F == IQ1_M ? kk / N : db0));
+            sm.ceb[i] = eb;
+            atomicMin(&sm.exb[k][c], eb);
+          }
+        }
+        __syncwarp();
+        for (int i = lane; i < ncand; i += 32) {
+          const uint32_t cd = sm.cand[i];
+          const int c = cd & 15u, k = (cd >> 4) & 15u;
+          if (sm.ceb[i] == sm.exb[k][c]) atomicMin(&sm.exkey[k][c], (int)(cd >> 8));
+        }
+      } else {
+        run_pairs(std::false_type{});
       }
       __syncwarp();
       // (d) exact choice: least sum over the vectors, lowest choice on equal error
@@ -1726,8 +1774,8 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       double bestG = INFINITY;
       for (int c = 0; c < C; c++) {
         if (!((near >> c) & 1)) continue;
-        double Eg = sm.ex[0][c];
-        for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, sm.ex[k][c]);
+        double Eg = __longlong_as_double((long long)sm.exb[0][c]);
+        for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, __longlong_as_double((long long)sm.exb[k][c]));
         if (cstar < 0 || Eg < bestG) { bestG = Eg; cstar = c; }
       }
       if (fx) cstar = cfix;

@@ -336,6 +336,23 @@ def test_zero_importance_vectors_tie_exactly(fmt, mode):
     assert np.array_equal(host(p), p_orc)
 
 
+@pytest.mark.parametrize("fmt", FORMATS)
+def test_zero_importance_vectors_many_flagged_blocks(fmt):
+    # every row's first vector has importance 0, so all 3072 rows' first blocks are flagged: more
+    # items than resident warps, so each warp re-decides its own items; the tied vectors overflow
+    # its candidate list, the other flagged groups fit it
+    store, wv = synth.as_dtype(synth.weight_t4(3072, 512, seed=24), "bf16")
+    imp = (np.abs(np.random.default_rng(25).standard_normal(512)) + 0.1).astype(np.float32)
+    imp[0:8] = 0; imp[300:304] = 0
+    grid = synth.grid(fmt)
+    p_orc, st_orc = oracle.encode(fmt, wv, grid, importance=imp)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    p = api.encode(fmt, dev_tensor(store, "bf16"), torch.from_numpy(grid).to(DEV), importance=torch.from_numpy(imp).to(DEV),
+                   status=st)
+    assert int(st.item()) == st_orc == 0
+    assert np.array_equal(host(p), p_orc)
+
+
 def test_argument_errors_change_nothing():
     with pytest.raises(api.IQError):
         api.encode("IQ2_XXS", torch.zeros(2, 300, device=DEV), torch.from_numpy(synth.grid("IQ2_XXS")).to(DEV))
