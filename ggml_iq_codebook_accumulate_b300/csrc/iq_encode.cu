@@ -1331,6 +1331,7 @@ struct RescoreSmem {
   unsigned long long exb[4][16];     // (c) least exact error per (vector, choice), as its bits
   int exkey[4][16];                  //     and its key
   uint32_t cand[kRsCap];             // (c) listed candidates: choice | vector << 4 | key << 8
+  float4 candg[kRsCap][2];           //     and their codebook values
   int ncand;
 };
 
@@ -1484,7 +1485,11 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
                   if (lane == 0) base = atomicAdd(&sm.ncand, __popc(pm));
                   base = __shfl_sync(0xffffffffu, base, 0);
                   const int slot = base + __popc(pm & ((1u << lane) - 1u));
-                  if (pass && slot < kRsCap) sm.cand[slot] = (uint32_t)c | ((uint32_t)k << 4) | ((uint32_t)kk << 8);
+                  if (pass && slot < kRsCap) {
+                    sm.cand[slot] = (uint32_t)c | ((uint32_t)k << 4) | ((uint32_t)kk << 8);
+                    sm.candg[slot][0] = make_float4(en.g[0], en.g[1], en.g[2], en.g[3]);
+                    sm.candg[slot][1] = make_float4(en.g[4], en.g[5], en.g[6], en.g[7]);
+                  }
                 }
               } else if (pass) {
                 const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
@@ -1517,8 +1522,10 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         if (i < ncand) {
           int s, db0, db1;
           cand_of_choice<F>(c, s, db0, db1);
-          Entry en;
-          load_entry<F>(a.grid, F == IQ1_M ? kk % N : kk, en);
+          Entry en;  // the codebook values the screen kept (the direct form reads only g)
+          const float4 g0 = sm.candg[i][0], g1 = sm.candg[i][1];
+          en.g[0] = g0.x; en.g[1] = g0.y; en.g[2] = g0.z; en.g[3] = g0.w;
+          en.g[4] = g1.x; en.g[5] = g1.y; en.g[6] = g1.z; en.g[7] = g1.w;
           eb = (unsigned long long)__double_as_longlong(exact_err<F>(u.x, u.w, en, d, s, u.sgn, F == IQ1_M ? kk / N : db0));
           atomicMin(&sm.exb[k][c], eb);
         }
@@ -1545,9 +1552,10 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
       // (d) exact choice: least sum over the vectors, lowest choice on equal error; (e) rewrite the
       // group's fields (keep the sweep's decision if nothing was comparable)
       if (threadIdx.x == 0) {
-        int cstar = -1;
+        const bool one = __popc(near) == 1;  // a single near choice needs no sums
+        int cstar = one ? __ffs(near) - 1 : -1;
         double bestG = INFINITY;
-        for (int c = 0; c < C; c++) {
+        for (int c = 0; !one && c < C; c++) {
           if (!((near >> c) & 1)) continue;
           double Eg = __longlong_as_double((long long)sm.exb[0][c]);
           for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, __longlong_as_double((long long)sm.exb[k][c]));
@@ -1583,6 +1591,7 @@ struct RescoreWarpSmem {
   unsigned long long exb[4][16];     // least exact error per (vector, choice), as its bits
   int exkey[4][16];                  // and its key
   uint32_t cand[kRsWarpCap];         // listed candidates: choice | vector << 4 | key << 8
+  float4 candg[kRsWarpCap][2];       // and their codebook values
   unsigned long long ceb[kRsWarpCap];  // their exact errors' bits
   uint32_t pay[24];
 };
@@ -1719,7 +1728,11 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
                 if constexpr (LISTED) {
                   const uint32_t pm = __ballot_sync(0xffffffffu, pass);
                   const int slot = ncand + __popc(pm & ((1u << lane) - 1u));
-                  if (pass && slot < kRsWarpCap) sm.cand[slot] = (uint32_t)c | ((uint32_t)k << 4) | ((uint32_t)kk << 8);
+                  if (pass && slot < kRsWarpCap) {
+                    sm.cand[slot] = (uint32_t)c | ((uint32_t)k << 4) | ((uint32_t)kk << 8);
+                    sm.candg[slot][0] = make_float4(en.g[0], en.g[1], en.g[2], en.g[3]);
+                    sm.candg[slot][1] = make_float4(en.g[4], en.g[5], en.g[6], en.g[7]);
+                  }
                   ncand += __popc(pm);
                 } else if (pass) {
                   const double E = exact_err<F>(u.x, u.w, en, d, s, u.sgn, db);
@@ -1751,8 +1764,10 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
           if (i < ncand) {
             int s, db0, db1;
             cand_of_choice<F>(c, s, db0, db1);
-            Entry en;
-            load_entry<F>(a.grid, F == IQ1_M ? kk % N : kk, en);
+            Entry en;  // the codebook values the screen kept (the direct form reads only g)
+            const float4 g0 = sm.candg[i][0], g1 = sm.candg[i][1];
+            en.g[0] = g0.x; en.g[1] = g0.y; en.g[2] = g0.z; en.g[3] = g0.w;
+            en.g[4] = g1.x; en.g[5] = g1.y; en.g[6] = g1.z; en.g[7] = g1.w;
             const unsigned long long eb =
                 (unsigned long long)__double_as_longlong(exact_err<F>(u.x, u.w, en, d, s, u.sgn, F == IQ1_M ? kk / N : db0));
             sm.ceb[i] = eb;
@@ -1770,9 +1785,10 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
       }
       __syncwarp();
       // (d) exact choice: least sum over the vectors, lowest choice on equal error
-      int cstar = -1;
+      const bool one = __popc(near) == 1;  // a single near choice needs no sums
+      int cstar = one ? __ffs(near) - 1 : -1;
       double bestG = INFINITY;
-      for (int c = 0; c < C; c++) {
+      for (int c = 0; !one && c < C; c++) {
         if (!((near >> c) & 1)) continue;
         double Eg = __longlong_as_double((long long)sm.exb[0][c]);
         for (int k = 1; k < VPG; k++) Eg = __dadd_rn(Eg, __longlong_as_double((long long)sm.exb[k][c]));
