@@ -1310,9 +1310,9 @@ __device__ __forceinline__ int payload_choice(const uint8_t *pb, int g) {
 
 // CTA per item (used when the items are fewer than the resident warps): one CTA of 4 warps
 // re-decides one flagged item at a time, and 4 CTAs share an SM, so that the latency-bound items
-// overlap.  Per flagged group, warp w takes the
-// group's vector w % VPG over entry slice w / VPG (4 / VPG slices of the codebook) for the fp32
-// minima, and the (near choice, vector, slice) units in turn for the fp32 screen of the exact
+// overlap.  Per flagged group, the n vectors it re-decides (all, or with its choice known only the
+// flagged ones) share the warps, each over 4 / n slices of the codebook, for the fp32 minima; the
+// (near choice, vector, slice) units go to the warps in turn for the fp32 screen of the exact
 // minima.  The screen lists its survivors in shared memory and the CTA evaluates the list in fp64
 // at once, one thread per candidate: fp64 issues at a small fraction of the fp32 rate on this
 // part, so the evaluations are packed into as few warp instructions as possible.  Every reduction
@@ -1338,11 +1338,8 @@ struct RescoreSmem {
 template <int F, int MODE, typename TIn>
 __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws, int nflag, RescoreSmem &sm) {
   constexpr int C = Fmt<F>::C, N = Fmt<F>::N, VPG = Fmt<F>::VPG, BB = Fmt<F>::BB, G = Fmt<F>::G;
-  constexpr int NSL = kRsWarps / VPG;  // entry slices per vector
-  constexpr int SL = N / NSL;          // entries per slice
-  static_assert(kRsWarps % VPG == 0 && SL % 32 == 0 && NSL <= 4 && VPG <= 4, "slices of whole warps");
+  static_assert(kRsWarps == 4 && VPG <= 4 && (N / kRsWarps) % 32 == 0, "slices of whole warps");
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int kv = wid % VPG, js = wid / VPG;  // this warp's vector in the group and slice in (a)
   const float4 *tab = ws.tab;
   // an item is (block, flagged vectors); every-choice payloads: (block | choice << 27, flagged
   // vectors), re-decided as a fixed-choice block in that choice's payload
@@ -1378,11 +1375,20 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         const float cs = __shfl_sync(0xffffffffu, v.Cs, g * VPG + k);
         Cg = k == 0 ? cs : __fadd_rn(Cg, cs);
       }
-      // (a) fp32 minima of vector kv over slice js for every choice (or the fixed one), as the
+      // the vectors re-decided (with the group's choice known only the flagged ones: the entries of
+      // the others are independent decisions the sweep already made exactly), each over nsl slices
+      // of sl entries
+      const uint32_t act = fx ? (mask >> (g * VPG)) & ((1u << VPG) - 1u) : (1u << VPG) - 1u;
+      const int nact = __popc(act), nsl = kRsWarps / nact, sl = N / nsl;
+      auto act_vec = [&](int r) {  // the r-th re-decided vector of the group
+        uint32_t rest = act;
+        for (int q = 0; q < r; q++) rest &= rest - 1u;
+        return __ffs(rest) - 1;
+      };
+      // (a) fp32 minima of vector kv over slice js for every choice (or the known one), as the
       // sweep computes them
-      // (with the group's choice fixed only the flagged vectors are re-decided: the entries of the
-      // others are independent decisions the sweep already made exactly)
-      const bool kvflag = !fx || ((mask >> (g * VPG + kv)) & 1u);
+      const bool kvflag = wid < nact * nsl;
+      const int kv = kvflag ? act_vec(wid / nsl) : 0, js = wid % nsl;
       {
         const Vec u = shfl_vec(v, g * VPG + kv);
         float lm[C], alc[C];
@@ -1394,7 +1400,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
           alc[c] = alpha_of<F>(d, s);
         }
 #pragma unroll 4
-        for (int e = js * SL + lane; kvflag && e < (js + 1) * SL; e += 32) {
+        for (int e = js * sl + lane; kvflag && e < (js + 1) * sl; e += 32) {
           Entry en;
           load_entry<F>(a.grid, e, en);
           // the entry's sums once, then every choice's score as cand_score forms it
@@ -1426,7 +1432,10 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
       for (int t = threadIdx.x; t < VPG * C; t += blockDim.x) {
         const int k = t / C, c = t % C;
         float x = INFINITY;
-        for (int j = 0; j < NSL; j++) x = fminf(x, sm.part[j * VPG + k][c]);
+        if ((act >> k) & 1u) {
+          const int r = __popc(act & ((1u << k) - 1u));
+          for (int j = 0; j < nsl; j++) x = fminf(x, sm.part[r * nsl + j][c]);
+        }
         sm.mh[k][c] = x;
         sm.exb[k][c] = kInfBits;
         sm.exkey[k][c] = 0x7fffffff;
@@ -1453,12 +1462,11 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
       // units (near choice, vector, slice) dealt to the warps screen in fp32.  LISTED: the
       // survivors go to the shared list; otherwise (a list longer than its capacity: many
       // candidates within the bound) each unit evaluates its own survivors in fp64.
-      const int nunits = __popc(near) * VPG * NSL;
+      const int nunits = __popc(near) * nact * nsl;
       auto run_units = [&](auto listed_t) {
         constexpr bool LISTED = decltype(listed_t)::value;
         for (int unit = wid; unit < nunits; unit += kRsWarps) {
-          const int ci = unit / (VPG * NSL), k = (unit / NSL) % VPG, j = unit % NSL;
-          if (fx && !((mask >> (g * VPG + k)) & 1u)) continue;
+          const int ci = unit / (nact * nsl), k = act_vec((unit / nsl) % nact), j = unit % nsl;
           uint32_t rest = near;
           for (int q = 0; q < ci; q++) rest &= rest - 1u;
           const int c = __ffs(rest) - 1;
@@ -1470,7 +1478,7 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
           double bestE = INFINITY;
           int bestK = 0x7fffffff;
 #pragma unroll 4
-          for (int e = j * SL + lane; e < (j + 1) * SL; e += 32) {  // the same trip count in every lane
+          for (int e = j * sl + lane; e < (j + 1) * sl; e += 32) {  // the same trip count in every lane
             Entry en;
             load_entry<F>(a.grid, e, en);
             for (int db = db0; db <= db1; db++) {
@@ -1536,10 +1544,10 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
         __syncthreads();
         for (int t = threadIdx.x; t < VPG * C; t += blockDim.x) {
           const int k = t / C, c = t % C;
-          if (!((near >> c) & 1)) continue;
+          if (!((near >> c) & 1) || !((act >> k) & 1u)) continue;
           double E = sm.pex[c][k][0];
           int K = sm.pkey[c][k][0];
-          for (int j = 1; j < NSL; j++) {
+          for (int j = 1; j < nsl; j++) {
             const double oE = sm.pex[c][k][j];
             const int oK = sm.pkey[c][k][j];
             if (oE < E || (oE == E && oK < K)) { E = oE; K = oK; }
