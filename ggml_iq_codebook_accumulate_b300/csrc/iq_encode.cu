@@ -39,7 +39,7 @@ enum { MODE_SEARCH = 0, MODE_FIXED = 1, MODE_TABLE = 2, MODE_EVERY = 3 };
 __host__ __device__ inline size_t al256(size_t n) { return (n + 255) & ~(size_t)255; }
 
 struct EncWs {
-  int32_t *hdr;  // [0] codebook invalid, [1] number of flagged blocks
+  int32_t *hdr;  // [0] codebook invalid, [1] number of flagged blocks, [2] rescoring's next item
   float4 *tab;   // [N][4] prepared codebook
   uint2 *fb;     // [B] flagged blocks: (block index, vector mask)
 };
@@ -1333,6 +1333,7 @@ struct RescoreSmem {
   uint32_t cand[kRsCap];             // (c) listed candidates: choice | vector << 4 | key << 8
   float4 candg[kRsCap][2];           //     and their codebook values
   int ncand;
+  int nextit;                        // the CTA's next item
 };
 
 template <int F, int MODE, typename TIn>
@@ -1345,7 +1346,9 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
   // vectors), re-decided as a fixed-choice block in that choice's payload
   constexpr bool kFixedLike = MODE == MODE_FIXED || MODE == MODE_EVERY;
   uint8_t *pbytes = reinterpret_cast<uint8_t *>(sm.pay);
-  for (int it = blockIdx.x; it < nflag; it += gridDim.x) {
+  // each CTA's first item by its index, every later one from a counter, so that the CTAs whose
+  // items were cheap take more
+  for (int it = blockIdx.x; it < nflag;) {
     const uint2 item = ws.fb[it];
     const int cpass = MODE == MODE_EVERY ? (int)(item.x >> 27) : 0;
     const int64_t b = MODE == MODE_EVERY ? (int64_t)(item.x & ((1u << 27) - 1u)) : (int64_t)item.x;
@@ -1589,7 +1592,9 @@ __device__ __forceinline__ void rescore_by_cta(const EncArgs &a, const EncWs &ws
     }
     for (int i = threadIdx.x; i < BB; i += blockDim.x) payb[i] = pbytes[i];
     if (a.wb && wid == 0) write_back_bytes<F, TIn>(a, tab, b, lane, pbytes, d);
+    if (threadIdx.x == 0) sm.nextit = (int)gridDim.x + atomicAdd(&ws.hdr[2], 1);
     __syncthreads();  // the payload bytes are reused by the next item
+    it = sm.nextit;
   }
 }
 
@@ -1614,7 +1619,8 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
   // an item is (block, flagged vectors); every-choice payloads: (block | choice << 27, flagged
   // vectors), re-decided as a fixed-choice block in that choice's payload
   constexpr bool kFixedLike = MODE == MODE_FIXED || MODE == MODE_EVERY;
-  for (int it = blockIdx.x * kRsWarps + wid; it < nflag; it += gridDim.x * kRsWarps) {
+  // each warp's first item by its index, every later one from a counter
+  for (int it = blockIdx.x * kRsWarps + wid; it < nflag;) {
    const uint2 item = ws.fb[it];
    {
     const int cpass = MODE == MODE_EVERY ? (int)(item.x >> 27) : 0;
@@ -1824,6 +1830,9 @@ __device__ __forceinline__ void rescore_by_warp(const EncArgs &a, const EncWs &w
     if (a.wb) write_back_bytes<F, TIn>(a, tab, b, lane, pbytes, d);
     __syncwarp();
    }
+   int nx = 0;
+   if (lane == 0) nx = (int)gridDim.x * kRsWarps + atomicAdd(&ws.hdr[2], 1);
+   it = __shfl_sync(0xffffffffu, nx, 0);
   }
 }
 
