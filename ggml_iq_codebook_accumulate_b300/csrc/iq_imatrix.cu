@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
                                                      int32_t *__restrict__ status) {
   __shared__ uint32_t bm[1024][kMaxSub / 32];   // expert x row bitmap of the sub-tile
   __shared__ int cnt[1024 + 1], off[1024 + 1];
+  __shared__ int wtot[8];                        // the scan's warp totals (256 threads)
   // the accumulate kernel may be scheduled now: it waits for this grid's completion itself
   asm volatile("griddepcontrol.launch_dependents;");
   const int words = sub / 32;
@@ -238,27 +239,33 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
   const int rows = (int)max((int64_t)0, min((int64_t)sub, rend - r0));
   for (int i = threadIdx.x; i < E * words; i += blockDim.x) bm[i / words][i % words] = 0u;
   __syncthreads();
-  // a warp takes one slot of 32 consecutive rows at a time; the lanes holding the same expert set
-  // their bits with one atomic (the rows of a 32-row group are one bitmap word)
+  // a unit is one slot of 32 consecutive rows; the lanes holding the same expert set their bits
+  // with one atomic (the rows of a 32-row group are one bitmap word).  A bit that is already set
+  // is the same (row, expert) from another slot: a repeated id, which the bitmap counts once.  A
+  // warp loads the ids of up to 8 of its units before it sets their bits.
   int st = 0;
-  const int lane = threadIdx.x & 31, groups = (rows + 31) / 32;
-  for (int idx = threadIdx.x >> 5; idx < groups * top_k; idx += blockDim.x >> 5) {
-    const int g = idx % groups, a = idx / groups, r = g * 32 + lane;
-    int e = -1;
-    if (r < rows) {
-      const int32_t *row = ids + (r0 + r) * top_k;
-      e = row[a];
-      if (e < 0 || e >= E) {
-        st |= IQ_STATUS_BAD_EXPERT_ID;
-        e = -1;
-      } else {
-        bool dup = false;
-        for (int b = 0; b < a; b++) dup |= (row[b] == e);
-        if (dup) { st |= IQ_STATUS_DUP_EXPERT_ID; e = -1; }
-      }
+  const int lane = threadIdx.x & 31, groups = (rows + 31) / 32, nunits = groups * top_k;
+  const int nw = blockDim.x >> 5;
+  for (int u0 = threadIdx.x >> 5; u0 < nunits; u0 += 8 * nw) {
+    int ev[8];
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int idx = u0 + j * nw, g = idx % groups, a = idx / groups, r = g * 32 + lane;
+      ev[j] = idx < nunits && r < rows ? ids[(r0 + r) * top_k + a] : 0;
     }
-    const unsigned same = __match_any_sync(0xffffffffu, e);
-    if (e >= 0 && lane == __ffs(same) - 1) atomicOr(&bm[e][g], same);
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+      const int idx = u0 + j * nw;
+      if (idx >= nunits) break;  // the same in every lane
+      const int g = idx % groups;
+      const bool in = g * 32 + lane < rows;
+      int e = ev[j];
+      if (in && (e < 0 || e >= E)) st |= IQ_STATUS_BAD_EXPERT_ID;
+      if (!in || e < 0 || e >= E) e = -1;
+      const unsigned same = __match_any_sync(0xffffffffu, e);
+      if (e >= 0 && lane == __ffs(same) - 1 && (atomicOr(&bm[e][g], same) & same))
+        st |= IQ_STATUS_DUP_EXPERT_ID;
+    }
   }
   if (st && status) atomicOr(status, st);
   __syncthreads();
@@ -268,19 +275,29 @@ __global__ void __launch_bounds__(256) imatrix_route(const int32_t *__restrict__
     cnt[e] = c;
   }
   __syncthreads();
-  if (threadIdx.x < 32) {   // exclusive scan of the padded run lengths over experts (warp 0)
-    const int lane = threadIdx.x;
-    int run = 0;
-    for (int base = 0; base < E; base += 32) {
-      const int v = base + lane < E ? (cnt[base + lane] + 3) & ~3 : 0;
-      int incl = v;
+  {  // exclusive scan of the padded run lengths over experts: 4 consecutive experts a thread
+     // (256 x 4 >= 1024 >= E), a warp scan of the threads' sums, then the warps' totals
+    const int e0 = threadIdx.x * 4, warp = threadIdx.x >> 5;
+    int v[4], tsum = 0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (base + lane < E) off[base + lane] = run + incl - v;
-      run += __shfl_sync(0xffffffffu, incl, 31);
+    for (int j = 0; j < 4; j++) {
+      v[j] = e0 + j < E ? (cnt[e0 + j] + 3) & ~3 : 0;
+      tsum += v[j];
+    }
+    int incl = tsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) wtot[warp] = incl;
+    __syncthreads();
+    int p = incl - tsum;
+    for (int w = 0; w < warp; w++) p += wtot[w];
+#pragma unroll
+    for (int j = 0; j < 4; j++) {
+      if (e0 + j < E) off[e0 + j] = p;
+      p += v[j];
     }
   }
   __syncthreads();
