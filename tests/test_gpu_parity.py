@@ -138,6 +138,7 @@ def test_imatrix_status_and_sets():
     ids = np.tile(np.array([[0, 1]], np.int32), (64, 1))
     ids[3] = [0, 9]
     ids[5] = [1, 1]
+    ids[6] = [-1, 2]
     ref_s, ref_c, ref_st = oracle.imatrix_accumulate(x, ids, 4)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     s2, cn = api.imatrix_accumulate(torch.from_numpy(x).to(DEV), torch.from_numpy(ids).to(DEV), 4, status=st)
@@ -337,18 +338,23 @@ def test_zero_importance_vectors_tie_exactly(fmt, mode):
 
 
 @pytest.mark.parametrize("fmt", FORMATS)
-def test_zero_importance_vectors_many_flagged_blocks(fmt):
+@pytest.mark.parametrize("mode", ["searched", "fixed"])
+def test_zero_importance_vectors_many_flagged_blocks(fmt, mode):
     # every row's first vector has importance 0, so all 3072 rows' first blocks are flagged: more
     # items than resident warps, so each warp re-decides its own items; the tied vectors overflow
     # its candidate list, the other flagged groups fit it
+    info = oracle.format_info(fmt)
     store, wv = synth.as_dtype(synth.weight_t4(3072, 512, seed=24), "bf16")
     imp = (np.abs(np.random.default_rng(25).standard_normal(512)) + 0.1).astype(np.float32)
     imp[0:8] = 0; imp[300:304] = 0
     grid = synth.grid(fmt)
-    p_orc, st_orc = oracle.encode(fmt, wv, grid, importance=imp)
+    ch = None
+    if mode == "fixed":
+        ch = np.random.default_rng(26).integers(0, info["num_choices"], (3072 * 2, info["groups"])).astype(np.uint8)
+    p_orc, st_orc = oracle.encode(fmt, wv, grid, importance=imp, choices=ch)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
     p = api.encode(fmt, dev_tensor(store, "bf16"), torch.from_numpy(grid).to(DEV), importance=torch.from_numpy(imp).to(DEV),
-                   status=st)
+                   choices=None if ch is None else torch.from_numpy(ch).to(DEV), status=st)
     assert int(st.item()) == st_orc == 0
     assert np.array_equal(host(p), p_orc)
 
